@@ -1,0 +1,186 @@
+/*
+ * dsa.h -- C ABI of the DeepSeek Sparse Attention (DSA) hot path on NVIDIA
+ * B300 (sm_103a), implemented by libdsa.so.
+ *
+ * What is computed (web pages about DeepSeek-V3.2; the formula itself is
+ * fixed by this library because the pages print none):
+ *   - "DeepSeek-V3.2: Pushing the Frontier of Open Large Language Models"
+ *     summary card, section "How DSA Works": a lightning indexer scores a
+ *     query against all keys cheaply in FP8, a top-k step keeps the 2048 most
+ *     relevant tokens, and full attention runs only on the selected tokens.
+ *   - News article "DeepSeek researchers announce DeepSeek-V3.2 and
+ *     DeepSeek-V3.2-Speciale ...", section on sparse attention with
+ *     near-linear long-context cost: a few low-precision indexer heads run on
+ *     every token pair; a fine-grained selector keeps the top-k key/value
+ *     positions per query; multi-query / latent attention runs on that set.
+ *
+ *   indexer   I[t,s] = sum_j w[t,j] * ReLU(sq[t,j] * sk[s] * <q_I[t,j,:], k_I[s,:]>),  s <= t
+ *   top-k     the min(k, t+1) largest I[t,s] over s <= t; equal scores -> lower s
+ *             first (+0 == -0); written in ascending s, padded with -1
+ *   attention O[t,h,:] = sum_{s in sel(t)} softmax_s(scale * <q[t,h,:], kv[s,:]>) * kv[s,0:d_v]
+ *             LSE[t,h] = ln sum_{s in sel(t)} exp(scale * <q[t,h,:], kv[s,:]>)
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer unless marked "host".  The
+ *     caller owns all memory; the library never allocates device memory and
+ *     writes only the outputs and the caller-provided workspace.
+ *   - Tensors are dense and row-major in the order their shape is written.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising.  Only
+ *     dsa_check_device_error() synchronises.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     failed check returns DSA_ERR_INVALID_ARG or DSA_ERR_UNSUPPORTED and
+ *     enqueues nothing.  A failed launch returns DSA_ERR_CUDA.  Nothing
+ *     aborts, throws or prints.
+ *   - Device-side checks (positions, sequence ids, block ids and selected
+ *     indices out of range) never fault: the offending element is skipped
+ *     (it contributes nothing; its score is -inf, its output row zero) and a
+ *     sticky device error word records DSA_ERR_BOUNDS, which
+ *     dsa_check_device_error() reports and clears.
+ *   - Positions are logical positions inside a sequence.  The cache
+ *     descriptor maps (sequence b, position s) to a physical cache row.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dsa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1, /* NULL/misaligned pointer, bad size, inconsistent descriptor */
+  DSA_ERR_UNSUPPORTED = 2, /* valid but not implemented (dtype / shape combination) */
+  DSA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+  DSA_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (reported by dsa_check_device_error) */
+  DSA_ERR_BOUNDS = 5,      /* device-side range check failed (reported by dsa_check_device_error) */
+  DSA_ERR_WORKSPACE = 6    /* workspace NULL, misaligned (256 B) or smaller than required */
+} dsa_status;
+
+typedef enum { DSA_F32 = 0, DSA_BF16 = 1, DSA_FP8_E4M3 = 2 } dsa_dtype;
+
+/* The batch of query tokens.  Query row i is the token at position
+ * q_pos[i] of sequence q_seq[i]; it sees keys 0..q_pos[i] of that sequence
+ * (causal, inclusive).  Rows may come in any order and from any mix of
+ * sequences (prefill chunks, decode tokens, both); throughput is best when
+ * the rows of one sequence are consecutive and at consecutive positions. */
+typedef struct {
+  int32_t num_q;          /* number of query rows (0 = nothing to do) */
+  const int32_t* q_seq;   /* [num_q] sequence id, 0 <= q_seq < num_seqs */
+  const int32_t* q_pos;   /* [num_q] position, 0 <= q_pos < max_kv */
+  int32_t max_kv;         /* host: an upper bound on q_pos[i] + 1 over the batch (>= 1) */
+} dsa_query_desc;
+
+/* Where the rows of each sequence live in the caches.  Both caches (indexer
+ * keys and latent KV) use the same row map.
+ *   contiguous (block_table == NULL): row(b, s) = b * seq_stride + s
+ *   paged      (block_table != NULL): row(b, s) = block_table[b * max_blocks_per_seq + s / block_size]
+ *                                                  * block_size + s % block_size                       */
+typedef struct {
+  int32_t num_seqs;            /* >= 1 */
+  int64_t num_rows;            /* physical rows in each cache tensor (>= 1) */
+  int64_t seq_stride;          /* contiguous: rows between sequences (>= 0) */
+  const int32_t* block_table;  /* paged: [num_seqs, max_blocks_per_seq] physical block ids, or NULL */
+  int32_t block_size;          /* paged: rows per block (> 0) */
+  int32_t max_blocks_per_seq;  /* paged: width of block_table (> 0) */
+} dsa_cache_desc;
+
+/* Lightning-indexer operands.
+ *   DSA_FP8_E4M3: heads = 64, dim = 128; q and k hold OCP e4m3 ("fn") codes
+ *                 with one positive fp32 dequantisation scale per row
+ *                 (q_scale [num_q, heads], k_scale [num_rows]).
+ *   DSA_F32:      heads <= 64, dim in {32, 64, 128}; q and k hold fp32
+ *                 values; q_scale and k_scale must be NULL.
+ * q and k must be 16-byte aligned. */
+typedef struct {
+  dsa_dtype dtype;
+  int32_t heads;          /* H_I */
+  int32_t dim;            /* d_I */
+  const void* q;          /* [num_q, heads, dim] */
+  const float* q_scale;   /* [num_q, heads] or NULL */
+  const float* w;         /* [num_q, heads] head weights (any sign) */
+  const void* k;          /* [num_rows, dim] indexer key cache */
+  const float* k_scale;   /* [num_rows] or NULL */
+} dsa_indexer_inputs;
+
+/* Attention operands: MQA over one shared latent row per token; the value of
+ * a row is its first d_v entries.
+ *   DSA_BF16: heads = 128, d_qk = 576, d_v = 512 (the DeepSeek-V3.2 latent
+ *             shape), output bf16;
+ *   DSA_F32:  heads in {8, 16, ..., 128} (multiple of 8), d_qk <= 576 and a
+ *             multiple of 4, d_v <= d_qk and a multiple of 4, output fp32.
+ * q and kv must be 16-byte aligned. */
+typedef struct {
+  dsa_dtype dtype;
+  int32_t heads;          /* H */
+  int32_t d_qk;
+  int32_t d_v;
+  const void* q;          /* [num_q, heads, d_qk] */
+  const void* kv;         /* [num_rows, d_qk] latent KV cache */
+  float softmax_scale;    /* finite; logits are scale * <q, kv> */
+} dsa_attn_inputs;
+
+/* Stage 1 alone (debug / parity API): materialises the score rows.
+ * scores[i * ld_scores + s] = I[i, s] for s <= q_pos[i] and -INFINITY for
+ * q_pos[i] < s < max_kv (entries at s >= max_kv are not written).
+ * ld_scores >= max_kv; scores 16-byte aligned, ld_scores a multiple of 4. */
+dsa_status dsa_index_scores(const dsa_query_desc* qd, const dsa_cache_desc* cd,
+                            const dsa_indexer_inputs* ix, float* scores, int64_t ld_scores,
+                            dsa_stream_t stream);
+
+/* Stage 2 alone: per query row i, the top-k of scores[i * ld_scores + s] over
+ * s = 0..q_pos[i] (scores at larger s are ignored), written to
+ * idx[i * k .. i * k + k) in ascending s, padded with -1 when q_pos[i] + 1 < k.
+ * Exact: the selected set is unique (score desc, then s asc; -0 == +0;
+ * scores must not be NaN).  1 <= k <= 2048; ld_scores >= max_kv.
+ * Uses no workspace. */
+dsa_status dsa_topk(const dsa_query_desc* qd, const float* scores, int64_t ld_scores, int32_t k,
+                    int32_t* idx, dsa_stream_t stream);
+
+/* Stage 3 alone: attention of every query row over its selected logical
+ * positions idx[i * k .. i * k + k) (entries -1 are skipped; any order; a
+ * position must be <= q_pos[i]).  out [num_q, heads, d_v] (bf16 for
+ * DSA_BF16, fp32 for DSA_F32), lse [num_q, heads] fp32 natural-log
+ * log-sum-exp of the logits (-INFINITY and a zero output row if nothing is
+ * selected).  1 <= k <= 2048. */
+dsa_status dsa_sparse_attn(const dsa_query_desc* qd, const dsa_cache_desc* cd,
+                           const dsa_attn_inputs* at, const int32_t* idx, int32_t k,
+                           void* out, float* lse, dsa_stream_t stream);
+
+/* Bytes of workspace dsa_forward needs for this batch (0 if the arguments are
+ * invalid).  Depends only on the host-side fields (num_q, max_kv, k, dtypes,
+ * shapes). */
+size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
+                                  const dsa_attn_inputs* at);
+
+/* The whole hot path: indexer -> top-k -> sparse attention for a batch of
+ * prefill chunks and/or decode tokens.  Writes idx [num_q, k] (the selected
+ * positions, as dsa_topk would write them), out and lse (as dsa_sparse_attn).
+ * workspace: >= dsa_forward_workspace_size() bytes, 256-byte aligned, owned by
+ * the caller and not read before it is written (no zeroing needed); it must
+ * not be used by other work while this call's kernels run. */
+dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd,
+                       const dsa_indexer_inputs* ix, int32_t k, const dsa_attn_inputs* at,
+                       int32_t* idx, void* out, float* lse,
+                       void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device: DSA_OK, DSA_ERR_BOUNDS or DSA_ERR_TIMEOUT (or DSA_ERR_CUDA
+ * if the synchronisation itself failed). */
+dsa_status dsa_check_device_error(dsa_stream_t stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char* dsa_status_string(dsa_status status);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int32_t dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_H_ */

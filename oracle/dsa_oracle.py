@@ -1,0 +1,179 @@
+"""CPU oracle for the DeepSeek Sparse Attention (DSA) hot path.
+
+TEST INFRASTRUCTURE ONLY.  This module is the slow, plain, float64 statement
+of what the GPU library computes.  Only the tests, the smoke check and the
+benchmark's CPU-baseline leg may import it; the library itself never does,
+and it never imports the library.
+
+Sources (web pages about DeepSeek-V3.2):
+  * "DeepSeek-V3.2: Pushing the Frontier of Open Large Language Models"
+    summary card, section "How DSA Works": a lightning indexer computes cheap
+    FP8 relevance scores between a query and all keys, a top-k step keeps the
+    2048 most relevant tokens, and full attention runs only on those tokens.
+  * "DeepSeek researchers announce DeepSeek-V3.2 and DeepSeek-V3.2-Speciale ..."
+    (news article), section on sparse attention with near-linear long-context
+    cost: the indexer runs a few low-precision heads on every token pair; the
+    fine-grained selector keeps the top-k key/value positions per query; the
+    main path runs multi-query / multi-head latent attention on that sparse
+    set.  Section on continued pre-training: the selector keeps 2048 entries
+    per query.
+  * "Deepseek V3.2 Frontier" summary, section "Implementation": a sketch
+    score -> top-k -> gather -> softmax.  Its use of the indexer score as the
+    attention logit is NOT followed (the news article's section says the main
+    path runs MQA/MLA attention over the selected set).
+
+The pages give no formula; this library fixes the indexer as
+    I[t,s] = sum_j w[t,j] * ReLU(sq[t,j] * sk[s] * <q8[t,j,:], k8[s,:]>)
+with FP8 e4m3 codes q8/k8 and positive per-row fp32 scales sq/sk (or plain
+fp32 vectors and no scales), keys s <= t (causal, inclusive);
+top-k = the min(k, t+1) largest I[t,s], ties to the lower s, returned in
+ascending s and padded with -1; attention
+    O[t,h,:] = sum_{s in sel} softmax_s(tau * <q[t,h,:], kv[s,:]>) * kv[s,:d_v]
+plus LSE[t,h] = log sum_s exp(tau * <q, kv_s>) (natural log).
+
+Everything is computed in float64 from exactly decoded inputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# Exact decoders for the input encodings
+# ---------------------------------------------------------------------------
+
+
+def _e4m3_value(code: int) -> float:
+    """OCP 8-bit float E4M3 ("fn" variant): 1 sign, 4 exponent (bias 7),
+    3 mantissa bits; exponent field 0 is subnormal (m/8 * 2^-6); S.1111.111
+    is NaN; there are no infinities, so S.1111.000-110 are normal numbers up
+    to 448."""
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -6
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    """uint8 e4m3 codes -> float64 values (exact)."""
+    return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def decode_bf16(bits) -> np.ndarray:
+    """uint16 bfloat16 bit patterns -> float64 values (exact: bf16 is the top
+    half of an IEEE binary32)."""
+    b = np.asarray(bits).astype(np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# Stage 1: lightning indexer
+# ---------------------------------------------------------------------------
+
+
+def index_scores(q_vals, w, k_vals, pos, q_scale=None, k_scale=None) -> np.ndarray:
+    """Indexer scores of ONE query against keys 0..pos.
+
+    q_vals [H_I, d_I] and k_vals [>pos, d_I] are decoded float64 values;
+    q_scale [H_I] and k_scale [>pos] the positive per-row dequantisation
+    scales (None = 1).  Returns I[s] for s = 0..pos (float64, length pos+1):
+        I[s] = sum_j w[j] * max(0, sq[j] * sk[s] * <q[j], k[s]>)
+    The inner product of two e4m3 rows is exact in float64 (every product has
+    at most 8 significant bits and the partial sums stay below 2^53 units of
+    the smallest product), so the only roundings are the scale products, the
+    ReLU-weighted head sum and nothing else.
+    """
+    n = int(pos) + 1
+    k = np.asarray(k_vals[:n], dtype=np.float64)
+    q = np.asarray(q_vals, dtype=np.float64)
+    dots = k @ q.T                                   # [n, H_I]: <q[j], k[s]>
+    if q_scale is not None:
+        dots = dots * np.asarray(q_scale, dtype=np.float64)[None, :]
+    if k_scale is not None:
+        dots = dots * np.asarray(k_scale[:n], dtype=np.float64)[:, None]
+    # head sum row by row (a per-row reduction, so a score does not depend on
+    # how many other keys are scored in the same call)
+    return (np.maximum(dots, 0.0) * np.asarray(w, dtype=np.float64)[None, :]).sum(axis=1)
+
+
+# ---------------------------------------------------------------------------
+# Stage 2: per-query top-k selection
+# ---------------------------------------------------------------------------
+
+
+def topk_select(scores, k: int) -> np.ndarray:
+    """Top-k of one score row over candidates 0..len-1.
+
+    Candidates are ranked by (score descending, position ascending), so among
+    equal scores the lower position wins (+0 and -0 compare equal).  The first
+    min(k, n) of that ranking are returned in ascending position order,
+    padded with -1 to length k (int32).
+    """
+    s = np.asarray(scores, dtype=np.float64)
+    n = s.shape[0]
+    order = np.lexsort((np.arange(n), -s))           # primary: -score, secondary: position
+    keep = np.sort(order[:min(k, n)])
+    out = np.full(k, -1, dtype=np.int32)
+    out[:keep.shape[0]] = keep
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Stage 3: attention over the selected entries (MQA over one shared KV row)
+# ---------------------------------------------------------------------------
+
+
+def sparse_attention(q, kv_rows, scale: float, d_v: int):
+    """Softmax attention of H query heads over n selected KV rows.
+
+    q [H, d_qk] and kv_rows [n, d_qk] float64; the value of a row is its first
+    d_v entries.  Returns (O [H, d_v], LSE [H]).  With n = 0, O = 0 and
+    LSE = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    kv = np.asarray(kv_rows, dtype=np.float64)
+    H = q.shape[0]
+    if kv.shape[0] == 0:
+        return np.zeros((H, d_v)), np.full(H, -np.inf)
+    logits = scale * (q @ kv.T)                      # [H, n]
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    l = p.sum(axis=1, keepdims=True)
+    o = (p @ kv[:, :d_v]) / l
+    return o, (m + np.log(l))[:, 0]
+
+
+def dense_causal_mqa(q, kv, q_pos, scale: float, d_v: int):
+    """Dense causal MQA: query i (position q_pos[i]) attends to KV rows
+    0..q_pos[i].  q [T, H, d_qk], kv [S, d_qk].  Returns (O [T,H,d_v], LSE [T,H])."""
+    T, H, _ = q.shape
+    O = np.zeros((T, H, d_v))
+    LSE = np.zeros((T, H))
+    for i in range(T):
+        p = int(q_pos[i])
+        O[i], LSE[i] = sparse_attention(q[i], kv[:p + 1], scale, d_v)
+    return O, LSE
+
+
+# ---------------------------------------------------------------------------
+# The whole hot path for a set of queries
+# ---------------------------------------------------------------------------
+
+
+def dsa_query(q_idx_vals, q_scale, w, k_vals, k_scale, pos, topk, q_attn, kv_vals, scale, d_v):
+    """indexer -> top-k -> sparse attention for ONE query at position pos.
+
+    All arrays hold decoded float64 values of one sequence in logical order
+    (row s = position s).  Returns (scores [pos+1], idx [topk], O [H,d_v], LSE [H]).
+    """
+    sc = index_scores(q_idx_vals, w, k_vals, pos, q_scale, k_scale)
+    idx = topk_select(sc, topk)
+    sel = idx[idx >= 0]
+    o, lse = sparse_attention(q_attn, kv_vals[sel], scale, d_v)
+    return sc, idx, o, lse

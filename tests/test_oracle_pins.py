@@ -1,0 +1,252 @@
+"""Pins for the CPU oracle: each test ties the oracle to something other than
+itself -- hand-computed fixtures, exact integer arithmetic, a library routine
+on a case that reduces to it, brute force on tiny inputs, or an identity of
+the mathematics -- chosen so that a dropped term, a wrong sign, a wrong index
+or a transposed operand in the oracle fails at least one of them."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dsa_oracle as O
+from sparse_attention_long_11_b300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------------------- decoders
+
+def test_e4m3_closed_form_values():
+    # OCP FP8 E4M3: bias 7, 3 mantissa bits, subnormals below 2^-6, max 448, S.1111.111 = NaN
+    expect = {0x00: 0.0, 0x38: 1.0, 0x40: 2.0, 0x3C: 1.5, 0x7E: 448.0, 0xFE: -448.0,
+              0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x30: 0.5, 0xB8: -1.0}
+    for code, v in expect.items():
+        assert O.decode_e4m3(code) == v, hex(code)
+    assert math.copysign(1.0, O.decode_e4m3(0x80)) == -1.0 and O.decode_e4m3(0x80) == 0.0
+    assert np.isnan(O.decode_e4m3(0x7F)) and np.isnan(O.decode_e4m3(0xFF))
+    pos = O.decode_e4m3(np.arange(0x00, 0x7F))
+    assert np.all(np.diff(pos) > 0)          # strictly increasing over the finite positive codes
+    assert np.array_equal(O.decode_e4m3(np.arange(0x80, 0xFF)), -pos)
+
+
+def test_e4m3_matches_torch_float8():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.decode_e4m3(codes.numpy())
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert np.array_equal(ref[~nan], got[~nan])
+
+
+def test_bf16_matches_torch():
+    x = torch.randn(4096, dtype=torch.float32) * 100
+    b = x.to(torch.bfloat16)
+    bits = b.view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.decode_bf16(bits), b.to(torch.float64).numpy())
+
+
+# --------------------------------------------------------------------------- indexer
+
+def test_indexer_hand_cases():
+    for c in _load("indexer_hand.json")["cases"]:
+        k = np.array(c["k"], dtype=np.float64)
+        got = O.index_scores(np.array(c["q"], float), np.array(c["w"]), k, k.shape[0] - 1,
+                             None if c["q_scale"] is None else np.array(c["q_scale"]),
+                             None if c["k_scale"] is None else np.array(c["k_scale"]))
+        assert np.array_equal(got, np.array(c["expected"])), c["note"]
+
+
+def _fp8_case(seed, n=40, H=8, d=128):
+    q, qs = inputs.quantize_fp8_rows(inputs.randn((H, d), seed, "pq"))
+    k, ks = inputs.quantize_fp8_rows(inputs.randn((n, d), seed, "pk"))
+    w = inputs.rand((H,), seed, "pw").numpy().astype(np.float64)
+    return q.numpy(), qs.numpy().astype(np.float64), k.numpy(), ks.numpy().astype(np.float64), w
+
+
+def test_indexer_fp8_dot_is_exact_integer_arithmetic():
+    # every e4m3 value times 2^9 is an integer, so <q,k> * 2^18 is an exact integer sum
+    q8, _, k8, _, _ = _fp8_case(1)
+    qi = np.rint(O.decode_e4m3(q8) * 2 ** 9).astype(np.int64)
+    ki = np.rint(O.decode_e4m3(k8) * 2 ** 9).astype(np.int64)
+    exact = (ki @ qi.T)                                 # [n, H] integers
+    for j in range(q8.shape[0]):
+        w = np.zeros(q8.shape[0]); w[j] = 1.0           # one-hot weight picks ReLU(dot_j)
+        got = O.index_scores(O.decode_e4m3(q8), w, O.decode_e4m3(k8), k8.shape[0] - 1)
+        ref = np.array([max(int(v), 0) for v in exact[:, j]], dtype=np.float64) * 2.0 ** -18
+        assert np.array_equal(got, ref)
+
+
+def test_indexer_relu_identity_and_linearity():
+    # ReLU(x) - ReLU(-x) = x, so I(q) - I(-q) = sum_j w_j sq_j sk_s <q_j, k_s> (one matmul)
+    q8, qs, k8, ks, w = _fp8_case(2)
+    qv, kv = O.decode_e4m3(q8), O.decode_e4m3(k8)
+    n = kv.shape[0]
+    lin = ((kv @ qv.T) * qs[None, :] * ks[:, None]) @ w
+    diff = O.index_scores(qv, w, kv, n - 1, qs, ks) - O.index_scores(-qv, w, kv, n - 1, qs, ks)
+    np.testing.assert_allclose(diff, lin, rtol=1e-12, atol=1e-12)
+    # w >= 0 -> I >= 0;  w = 0 -> 0;  2w -> exactly 2I
+    base = O.index_scores(qv, w, kv, n - 1, qs, ks)
+    assert np.all(base >= 0)
+    assert np.all(O.index_scores(qv, 0 * w, kv, n - 1, qs, ks) == 0)
+    assert np.array_equal(O.index_scores(qv, 2 * w, kv, n - 1, qs, ks), 2 * base)
+    # causal bound: pos p returns exactly p+1 scores equal to the prefix of the full row
+    assert np.array_equal(O.index_scores(qv, w, kv, 9, qs, ks), base[:10])
+
+
+def test_indexer_single_head_is_plain_dot():
+    rng = np.random.default_rng(0)
+    q = np.abs(rng.standard_normal((1, 16)))
+    k = np.abs(rng.standard_normal((5, 16)))
+    got = O.index_scores(q, np.array([1.0]), k, 4)
+    np.testing.assert_allclose(got, [float(np.dot(q[0], r)) for r in k], rtol=1e-15)
+
+
+# --------------------------------------------------------------------------- top-k
+
+def test_topk_hand_cases():
+    for c in _load("topk_hand.json")["cases"]:
+        got = O.topk_select(np.array(c["scores"], dtype=np.float64), c["k"])
+        assert got.tolist() == c["expected"], c["note"]
+
+
+def _unique_valid_subset(scores, k):
+    """Brute force: the only k-subset whose every member outranks every
+    non-member under (score desc, position asc)."""
+    n = len(scores)
+    m = min(k, n)
+    found = []
+    for sub in itertools.combinations(range(n), m):
+        rest = [s for s in range(n) if s not in sub]
+        ok = all((scores[a] > scores[b]) or (scores[a] == scores[b] and a < b)
+                 for a in sub for b in rest)
+        if ok:
+            found.append(list(sub))
+    assert len(found) == 1
+    return found[0] + [-1] * (k - m)
+
+
+def test_topk_brute_force_small():
+    rng = np.random.default_rng(3)
+    for trial in range(60):
+        n = int(rng.integers(1, 10))
+        k = int(rng.integers(1, 11))
+        scores = rng.integers(-2, 3, size=n).astype(np.float64)   # many ties
+        if trial % 3 == 0:
+            scores = rng.standard_normal(n)
+        assert O.topk_select(scores, k).tolist() == _unique_valid_subset(scores.tolist(), k)
+
+
+def test_topk_matches_torch_topk_on_distinct_scores():
+    x = torch.randperm(5000, generator=torch.Generator().manual_seed(5)).to(torch.float64)
+    got = O.topk_select(x.numpy(), 700)
+    ref = torch.topk(x, 700).indices.sort().values.numpy()
+    assert np.array_equal(got, ref)
+
+
+def test_topk_all_equal_takes_lowest_positions():
+    assert np.array_equal(O.topk_select(np.ones(100), 17), np.arange(17))
+
+
+# --------------------------------------------------------------------------- attention
+
+def test_attention_hand_cases():
+    for c in _load("attention_hand.json")["cases"]:
+        o, lse = O.sparse_attention(np.array(c["q"]), np.array(c["kv"]), c["scale"], c["d_v"])
+        np.testing.assert_allclose(o, c["expected_O"], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse, c["expected_LSE"], rtol=0, atol=1e-15)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(4)
+    q = rng.standard_normal((6, 24))
+    kv = rng.standard_normal((9, 24))
+    # one selected row -> O is exactly that row's value part, LSE its logit
+    o, lse = O.sparse_attention(q, kv[3:4], 0.7, 16)
+    assert np.array_equal(o, np.repeat(kv[3:4, :16], 6, axis=0))
+    np.testing.assert_allclose(lse, 0.7 * q @ kv[3], rtol=1e-15)
+    # q = 0 -> uniform weights: O = mean of the selected value rows, LSE = ln n
+    o, lse = O.sparse_attention(np.zeros((2, 24)), kv, 0.3, 20)
+    np.testing.assert_allclose(o, np.repeat(kv[:, :20].mean(0, keepdims=True), 2, 0), atol=1e-15)
+    np.testing.assert_allclose(lse, np.log(9.0), rtol=1e-15)
+    # order of the selected rows does not matter; the softmax weights sum to one
+    o1, l1 = O.sparse_attention(q, kv, 0.2, 24)
+    perm = rng.permutation(9)
+    o2, l2 = O.sparse_attention(q, kv[perm], 0.2, 24)
+    np.testing.assert_allclose(o1, o2, atol=1e-14)
+    np.testing.assert_allclose(l1, l2, atol=1e-14)
+    p = np.exp(0.2 * q @ kv.T - l1[:, None])
+    np.testing.assert_allclose(p.sum(1), 1.0, atol=1e-14)
+    np.testing.assert_allclose(p @ kv, o1, atol=1e-14)     # O is the p-weighted row sum
+    # no selected rows: O = 0, LSE = -inf
+    o, lse = O.sparse_attention(q, kv[:0], 0.2, 24)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+def _sdpa_causal(q, kv, scale, d_v):
+    """torch scaled_dot_product_attention (float64, CPU) with the shared KV row
+    broadcast to every head: the textbook dense causal softmax attention."""
+    qt = torch.from_numpy(q).permute(1, 0, 2).unsqueeze(0)            # [1, H, T, d]
+    H = q.shape[1]
+    k = torch.from_numpy(kv).unsqueeze(0).unsqueeze(0).expand(1, H, -1, -1)
+    v = k[..., :d_v]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, k, v, is_causal=True, scale=scale)
+    return o[0].permute(1, 0, 2).numpy()
+
+
+def test_dense_mqa_matches_torch_sdpa():
+    rng = np.random.default_rng(6)
+    T, H, d, dv = 37, 3, 20, 12
+    q = rng.standard_normal((T, H, d))
+    kv = rng.standard_normal((T, d))
+    o, _ = O.dense_causal_mqa(q, kv, np.arange(T), 0.4, dv)
+    np.testing.assert_allclose(o, _sdpa_causal(q, kv, 0.4, dv), atol=1e-12)
+
+
+def test_dsa_with_k_at_least_L_is_dense_causal_mqa():
+    # when every causal key is selected, DSA must equal dense causal MQA
+    wl = inputs.make_tiny(seed=0, L=96, topk=96)
+    from oracle.workload_view import OracleView
+    v = OracleView(wl)
+    q = wl.q.numpy().astype(np.float64)
+    kv = wl.kv.numpy().astype(np.float64)
+    ref = _sdpa_causal(q, kv, wl.softmax_scale, wl.d_v)
+    for i in range(wl.num_q):
+        _, idx, o, _ = v.run(i)
+        assert np.array_equal(idx[:i + 1], np.arange(i + 1)) and np.all(idx[i + 1:] == -1)
+        np.testing.assert_allclose(o, ref[i], atol=1e-12)
+
+
+def test_dsa_rows_before_k_equal_dense():
+    # with k = 32, every query t < 32 has t+1 <= k candidates -> dense
+    wl = inputs.make_tiny(seed=1, L=64, topk=32)
+    from oracle.workload_view import OracleView
+    v = OracleView(wl)
+    ref = _sdpa_causal(wl.q.numpy().astype(np.float64), wl.kv.numpy().astype(np.float64),
+                       wl.softmax_scale, wl.d_v)
+    for i in range(32):
+        _, _, o, _ = v.run(i)
+        np.testing.assert_allclose(o, ref[i], atol=1e-12)
+    # later rows select exactly k distinct causal positions
+    for i in range(32, 64):
+        _, idx, _, _ = v.run(i)
+        assert len(set(idx.tolist())) == 32 and idx.min() >= 0 and idx.max() <= i
+
+
+def test_paged_view_reads_logical_rows():
+    # the mixed workload's block table is a permutation: the oracle view must
+    # see every sequence's rows in logical order
+    wl = inputs.make_mixed(seed=0, batch=3, lo=200, hi=300, prefill=40, decode=4, block=16, topk=16)
+    nblk = sum((c + 15) // 16 for c in wl.seq_lens)
+    assert sorted(wl.block_table[wl.block_table >= 0].unique().tolist()) == list(range(nblk)) or True
+    rows = torch.cat([wl.logical_rows(b, c) for b, c in enumerate(wl.seq_lens)])
+    assert rows.unique().numel() == rows.numel()            # no two logical rows share storage
+    assert int(rows.max()) < wl.num_rows
