@@ -1,0 +1,393 @@
+"""Benchmark of the DSA hot path (lightning indexer -> top-k -> sparse MQA
+attention) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the whole hot path over the long-prefill workload:
+L = 32768 tokens of one sequence, processed as 8 chunks of 4096 queries
+against the full causal prefix (one dsa_forward call per chunk).  Synthetic,
+seeded inputs of the DeepSeek-V3.2 shapes: FP8 indexer with 64 heads x 128,
+k = 2048, 128 attention heads over one 576-wide bf16 latent KV row.  The
+decode workload (64 sequences x 65536 cached rows, one query each) is timed in
+the same run and reported under "decode".
+
+Prints ONE JSON line on rank 0.  Under torchrun each rank runs an
+independent replica on its own GPU (weak scaling, no collective on the data
+path); timing is the max over ranks.
+
+--impl reference times the CPU oracle (float64 numpy, the machine's host cores)
+on a bounded sample of the same workload and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_attention_long_11_b300 import api, inputs  # noqa: E402
+
+METRIC = "DSA tokens/s (prefill 32K; decode B=64@64K ctx) and % of FP8/BF16/HBM roofline"
+FLOP_PER_ATTN_PAIR = 2 * 128 * (576 + 512)        # QK^T + PV per selected (query, key), 128 heads
+FLOP_PER_IDX_PAIR = 2 * 64 * 128                  # per causal (query, key) indexer pair
+BYTES_PER_IDX_KEY = 128 + 4                       # FP8 key row + its scale
+BYTES_PER_ATTN_KEY = 576 * 2                      # gathered bf16 latent row
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"], src="measured")
+    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class Runner:
+    """Outputs, workspace and one full step of dsa_forward over a workload."""
+
+    def __init__(self, wl):
+        self.wl = wl
+        self.prob = api.Problem(wl)
+        dev = wl.q.device
+        self.idx = torch.empty((wl.num_q, wl.topk), dtype=torch.int32, device=dev)
+        self.out = torch.empty((wl.num_q, wl.H, wl.d_v), dtype=self.prob.out_dtype(), device=dev)
+        self.lse = torch.empty((wl.num_q, wl.H), dtype=torch.float32, device=dev)
+        self.calls = []
+        for a, b in wl.chunks:
+            qd, ix, at = self.prob.rows(a, b)
+            self.calls.append((a, b, qd, ix, at))
+        wsb = max(api.dsa_forward_workspace_size(qd, ix, wl.topk, at) for _, _, qd, ix, at in self.calls)
+        self.ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        self.cache = self.prob.cache.desc()
+
+    def step(self):
+        k = self.wl.topk
+        for a, b, qd, ix, at in self.calls:
+            api.dsa_forward(qd, self.cache, ix, k, at, self.idx[a:b], self.out[a:b], self.lse[a:b], self.ws)
+
+
+def _pairs(wl):
+    """Algorithmic work of one step: (indexer causal pairs, selected attention pairs)."""
+    pos = wl.q_pos.to(torch.int64)
+    return int((pos + 1).sum()), int(torch.clamp(pos + 1, max=wl.topk).sum())
+
+
+def _time_steps(r: Runner, steps: int, warmup: int, ws: int, gpu: int):
+    for _ in range(warmup):
+        r.step()
+    torch.cuda.synchronize()
+    cap = 8192
+    api.dsa_profile_start(cap)
+    n0 = api.dsa_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu) as clk:
+        _barrier(ws)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(steps):
+            r.step()
+        e1.record()
+        torch.cuda.synchronize()
+        _barrier(ws)
+    launches = api.dsa_launch_count() - n0
+    api.dsa_profile_stop()
+    recs = api.dsa_profile_read(cap)
+    st = api.dsa_check_device_error()
+    if st != api.DSA_OK:
+        raise RuntimeError(f"device error during bench: {api.status_string(st)}")
+    ms = e0.elapsed_time(e1) / steps
+    per_stage = {}
+    for s, t in recs:
+        d = per_stage.setdefault(api.STAGE_NAMES[s], [0, 0.0])
+        d[0] += 1
+        d[1] += t
+    return ms, per_stage, launches, clk.summary()
+
+
+def _roofline_prefill(wl, per_stage, steps, peaks):
+    """Dominant kernel of the prefill step (by device time) against its roofline."""
+    n_idx, n_attn = _pairs(wl)
+    dom = max(per_stage, key=lambda s: per_stage[s][1])
+    cnt, tot = per_stage[dom]
+    avg_s = tot / cnt / 1e3
+    per_launch_units = {"indexer": n_idx * steps / cnt, "attention": n_attn * steps / cnt,
+                        "topk": n_idx * steps / cnt}[dom]
+    if dom == "attention":
+        achieved = per_launch_units * FLOP_PER_ATTN_PAIR / avg_s / 1e12
+        return {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sus"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sus"], "traffic": None,
+                "peak_src": f"{peaks['src']} bf16 sustained", "avg_launch_ms": tot / cnt, "launches": cnt}
+    if dom == "indexer":
+        # FP8 peak = measured bf16 peak x the nominal fp8/bf16 ratio (2)
+        pk = 2 * peaks["bf16_sus"]
+        achieved = per_launch_units * FLOP_PER_IDX_PAIR / avg_s / 1e12
+        return {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
+                "frac": achieved / pk, "traffic": None, "peak_src": f"{peaks['src']} bf16 sustained x2 (fp8)",
+                "avg_launch_ms": tot / cnt, "launches": cnt}
+    achieved = per_launch_units * 4 / avg_s / 1e9
+    return {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm"], "traffic": None, "peak_src": f"{peaks['src']} hbm",
+            "avg_launch_ms": tot / cnt, "launches": cnt}
+
+
+def _roofline_decode(wl, per_stage, steps, peaks):
+    n_idx, n_attn = _pairs(wl)
+    dom = max(per_stage, key=lambda s: per_stage[s][1])
+    cnt, tot = per_stage[dom]
+    avg_s = tot / cnt / 1e3
+    if dom == "indexer":
+        byts = n_idx * BYTES_PER_IDX_KEY * steps / cnt
+    elif dom == "attention":
+        byts = n_attn * BYTES_PER_ATTN_KEY * steps / cnt
+    else:
+        byts = n_idx * 4 * steps / cnt
+    achieved = byts / avg_s / 1e9
+    return {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm"], "traffic": None, "peak_src": f"{peaks['src']} hbm burst",
+            "avg_launch_ms": tot / cnt, "launches": cnt}
+
+
+def _e2e(wl, steps: int):
+    """Same metric through the public API with host buffers: every step copies
+    the step's inputs from pinned host memory, runs the forward and reads the
+    outputs back.  Returns (tokens/s, h2d bytes, d2h bytes)."""
+    dev = wl.q.device
+    names = ["q_idx", "q_scale", "w", "k_idx", "k_scale", "q", "kv", "q_seq", "q_pos"]
+    host = {n: getattr(wl, n).to("cpu").pin_memory() for n in names}
+    r = Runner(wl)
+    dev_t = {n: getattr(wl, n) for n in names}
+    out_h = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
+    lse_h = torch.empty(r.lse.shape, dtype=r.lse.dtype).pin_memory()
+    idx_h = torch.empty(r.idx.shape, dtype=r.idx.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in (out_h, lse_h, idx_h))
+
+    def one():
+        for n in names:
+            dev_t[n].copy_(host[n], non_blocking=True)
+        r.step()
+        out_h.copy_(r.out, non_blocking=True)
+        lse_h.copy_(r.lse, non_blocking=True)
+        idx_h.copy_(r.idx, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del host, out_h, lse_h, idx_h
+    return wl.num_q / (ms / 1e3), h2d, d2h, ms
+
+
+def _oracle_sample(wl, budget_s: float, max_q: int = 100000):
+    """Runs the CPU oracle on a stratified sample of the workload's queries
+    (evenly spaced positions) until the time budget is spent."""
+    from oracle.workload_view import OracleView
+    import threadpoolctl
+    view = OracleView(wl)
+    nq = wl.num_q
+    order = np.linspace(0, nq - 1, min(nq, 256)).astype(int)
+    t0 = time.perf_counter()
+    done = 0
+    for i in order[:max_q]:
+        view.run(int(i))
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    info = threadpoolctl.threadpool_info()
+    cores = max([d.get("num_threads", 1) for d in info] + [1])
+    return done, dt, cores
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    wl = inputs.make_long(seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
+    budget = 4.0
+    for _ in range(args.warmup):
+        _oracle_sample(wl, 0.5, max_q=2)
+    done_tot, t_tot, cores = 0, 0.0, 1
+    for _ in range(args.steps):
+        d, t, cores = _oracle_sample(wl, budget)
+        done_tot += d
+        t_tot += t
+    val = done_tot / t_tot
+    sample = (f"{done_tot} queries over {args.steps} steps, evenly spaced positions of the L=32768 prefill "
+              f"(~{budget:.0f} s of oracle work per step)")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_tot / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": "long prefill L=32768 (8 chunks x 4096), k=2048",
+                                            "sample": sample},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    peaks = _peaks()
+    api.lib()
+
+    # ---------------- long prefill (the reported workload)
+    wl = inputs.make_long(seed=0, device=dev)
+    r = Runner(wl)
+    ms, per_stage, launches, clocks = _time_steps(r, args.steps, args.warmup, ws, local)
+    ms = _max_over_ranks(ms, ws)
+    tokens = wl.num_q * ws
+    value = tokens / (ms / 1e3)
+    roof = _roofline_prefill(wl, per_stage, args.steps, peaks)
+    stages = {k: {"launches": v[0], "ms_per_step": v[1] / args.steps} for k, v in per_stage.items()}
+    del r
+    torch.cuda.empty_cache()
+    e2e_val, h2d, d2h, e2e_ms = _e2e(wl, args.e2e_steps)
+    e2e_val = e2e_val * ws
+
+    cpu = None
+    if rank == 0 and ws == 1:
+        done, dt, cores = _oracle_sample(wl, args.cpu_budget)
+        cpu = {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{done} queries at evenly spaced positions of the L=32768 prefill, "
+                         f"full oracle path (indexer, top-k, attention) in {dt:.1f} s"}
+    del wl
+    torch.cuda.empty_cache()
+
+    # ---------------- decode batch (second half of the metric)
+    decode = None
+    if not args.no_decode:
+        wd = inputs.make_decode(seed=0, device=dev)
+        rd = Runner(wd)
+        dms, dstage, dl, dclk = _time_steps(rd, max(args.steps, 10), args.warmup, ws, local)
+        dms = _max_over_ranks(dms, ws)
+        decode = {"workload": "decode B=64, ctx 65536 each, k=2048", "value": wd.num_q * ws / (dms / 1e3),
+                  "unit": "tokens/s", "ms_per_step": dms, "gpu_launches": dl,
+                  "stages": {k: {"launches": v[0], "ms_per_step": v[1] / max(args.steps, 10)}
+                             for k, v in dstage.items()},
+                  "roofline": _roofline_decode(wd, dstage, max(args.steps, 10), peaks), "clocks": dclk}
+        del rd, wd
+        torch.cuda.empty_cache()
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "fp8+bf16 (fp32 accumulate)", "data": "synthetic",
+                "config": {"workload": "long prefill L=32768, 8 chunks x 4096 queries, causal, k=2048; "
+                                       "indexer FP8 64x128; attention 128 heads, d_qk 576, d_v 512, bf16",
+                           "global_batch": 1, "seq_len": 32768, "parallelism": f"replicas x{ws}",
+                           "l2": "inputs larger than L2 (q alone is 4.8 GB)"},
+                "roofline": roof, "stages": stages, "gpu_launches": launches, "clocks": clocks,
+                "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "cpu_baseline": cpu, "decode": decode}
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

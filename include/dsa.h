@@ -46,6 +46,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -129,7 +135,7 @@ typedef struct {
  * scores[i * ld_scores + s] = I[i, s] for s <= q_pos[i] and -INFINITY for
  * q_pos[i] < s < max_kv (entries at s >= max_kv are not written).
  * ld_scores >= max_kv; scores 16-byte aligned, ld_scores a multiple of 4. */
-dsa_status dsa_index_scores(const dsa_query_desc* qd, const dsa_cache_desc* cd,
+DSA_API dsa_status dsa_index_scores(const dsa_query_desc* qd, const dsa_cache_desc* cd,
                             const dsa_indexer_inputs* ix, float* scores, int64_t ld_scores,
                             dsa_stream_t stream);
 
@@ -139,7 +145,7 @@ dsa_status dsa_index_scores(const dsa_query_desc* qd, const dsa_cache_desc* cd,
  * Exact: the selected set is unique (score desc, then s asc; -0 == +0;
  * scores must not be NaN).  1 <= k <= 2048; ld_scores >= max_kv.
  * Uses no workspace. */
-dsa_status dsa_topk(const dsa_query_desc* qd, const float* scores, int64_t ld_scores, int32_t k,
+DSA_API dsa_status dsa_topk(const dsa_query_desc* qd, const float* scores, int64_t ld_scores, int32_t k,
                     int32_t* idx, dsa_stream_t stream);
 
 /* Stage 3 alone: attention of every query row over its selected logical
@@ -148,14 +154,14 @@ dsa_status dsa_topk(const dsa_query_desc* qd, const float* scores, int64_t ld_sc
  * DSA_BF16, fp32 for DSA_F32), lse [num_q, heads] fp32 natural-log
  * log-sum-exp of the logits (-INFINITY and a zero output row if nothing is
  * selected).  1 <= k <= 2048. */
-dsa_status dsa_sparse_attn(const dsa_query_desc* qd, const dsa_cache_desc* cd,
+DSA_API dsa_status dsa_sparse_attn(const dsa_query_desc* qd, const dsa_cache_desc* cd,
                            const dsa_attn_inputs* at, const int32_t* idx, int32_t k,
                            void* out, float* lse, dsa_stream_t stream);
 
 /* Bytes of workspace dsa_forward needs for this batch (0 if the arguments are
  * invalid).  Depends only on the host-side fields (num_q, max_kv, k, dtypes,
  * shapes). */
-size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
+DSA_API size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
                                   const dsa_attn_inputs* at);
 
 /* The whole hot path: indexer -> top-k -> sparse attention for a batch of
@@ -164,7 +170,7 @@ size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_indexer_in
  * workspace: >= dsa_forward_workspace_size() bytes, 256-byte aligned, owned by
  * the caller and not read before it is written (no zeroing needed); it must
  * not be used by other work while this call's kernels run. */
-dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd,
+DSA_API dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd,
                        const dsa_indexer_inputs* ix, int32_t k, const dsa_attn_inputs* at,
                        int32_t* idx, void* out, float* lse,
                        void* workspace, size_t workspace_bytes, dsa_stream_t stream);
@@ -172,13 +178,28 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd,
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device: DSA_OK, DSA_ERR_BOUNDS or DSA_ERR_TIMEOUT (or DSA_ERR_CUDA
  * if the synchronisation itself failed). */
-dsa_status dsa_check_device_error(dsa_stream_t stream);
+DSA_API dsa_status dsa_check_device_error(dsa_stream_t stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
-const char* dsa_status_string(dsa_status status);
+DSA_API const char* dsa_status_string(dsa_status status);
+
+/* ---- Measurement aids (host-side state; not thread-safe) ----------------
+ * While a profile is open, every kernel the library launches is bracketed by
+ * a pair of CUDA events recorded on its launch stream, and tagged with its
+ * stage.  dsa_profile_read() waits for the recorded events and returns each
+ * launch's stage and device duration.  Events are created by the library (no
+ * device memory); at most `capacity` launches are recorded. */
+typedef enum { DSA_STAGE_INDEXER = 1, DSA_STAGE_TOPK = 2, DSA_STAGE_ATTN = 3 } dsa_stage;
+DSA_API dsa_status dsa_profile_start(int32_t capacity);
+/* Closes the profile; returns the number of launches recorded. */
+DSA_API int32_t dsa_profile_stop(void);
+/* stage[i] (dsa_stage) and ms[i] for i < min(cap, recorded); *n = that count. */
+DSA_API dsa_status dsa_profile_read(int32_t* stage, float* ms, int32_t cap, int32_t* n);
+/* Kernels launched by this library in this process so far. */
+DSA_API int64_t dsa_launch_count(void);
 
 /* ABI version: major * 10000 + minor * 100 + patch. */
-int32_t dsa_version(void);
+DSA_API int32_t dsa_version(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,298 @@
+// C ABI of the DSA hot path (declared in include/dsa.h): host-side argument
+// validation, the per-device error word, stage dispatch and the fused
+// forward schedule.  Nothing here allocates device memory.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "launch.h"
+
+namespace dsa {
+namespace {
+
+__device__ int g_device_error;   // sticky error word (see flag_error)
+
+// Scores of at most this many bytes are staged per indexer/top-k round of the
+// fused forward, so the staged rows stay resident in the 126 MB L2 between
+// the indexer writing them and the top-k reading them.
+constexpr size_t kStageBytes = size_t(64) << 20;
+constexpr int kMaxTopk = 2048;
+constexpr int kMaxKv = 1 << 22;   // keeps every grid dimension in range
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+dsa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+int* device_error_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+dsa_status check_query(const dsa_query_desc* qd) {
+  if (!qd || qd->num_q < 0) return DSA_ERR_INVALID_ARG;
+  if (qd->num_q == 0) return DSA_OK;
+  if (!qd->q_seq || !qd->q_pos || !aligned(qd->q_seq, 4) || !aligned(qd->q_pos, 4)) return DSA_ERR_INVALID_ARG;
+  if (qd->max_kv < 1 || qd->max_kv > kMaxKv) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+dsa_status check_cache(const dsa_cache_desc* cd, int max_kv) {
+  if (!cd || cd->num_seqs < 1 || cd->num_rows < 1) return DSA_ERR_INVALID_ARG;
+  if (cd->block_table) {
+    if (cd->block_size < 1 || cd->max_blocks_per_seq < 1 || !aligned(cd->block_table, 4)) return DSA_ERR_INVALID_ARG;
+    if ((int64_t)cd->block_size * cd->max_blocks_per_seq < max_kv) return DSA_ERR_INVALID_ARG;
+  } else {
+    if (cd->seq_stride < 0) return DSA_ERR_INVALID_ARG;
+    if (cd->num_seqs > 1 && cd->seq_stride < max_kv) return DSA_ERR_INVALID_ARG;   // sequences would overlap
+  }
+  return DSA_OK;
+}
+
+dsa_status check_indexer(const dsa_indexer_inputs* ix) {
+  if (!ix || !ix->q || !ix->w || !ix->k) return DSA_ERR_INVALID_ARG;
+  if (!aligned(ix->q, 16) || !aligned(ix->k, 16) || !aligned(ix->w, 4)) return DSA_ERR_INVALID_ARG;
+  if (ix->dtype == DSA_FP8_E4M3) {
+    if (!ix->q_scale || !ix->k_scale || !aligned(ix->q_scale, 4) || !aligned(ix->k_scale, 4)) return DSA_ERR_INVALID_ARG;
+    if (ix->heads != 64 || ix->dim != 128) return DSA_ERR_UNSUPPORTED;
+  } else if (ix->dtype == DSA_F32) {
+    if (ix->q_scale || ix->k_scale) return DSA_ERR_INVALID_ARG;
+    if (ix->heads < 1 || ix->heads > 64) return DSA_ERR_UNSUPPORTED;
+    if (ix->dim != 32 && ix->dim != 64 && ix->dim != 128) return DSA_ERR_UNSUPPORTED;
+  } else {
+    return DSA_ERR_UNSUPPORTED;
+  }
+  return DSA_OK;
+}
+
+dsa_status check_attn(const dsa_attn_inputs* at) {
+  if (!at || !at->q || !at->kv) return DSA_ERR_INVALID_ARG;
+  if (!aligned(at->q, 16) || !aligned(at->kv, 16)) return DSA_ERR_INVALID_ARG;
+  if (!std::isfinite(at->softmax_scale)) return DSA_ERR_INVALID_ARG;
+  if (at->dtype == DSA_BF16) {
+    if (at->heads != 128 || at->d_qk != 576 || at->d_v != 512) return DSA_ERR_UNSUPPORTED;
+  } else if (at->dtype == DSA_F32) {
+    if (at->heads < 8 || at->heads > 128 || at->heads % 8) return DSA_ERR_UNSUPPORTED;
+    if (at->d_qk < 4 || at->d_qk > 576 || at->d_qk % 4) return DSA_ERR_UNSUPPORTED;
+    if (at->d_v < 4 || at->d_v > at->d_qk || at->d_v > 512 || at->d_v % 4) return DSA_ERR_UNSUPPORTED;
+  } else {
+    return DSA_ERR_UNSUPPORTED;
+  }
+  return DSA_OK;
+}
+
+#define DSA_TRY(x)                       \
+  do {                                   \
+    dsa_status s_ = (x);                 \
+    if (s_ != DSA_OK) return s_;         \
+  } while (0)
+
+QueryBatch to_batch(const dsa_query_desc* qd) { return QueryBatch{qd->q_seq, qd->q_pos, qd->num_q, qd->max_kv}; }
+
+CacheMap to_map(const dsa_cache_desc* cd) {
+  CacheMap m{};
+  m.num_seqs = cd->num_seqs;
+  m.block_size = cd->block_table ? cd->block_size : 0;
+  m.max_blocks = cd->block_table ? cd->max_blocks_per_seq : 0;
+  m.num_rows = cd->num_rows;
+  m.seq_stride = cd->seq_stride;
+  m.block_table = cd->block_table;
+  return m;
+}
+
+int64_t score_ld(int max_kv) { return ((int64_t)max_kv + 3) & ~int64_t(3); }
+
+int64_t stage_rows(int num_q, int max_kv) {
+  int64_t per = score_ld(max_kv) * (int64_t)sizeof(float);
+  int64_t r = (int64_t)(kStageBytes / per);
+  if (r < 1) r = 1;
+  if (r > num_q) r = num_q;
+  return r;
+}
+
+size_t idx_elem_size(const dsa_indexer_inputs* ix) { return ix->dtype == DSA_FP8_E4M3 ? 1 : 4; }
+
+// ---- launch accounting and the optional per-launch event profile
+std::atomic<int64_t> g_launches{0};
+struct ProfRec {
+  int stage;
+  cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_prof;
+size_t g_prof_n = 0;
+bool g_prof_on = false;
+
+template <typename F>
+cudaError_t launch(int stage, cudaStream_t st, F&& f) {
+  const bool rec = g_prof_on && g_prof_n < g_prof.size();
+  if (rec) {
+    g_prof[g_prof_n].stage = stage;
+    cudaEventRecord(g_prof[g_prof_n].a, st);
+  }
+  cudaError_t e = f();
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (rec) {
+    cudaEventRecord(g_prof[g_prof_n].b, st);
+    ++g_prof_n;
+  }
+  return e;
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+dsa_status dsa_index_scores(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix,
+                            float* scores, int64_t ld_scores, dsa_stream_t stream) {
+  DSA_TRY(check_query(qd));
+  if (qd->num_q == 0) return DSA_OK;
+  DSA_TRY(check_cache(cd, qd->max_kv));
+  DSA_TRY(check_indexer(ix));
+  if (!scores || !aligned(scores, 16) || ld_scores < qd->max_kv || ld_scores % 4) return DSA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return DSA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(launch(DSA_STAGE_INDEXER, st, [&] {
+    return launch_indexer_simt(to_batch(qd), to_map(cd), *ix, scores, ld_scores, err, st);
+  }));
+}
+
+dsa_status dsa_topk(const dsa_query_desc* qd, const float* scores, int64_t ld_scores, int32_t k, int32_t* idx,
+                    dsa_stream_t stream) {
+  DSA_TRY(check_query(qd));
+  if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+  if (qd->num_q == 0) return DSA_OK;
+  if (!scores || !idx || !aligned(scores, 4) || !aligned(idx, 4) || ld_scores < qd->max_kv) return DSA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return DSA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(to_batch(qd), scores, ld_scores, k, idx, err, st); }));
+}
+
+dsa_status dsa_sparse_attn(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_attn_inputs* at,
+                           const int32_t* idx, int32_t k, void* out, float* lse, dsa_stream_t stream) {
+  DSA_TRY(check_query(qd));
+  if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+  if (qd->num_q == 0) return DSA_OK;
+  DSA_TRY(check_cache(cd, qd->max_kv));
+  DSA_TRY(check_attn(at));
+  if (!idx || !out || !lse || !aligned(idx, 4) || !aligned(out, 16) || !aligned(lse, 4)) return DSA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return DSA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] {
+    return launch_attn_simt(to_batch(qd), to_map(cd), *at, idx, k, out, lse, err, st);
+  }));
+}
+
+size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
+                                  const dsa_attn_inputs* at) {
+  if (check_query(qd) != DSA_OK || check_indexer(ix) != DSA_OK || check_attn(at) != DSA_OK) return 0;
+  if (k < 1 || k > kMaxTopk) return 0;
+  if (qd->num_q == 0) return 256;
+  size_t bytes = (size_t)stage_rows(qd->num_q, qd->max_kv) * score_ld(qd->max_kv) * sizeof(float);
+  return (bytes + 255) & ~size_t(255);
+}
+
+dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix, int32_t k,
+                       const dsa_attn_inputs* at, int32_t* idx, void* out, float* lse, void* workspace,
+                       size_t workspace_bytes, dsa_stream_t stream) {
+  DSA_TRY(check_query(qd));
+  if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+  if (qd->num_q == 0) return DSA_OK;
+  DSA_TRY(check_cache(cd, qd->max_kv));
+  DSA_TRY(check_indexer(ix));
+  DSA_TRY(check_attn(at));
+  if (!idx || !out || !lse || !aligned(idx, 4) || !aligned(out, 16) || !aligned(lse, 4)) return DSA_ERR_INVALID_ARG;
+  const size_t need = dsa_forward_workspace_size(qd, ix, k, at);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return DSA_ERR_WORKSPACE;
+  int* err = device_error_ptr();
+  if (!err) return DSA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  const CacheMap cm = to_map(cd);
+  const int64_t ld = score_ld(qd->max_kv);
+  const int64_t rows = stage_rows(qd->num_q, qd->max_kv);
+  float* scores = static_cast<float*>(workspace);
+  const size_t qi_row = (size_t)ix->heads * ix->dim * idx_elem_size(ix);
+  for (int64_t r0 = 0; r0 < qd->num_q; r0 += rows) {
+    const int n = (int)std::min<int64_t>(rows, qd->num_q - r0);
+    QueryBatch qb{qd->q_seq + r0, qd->q_pos + r0, n, qd->max_kv};
+    dsa_indexer_inputs sub = *ix;
+    sub.q = static_cast<const uint8_t*>(ix->q) + r0 * qi_row;
+    sub.w = ix->w + r0 * ix->heads;
+    if (ix->q_scale) sub.q_scale = ix->q_scale + r0 * ix->heads;
+    cudaError_t e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer_simt(qb, cm, sub, scores, ld, err, st); });
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    e = launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(qb, scores, ld, k, idx + r0 * k, err, st); });
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_attn_simt(to_batch(qd), cm, *at, idx, k, out, lse, err, st); }));
+}
+
+dsa_status dsa_check_device_error(dsa_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  return static_cast<dsa_status>(v);
+}
+
+const char* dsa_status_string(dsa_status s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK: success";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG: invalid argument (null/misaligned pointer, bad size or descriptor)";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED: dtype or shape combination not implemented";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA: a CUDA call failed";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT: a bounded device-side wait expired";
+    case DSA_ERR_BOUNDS: return "DSA_ERR_BOUNDS: a device-side range check failed (element skipped)";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+  }
+  return "unknown dsa_status";
+}
+
+int32_t dsa_version(void) { return 100; }
+
+dsa_status dsa_profile_start(int32_t capacity) {
+  if (capacity < 1) return DSA_ERR_INVALID_ARG;
+  while ((int32_t)g_prof.size() < capacity) {
+    ProfRec r{0, nullptr, nullptr};
+    if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return DSA_ERR_CUDA;
+    g_prof.push_back(r);
+  }
+  g_prof_n = 0;
+  g_prof_on = true;
+  return DSA_OK;
+}
+
+int32_t dsa_profile_stop(void) {
+  g_prof_on = false;
+  return (int32_t)g_prof_n;
+}
+
+dsa_status dsa_profile_read(int32_t* stage, float* ms, int32_t cap, int32_t* n) {
+  if (!stage || !ms || !n || cap < 0) return DSA_ERR_INVALID_ARG;
+  const int32_t m = std::min<int32_t>(cap, (int32_t)g_prof_n);
+  for (int32_t i = 0; i < m; ++i) {
+    if (cudaEventSynchronize(g_prof[i].b) != cudaSuccess) return DSA_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, g_prof[i].a, g_prof[i].b) != cudaSuccess) return DSA_ERR_CUDA;
+    stage[i] = g_prof[i].stage;
+    ms[i] = t;
+  }
+  *n = m;
+  return DSA_OK;
+}
+
+int64_t dsa_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

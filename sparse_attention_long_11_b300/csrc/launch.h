@@ -1,0 +1,23 @@
+// Internal host-side launchers of the DSA kernels (not part of the C ABI).
+// Each enqueues one kernel on `stream` and returns the launch status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include "common.cuh"
+
+namespace dsa {
+
+// Lightning indexer, CUDA-core version: any supported dtype/shape.
+cudaError_t launch_indexer_simt(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
+                                float* scores, int64_t ld, int* err, cudaStream_t stream);
+
+// Per-row exact top-k (radix select + ordered compaction).
+cudaError_t launch_topk(const QueryBatch& qb, const float* scores, int64_t ld, int k, int32_t* idx,
+                        int* err, cudaStream_t stream);
+
+// Sparse attention, CUDA-core version: fp32 or bf16 operands, any supported shape.
+cudaError_t launch_attn_simt(const QueryBatch& qb, const CacheMap& cm, const dsa_attn_inputs& at,
+                             const int32_t* idx, int k, void* out, float* lse, int* err,
+                             cudaStream_t stream);
+
+}  // namespace dsa

@@ -266,16 +266,6 @@ def make_mixed(seed=0, device="cpu", batch=8, lo=8192, hi=131072, prefill=8192, 
     rows = total_blocks * block
     nq = q_pos.shape[0]
     q_idx, q_scale, w, k_idx, k_scale = _indexer_fp8(seed, nq, rows, device, "uniform")
-    # chunks: each sequence's prefill run is one call; all decode queries form one call
-    chunks = []
-    r = 0
-    dec_rows = []
-    for b in range(len(lens)):
-        if prefill:
-            chunks.append((r, r + prefill))
-            r += prefill
-        dec_rows.append((r, r + decode))
-        r += decode
     return Workload(
         name="mixed", seed=seed, idx_dtype="fp8", H_I=64, d_I=128,
         q_idx=q_idx, q_scale=q_scale, w=w, k_idx=k_idx, k_scale=k_scale,
@@ -285,7 +275,7 @@ def make_mixed(seed=0, device="cpu", batch=8, lo=8192, hi=131072, prefill=8192, 
         softmax_scale=1.0 / math.sqrt(576),
         q_seq=q_seq, q_pos=q_pos, seq_lens=lens, seq_stride=0,
         block_table=bt.to(device), block_size=block,
-        chunks=[(0, nq)] if not prefill else [(0, nq)])
+        chunks=[(0, nq)])   # the whole mixed batch is one call
 
 
 def make_config(i: int, seed: int = 0, device="cpu") -> Workload:

@@ -1,0 +1,99 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, and its host-side validation rejects bad arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sparse_attention_long_11_b300 import api
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "dsa.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(dsa_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = _declared()
+    assert "dsa_forward" in names and "dsa_topk" in names and len(names) >= 8
+    L = api.lib()
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in api._SIGS, f"binding lacks {n}"
+
+
+def test_status_strings_and_version():
+    for s in range(7):
+        assert api.status_string(s).startswith("DSA_")
+    assert api.status_string(99) == "unknown dsa_status"
+    assert api.dsa_version() >= 100
+
+
+def _fake(addr=0x10000):
+    return ctypes.c_void_p(addr)
+
+
+def _ix(dtype=api.DSA_FP8_E4M3, heads=64, dim=128, scales=True, addr=0x10000):
+    s = addr if scales else None
+    return api.IndexerInputs(dtype, heads, dim, addr, s, addr, addr, s)
+
+
+def _at(dtype=api.DSA_BF16, heads=128, d_qk=576, d_v=512, addr=0x10000):
+    return api.AttnInputs(dtype, heads, d_qk, d_v, addr, addr, 0.04)
+
+
+def test_workspace_size_validation():
+    L = api.lib()
+    qd = api.QueryDesc(16, 0x10000, 0x10000, 4096)
+    ws = L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix()), 2048, ctypes.byref(_at()))
+    assert ws >= 16 * 4096 * 4 and ws % 256 == 0
+    # k out of range, unsupported shapes, bad dtypes -> 0
+    assert L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix()), 4096, ctypes.byref(_at())) == 0
+    assert L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix(heads=32)), 2048, ctypes.byref(_at())) == 0
+    assert L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix()), 2048, ctypes.byref(_at(d_v=256))) == 0
+    # staged scores are bounded (64 MiB) however many queries there are
+    big = api.QueryDesc(1 << 20, 0x10000, 0x10000, 131072)
+    assert L.dsa_forward_workspace_size(ctypes.byref(big), ctypes.byref(_ix()), 2048, ctypes.byref(_at())) <= 64 << 20
+
+
+def test_host_validation_rejects_before_launch():
+    L = api.lib()
+    cd = api.CacheDesc(1, 4096, 4096, None, 0, 0)
+    qd = api.QueryDesc(16, 0x10000, 0x10000, 4096)
+    f = L.dsa_forward
+    args = lambda q=qd, c=cd, ix=_ix(), k=2048, at=_at(), idx=0x10000, ws=0x10000, wsb=1 << 30: (
+        ctypes.byref(q), ctypes.byref(c), ctypes.byref(ix), k, ctypes.byref(at), idx, 0x10000, 0x10000, ws, wsb, None)
+    assert f(*args(k=0)) == api.DSA_ERR_INVALID_ARG
+    assert f(*args(k=2049)) == api.DSA_ERR_INVALID_ARG
+    assert f(*args(idx=None)) == api.DSA_ERR_INVALID_ARG
+    assert f(*args(ix=_ix(scales=False))) == api.DSA_ERR_INVALID_ARG           # fp8 without scales
+    assert f(*args(ix=_ix(addr=0x10004))) == api.DSA_ERR_INVALID_ARG           # misaligned operand
+    assert f(*args(ix=_ix(dtype=api.DSA_BF16))) == api.DSA_ERR_UNSUPPORTED
+    assert f(*args(at=_at(heads=64))) == api.DSA_ERR_UNSUPPORTED
+    assert f(*args(ws=None)) == api.DSA_ERR_WORKSPACE
+    assert f(*args(ws=0x10010)) == api.DSA_ERR_WORKSPACE                      # not 256-byte aligned
+    assert f(*args(wsb=1024)) == api.DSA_ERR_WORKSPACE
+    assert f(*args(q=api.QueryDesc(16, 0x10000, 0x10000, 0))) == api.DSA_ERR_INVALID_ARG
+    assert f(*args(c=api.CacheDesc(2, 4096, 100, None, 0, 0))) == api.DSA_ERR_INVALID_ARG   # overlapping seqs
+    assert f(*args(c=api.CacheDesc(1, 4096, 0, 0x10000, 64, 2))) == api.DSA_ERR_INVALID_ARG  # table too short
+    # an empty batch is a no-op that never touches the device
+    assert f(*args(q=api.QueryDesc(0, None, None, 0))) == api.DSA_OK
+    # stage entry points
+    assert L.dsa_topk(ctypes.byref(qd), 0x10000, 100, 2048, 0x10000, None) == api.DSA_ERR_INVALID_ARG  # ld < max_kv
+    assert L.dsa_topk(ctypes.byref(qd), None, 4096, 2048, 0x10000, None) == api.DSA_ERR_INVALID_ARG
+    assert L.dsa_index_scores(ctypes.byref(qd), ctypes.byref(cd), ctypes.byref(_ix()), 0x10000, 4094,
+                              None) == api.DSA_ERR_INVALID_ARG
+    assert L.dsa_sparse_attn(ctypes.byref(qd), ctypes.byref(cd), ctypes.byref(_at(dtype=7)), 0x10000, 2048,
+                             0x10000, 0x10000, None) == api.DSA_ERR_UNSUPPORTED
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(api, "_lib", None)
+    monkeypatch.setattr(api, "LIB_PATH", str(tmp_path / "libdsa.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        api.lib()

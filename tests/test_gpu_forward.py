@@ -1,0 +1,121 @@
+"""End-to-end parity of dsa_forward (indexer -> top-k -> sparse attention)
+with the CPU oracle, plus GPU-vs-GPU invariants (paged == contiguous,
+chunked == whole, decode row == prefill row, fused == staged).  The
+full-size cases run each workload exactly as the benchmark launches it and
+check a sample of queries the oracle can afford."""
+import numpy as np
+import pytest
+import torch
+
+from oracle.workload_view import OracleView
+from sparse_attention_long_11_b300 import api, inputs
+from dsa_testutil import ATTN_ATOL_BF16, ATTN_ATOL_F32, check_selection, run_forward
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _check_rows(wl, idx, out, lse, rows, atol):
+    view = OracleView(wl)
+    idx = idx.cpu().numpy()
+    swaps = 0
+    for i in rows:
+        want, nswap = check_selection(view, i, idx[i], wl.topk)
+        swaps += nswap
+        if nswap == 0:
+            # same selected set: attention must match the oracle on it
+            ro, rl = view.attention(i, want)
+            o = out[i].float().cpu().numpy()
+            err = np.abs(o - ro).max()
+            assert err <= atol, f"query {i}: max |O - O_ref| = {err}"
+            l = lse[i].cpu().numpy()
+            assert np.abs(l - rl).max() <= 1e-3 * max(1.0, np.abs(rl).max()), f"query {i}: LSE"
+    assert swaps <= max(2, len(rows) // 4), f"{swaps} near-tie swaps in {len(rows)} queries"
+    return swaps
+
+
+def _sample(nq, m, extra=()):
+    return sorted(set(np.linspace(0, nq - 1, m).astype(int).tolist()) | set(extra))
+
+
+def test_forward_tiny_all_queries():
+    wl = inputs.make_tiny(seed=0, device=DEV)
+    idx, out, lse = run_forward(api.Problem(wl))
+    assert api.dsa_check_device_error() == api.DSA_OK
+    _check_rows(wl, idx, out, lse, range(wl.num_q), ATTN_ATOL_F32)
+
+
+def test_forward_fp8_bf16_small():
+    wl = inputs.make_prefill(seed=1, device=DEV, L=2600)      # spans k=2048 and a ragged tail
+    idx, out, lse = run_forward(api.Problem(wl))
+    assert api.dsa_check_device_error() == api.DSA_OK
+    _check_rows(wl, idx, out, lse, _sample(wl.num_q, 40, [2046, 2047, 2048, 2049]), ATTN_ATOL_BF16)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4])
+def test_forward_full_size(cfg):
+    """Full workload sizes, launched as the benchmark launches them."""
+    torch.cuda.empty_cache()
+    wl = inputs.make_config(cfg, seed=0, device=DEV)
+    idx, out, lse = run_forward(api.Problem(wl))
+    assert api.dsa_check_device_error() == api.DSA_OK
+    nq = wl.num_q
+    rows = _sample(nq, 10 if cfg in (1, 3) else 8, [nq - 1])
+    _check_rows(wl, idx, out, lse, rows, ATTN_ATOL_BF16)
+    # properties at every row: causal, ascending, padded exactly where t+1 < k
+    pos = wl.q_pos.to(torch.int64)
+    valid = idx >= 0
+    assert torch.equal(valid.sum(1), torch.clamp(pos + 1, max=wl.topk))
+    assert bool((idx.to(torch.int64) <= pos[:, None]).all())
+    d = idx[:, 1:].to(torch.int64) - idx[:, :-1].to(torch.int64)
+    assert bool(((d > 0) | ~valid[:, 1:]).all())
+    assert bool(torch.isfinite(out.float()).all()) and bool(torch.isfinite(lse).all())
+    del wl, idx, out, lse
+    torch.cuda.empty_cache()
+
+
+# --------------------------------------------------------------------------- invariants (bitwise)
+
+def test_paged_equals_contiguous():
+    wm = inputs.make_mixed(seed=5, device=DEV, batch=3, lo=2200, hi=3000, prefill=200, decode=4, block=64)
+    # the same logical caches laid out contiguously, one sequence after another
+    stride = max(wm.seq_lens)
+    rows = torch.full((wm.num_seqs * stride,), 0, dtype=torch.int64)
+    for b, c in enumerate(wm.seq_lens):
+        rows[b * stride:b * stride + c] = wm.logical_rows(b, c)
+    rows = rows.to(DEV)
+    import dataclasses
+    wc = dataclasses.replace(wm, k_idx=wm.k_idx[rows], k_scale=wm.k_scale[rows], kv=wm.kv[rows],
+                             seq_stride=stride, block_table=None, block_size=0)
+    a = run_forward(api.Problem(wm))
+    b = run_forward(api.Problem(wc))
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_chunked_equals_whole_and_decode_equals_prefill_row():
+    wl = inputs.make_prefill(seed=6, device=DEV, L=3000)
+    whole = run_forward(api.Problem(wl), chunks=[(0, 3000)])
+    chunked = run_forward(api.Problem(wl), chunks=[(0, 1000), (1000, 2100), (2100, 3000)])
+    for x, y in zip(whole, chunked):
+        assert torch.equal(x, y)
+    # decode: rows 2999 and 2500 issued as single-token calls
+    for r in (2999, 2500):
+        one = run_forward(api.Problem(wl), chunks=[(r, r + 1)])
+        for x, y in zip(whole, one):
+            assert torch.equal(x[r], y[r])
+
+
+def test_fused_selection_equals_staged_stages():
+    wl = inputs.make_prefill(seed=7, device=DEV, L=2500)
+    prob = api.Problem(wl)
+    idx, out, lse = run_forward(prob)
+    sc = torch.empty((wl.num_q, 2500), dtype=torch.float32, device=DEV)
+    api.dsa_index_scores(prob.batch.desc(), prob.cache.desc(), prob.ix, sc)
+    idx2 = torch.empty_like(idx)
+    api.dsa_topk(prob.batch.desc(), sc, wl.topk, idx2)
+    assert torch.equal(idx, idx2)
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    api.dsa_sparse_attn(prob.batch.desc(), prob.cache.desc(), prob.at, idx2, wl.topk, out2, lse2)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)

@@ -1,0 +1,166 @@
+"""Stage-by-stage parity of the CUDA path (through the C ABI) with the CPU
+oracle, on identical seeded inputs.  Needs a B300 and the built library."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dsa_oracle as O
+from oracle.workload_view import OracleView
+from sparse_attention_long_11_b300 import api, inputs
+from dsa_testutil import ATTN_ATOL_BF16, ATTN_ATOL_F32, indexer_tolerance
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _scores(prob):
+    wl = prob.wl
+    ld = (wl.max_kv + 3) // 4 * 4
+    sc = torch.empty((wl.num_q, ld), dtype=torch.float32, device=DEV)
+    api.dsa_index_scores(prob.batch.desc(), prob.cache.desc(), prob.ix, sc)
+    assert api.dsa_check_device_error() == api.DSA_OK
+    return sc
+
+
+# --------------------------------------------------------------------------- indexer
+
+@pytest.mark.parametrize("make", [
+    lambda: inputs.make_tiny(seed=0, device=DEV),                                   # fp32, 4 x 64
+    lambda: inputs.make_prefill(seed=1, device=DEV, L=777, topk=2048),               # fp8, ragged tail
+])
+def test_index_scores_match_oracle(make):
+    wl = make()
+    prob = api.Problem(wl)
+    sc = _scores(prob).cpu().numpy()
+    view = OracleView(wl)
+    rows = range(wl.num_q) if wl.num_q <= 256 else sorted(set(np.linspace(0, wl.num_q - 1, 40).astype(int)))
+    for i in rows:
+        tol, ref = indexer_tolerance(view, i)
+        pos = int(view.q_pos[i])
+        got = sc[i, :pos + 1].astype(np.float64)
+        bad = np.abs(got - ref) > tol
+        assert not bad.any(), f"query {i}: {np.flatnonzero(bad)[:5]} got {got[bad][:3]} want {ref[bad][:3]}"
+        assert np.all(np.isneginf(sc[i, pos + 1:wl.max_kv]))
+
+
+def test_index_scores_decode_batch_and_paged():
+    # many sequences, one query each (contiguous), and the same under a paged layout
+    wl = inputs.make_decode(seed=2, device=DEV, batch=5, ctx=1000)
+    view = OracleView(wl)
+    sc = _scores(api.Problem(wl)).cpu().numpy()
+    for i in range(5):
+        tol, ref = indexer_tolerance(view, i)
+        assert np.all(np.abs(sc[i, :1000] - ref) <= tol)
+    wm = inputs.make_mixed(seed=3, device=DEV, batch=3, lo=300, hi=700, prefill=100, decode=5, block=64)
+    view = OracleView(wm)
+    sc = _scores(api.Problem(wm)).cpu().numpy()
+    for i in list(range(0, wm.num_q, 17)) + [wm.num_q - 1]:
+        tol, ref = indexer_tolerance(view, i)
+        pos = int(view.q_pos[i])
+        assert np.all(np.abs(sc[i, :pos + 1] - ref) <= tol), i
+
+
+# --------------------------------------------------------------------------- top-k
+
+@pytest.mark.parametrize("kind", ["normal", "ties", "const"])
+@pytest.mark.parametrize("n,k", [(300, 32), (5000, 2048), (5000, 2047), (3000, 1), (70000, 2048)])
+def test_topk_exact(kind, n, k):
+    nq = 24 if n < 60000 else 4
+    sc = inputs.make_scores(nq, n, seed=n + k, device=DEV, kind=kind)
+    # positions: some rows with fewer than k candidates, the last row full
+    pos = torch.linspace(0, n - 1, nq).round().to(torch.int32)
+    pos[0] = min(k - 1, n - 1)
+    batch = api.Batch(torch.zeros(nq, dtype=torch.int32, device=DEV), pos.to(DEV), n)
+    idx = torch.empty((nq, k), dtype=torch.int32, device=DEV)
+    api.dsa_topk(batch.desc(), sc, k, idx)
+    assert api.dsa_check_device_error() == api.DSA_OK
+    got = idx.cpu().numpy()
+    s_np = sc.cpu().numpy()
+    for i in range(nq):
+        p = int(pos[i])
+        want = O.topk_select(s_np[i, :p + 1], k)
+        assert np.array_equal(got[i], want), f"row {i} pos {p}"
+
+
+def test_topk_ignores_scores_beyond_position():
+    n, k = 4096, 64
+    sc = inputs.make_scores(2, n, seed=9, device=DEV)
+    sc[:, 2000:] = 1e30                      # huge scores after the causal bound must not be picked
+    pos = torch.tensor([1999, 1500], dtype=torch.int32, device=DEV)
+    batch = api.Batch(torch.zeros(2, dtype=torch.int32, device=DEV), pos, n)
+    idx = torch.empty((2, k), dtype=torch.int32, device=DEV)
+    api.dsa_topk(batch.desc(), sc, k, idx)
+    s_np = sc.cpu().numpy()
+    for i, p in enumerate([1999, 1500]):
+        assert np.array_equal(idx[i].cpu().numpy(), O.topk_select(s_np[i, :p + 1], k))
+
+
+# --------------------------------------------------------------------------- attention
+
+def _attn(prob, idx_cpu, k):
+    wl = prob.wl
+    out = torch.empty((wl.num_q, wl.H, wl.d_v), dtype=prob.out_dtype(), device=DEV)
+    lse = torch.empty((wl.num_q, wl.H), dtype=torch.float32, device=DEV)
+    api.dsa_sparse_attn(prob.batch.desc(), prob.cache.desc(), prob.at, idx_cpu.to(DEV), k, out, lse)
+    assert api.dsa_check_device_error() == api.DSA_OK
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("case", ["tiny", "bf16_k2048", "bf16_k100", "paged"])
+def test_sparse_attn_matches_oracle(case):
+    if case == "tiny":
+        wl, k, atol = inputs.make_tiny(seed=4, device=DEV), 32, ATTN_ATOL_F32
+    elif case == "bf16_k2048":
+        wl, k, atol = inputs.make_prefill(seed=5, device=DEV, L=2600), 2048, ATTN_ATOL_BF16
+    elif case == "bf16_k100":
+        wl, k, atol = inputs.make_prefill(seed=6, device=DEV, L=700, topk=100), 100, ATTN_ATOL_BF16
+    else:
+        wl = inputs.make_mixed(seed=7, device=DEV, batch=2, lo=2100, hi=2500, prefill=60, decode=3, block=64)
+        k, atol = 2048, ATTN_ATOL_BF16
+    prob = api.Problem(wl)
+    sel = inputs.random_index_sets(wl.q_pos, k, seed=11)
+    o, lse = _attn(prob, sel, k)
+    view = OracleView(wl)
+    rows = sorted(set(np.linspace(0, wl.num_q - 1, 24).astype(int)) | {0, wl.num_q - 1})
+    for i in rows:
+        ro, rl = view.attention(i, sel[i].numpy())
+        err = np.abs(o[i] - ro).max()
+        assert err <= atol, f"query {i}: max |O - O_ref| = {err}"
+        assert np.abs(lse[i] - rl).max() <= 1e-3 * max(1.0, np.abs(rl).max()), i
+
+
+def test_sparse_attn_skips_padding_and_any_order():
+    wl = inputs.make_tiny(seed=8, device=DEV, L=128, topk=48)
+    prob = api.Problem(wl)
+    sel = inputs.random_index_sets(wl.q_pos, 48, seed=3)
+    o1, l1 = _attn(prob, sel, 48)
+    g = torch.Generator().manual_seed(0)
+    perm = torch.stack([r[torch.randperm(48, generator=g)] for r in sel])   # shuffled, -1s anywhere
+    o2, l2 = _attn(prob, perm, 48)
+    np.testing.assert_allclose(o1, o2, atol=1e-5)
+    np.testing.assert_allclose(l1, l2, atol=1e-5)
+
+
+# --------------------------------------------------------------------------- device-side checks
+
+def test_out_of_range_inputs_are_flagged_not_faulted():
+    wl = inputs.make_tiny(seed=9, device=DEV, L=64, topk=16)
+    prob = api.Problem(wl)
+    assert api.dsa_check_device_error() == api.DSA_OK
+    bad_pos = wl.q_pos.clone()
+    bad_pos[5] = 1000                                   # beyond max_kv
+    batch = api.Batch(wl.q_seq, bad_pos, wl.max_kv)
+    sc = torch.zeros((wl.num_q, 64), dtype=torch.float32, device=DEV)
+    api.dsa_index_scores(batch.desc(), prob.cache.desc(), prob.ix, sc)
+    assert api.dsa_check_device_error() == api.DSA_ERR_BOUNDS
+    assert api.dsa_check_device_error() == api.DSA_OK          # the word was cleared
+    assert torch.isneginf(sc[5]).all()
+    sel = inputs.random_index_sets(wl.q_pos, 16, seed=1)
+    sel[7, 0] = 50                                      # later than the query's position (7)
+    out = torch.empty((wl.num_q, wl.H, wl.d_v), dtype=torch.float32, device=DEV)
+    lse = torch.empty((wl.num_q, wl.H), dtype=torch.float32, device=DEV)
+    api.dsa_sparse_attn(prob.batch.desc(), prob.cache.desc(), prob.at, sel.to(DEV), 16, out, lse)
+    assert api.dsa_check_device_error() == api.DSA_ERR_BOUNDS
+    assert torch.isfinite(out).all()
