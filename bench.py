@@ -272,7 +272,6 @@ def _oracle_sample(wl, budget_s: float, max_q: int = 100000):
     """Runs the CPU oracle on a stratified sample of the workload's queries
     (evenly spaced positions) until the time budget is spent."""
     from oracle.workload_view import OracleView
-    import threadpoolctl
     view = OracleView(wl)
     nq = wl.num_q
     order = np.linspace(0, nq - 1, min(nq, 256)).astype(int)
@@ -284,9 +283,20 @@ def _oracle_sample(wl, budget_s: float, max_q: int = 100000):
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
-    info = threadpoolctl.threadpool_info()
-    cores = max([d.get("num_threads", 1) for d in info] + [1])
-    return done, dt, cores
+    return done, dt, _blas_threads()
+
+
+def _blas_threads() -> int:
+    """Threads the oracle's BLAS uses (numpy matmul), else the usable cores."""
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = max([d.get("num_threads", 0) for d in info if d.get("user_api") == "blas"] + [0])
+        if n:
+            return n
+    except ImportError:
+        pass
+    return len(os.sched_getaffinity(0))
 
 
 def run_reference(args, ws, rank):
