@@ -175,6 +175,36 @@ DSA_API dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* c
                        int32_t* idx, void* out, float* lse,
                        void* workspace, size_t workspace_bytes, dsa_stream_t stream);
 
+/* dsa_forward for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point; it exists for users of
+ * this library.  Some callers cannot call cudaMalloc (or any allocator) when
+ * they run the forward: an inference engine whose memory plan is fixed before
+ * serving starts, a plugin whose host forbids allocation, or a serving loop
+ * that must not let cudaMalloc synchronise the device.  This variant takes no
+ * workspace.  Its scratch (the staged score rows) lives in one file-scope
+ * device array of DSA_NOALLOC_SCRATCH_BYTES bytes inside libdsa.so; every GPU
+ * that loads the library holds that array until the process exits.
+ *
+ *   - Arguments and outputs are exactly those of dsa_forward without the
+ *     workspace; results equal dsa_forward's.
+ *   - max_kv above DSA_NOALLOC_MAX_KV (one staged score row must fit in the
+ *     array) is rejected with DSA_ERR_UNSUPPORTED before anything runs.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents.  Nothing in it needs to start at zero (each staged row
+ *     is written before it is read).  Calls whose kernels overlap on the GPU
+ *     (different streams, or different host threads) race on the array:
+ *     order them on one stream or with events.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine. */
+#define DSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define DSA_NOALLOC_MAX_KV 2097152
+DSA_API dsa_status dsa_forward_noalloc(const dsa_query_desc* qd, const dsa_cache_desc* cd,
+                                       const dsa_indexer_inputs* ix, int32_t k, const dsa_attn_inputs* at,
+                                       int32_t* idx, void* out, float* lse, dsa_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the device error word of the
  * current device: DSA_OK, DSA_ERR_BOUNDS or DSA_ERR_TIMEOUT (or DSA_ERR_CUDA
  * if the synchronisation itself failed). */

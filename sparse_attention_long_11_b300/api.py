@@ -64,6 +64,9 @@ _SIGS = {
     "dsa_forward": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(IndexerInputs), ctypes.c_int32,
                                    _P(AttnInputs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "dsa_forward_noalloc": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(IndexerInputs), ctypes.c_int32,
+                                           _P(AttnInputs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.c_void_p]),
     "dsa_check_device_error": (ctypes.c_int, [ctypes.c_void_p]),
     "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dsa_version": (ctypes.c_int32, []),
@@ -180,6 +183,19 @@ def dsa_forward(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, k: int, a
     _check(lib().dsa_forward(ctypes.byref(batch), ctypes.byref(cache), ctypes.byref(ix), k, ctypes.byref(at),
                              _ptr(idx), _ptr(out), _ptr(lse), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream)), "dsa_forward")
+
+
+NOALLOC_MAX_KV = 2097152
+
+
+def dsa_forward_noalloc(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, k: int, at: AttnInputs,
+                        idx: torch.Tensor, out: torch.Tensor, lse: torch.Tensor, stream=None) -> None:
+    """dsa_forward without a workspace, for callers that cannot allocate device
+    memory: the library keeps its scratch in a fixed device array (calls that
+    overlap on the GPU race on it; max_kv <= NOALLOC_MAX_KV)."""
+    _check(lib().dsa_forward_noalloc(ctypes.byref(batch), ctypes.byref(cache), ctypes.byref(ix), k,
+                                     ctypes.byref(at), _ptr(idx), _ptr(out), _ptr(lse), _stream(stream)),
+           "dsa_forward_noalloc")
 
 
 def dsa_check_device_error(stream=None) -> int:

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "launch.h"
@@ -261,6 +262,78 @@ const char* dsa_status_string(dsa_status s) {
 }
 
 int32_t dsa_version(void) { return 100; }
+
+}  // extern "C"
+
+// ---- dsa_forward_noalloc: the forward with its scratch in a file-scope array
+
+// Staged score rows of dsa_forward_noalloc (the only device memory the library
+// itself owns).  Shared by every call on a device; see dsa.h.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+dsa_status noalloc_scratch(float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return DSA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return DSA_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = static_cast<float*>(g_noalloc_addr[dev]);
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dsa_status dsa_forward_noalloc(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix,
+                               int32_t k, const dsa_attn_inputs* at, int32_t* idx, void* out, float* lse,
+                               dsa_stream_t stream) {
+  DSA_TRY(check_query(qd));
+  if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+  if (qd->num_q == 0) return DSA_OK;
+  if (qd->max_kv > DSA_NOALLOC_MAX_KV) return DSA_ERR_UNSUPPORTED;   // one staged row must fit the array
+  DSA_TRY(check_cache(cd, qd->max_kv));
+  DSA_TRY(check_indexer(ix));
+  DSA_TRY(check_attn(at));
+  if (!idx || !out || !lse || !aligned(idx, 4) || !aligned(out, 16) || !aligned(lse, 4)) return DSA_ERR_INVALID_ARG;
+  float* scores = nullptr;
+  DSA_TRY(noalloc_scratch(&scores));
+  int* err = device_error_ptr();
+  if (!err) return DSA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  const CacheMap cm = to_map(cd);
+  const int64_t ld = score_ld(qd->max_kv);
+  const int64_t rows = std::max<int64_t>(
+      1, std::min<int64_t>(qd->num_q, (int64_t)(DSA_NOALLOC_SCRATCH_BYTES / (ld * sizeof(float)))));
+  const size_t qi_row = (size_t)ix->heads * ix->dim * idx_elem_size(ix);
+  for (int64_t r0 = 0; r0 < qd->num_q; r0 += rows) {
+    const int n = (int)std::min<int64_t>(rows, qd->num_q - r0);
+    QueryBatch qb{qd->q_seq + r0, qd->q_pos + r0, n, qd->max_kv};
+    dsa_indexer_inputs sub = *ix;
+    sub.q = static_cast<const uint8_t*>(ix->q) + r0 * qi_row;
+    sub.w = ix->w + r0 * ix->heads;
+    if (ix->q_scale) sub.q_scale = ix->q_scale + r0 * ix->heads;
+    cudaError_t e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer_simt(qb, cm, sub, scores, ld, err, st); });
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    e = launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(qb, scores, ld, k, idx + r0 * k, err, st); });
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_attn_simt(to_batch(qd), cm, *at, idx, k, out, lse, err, st); }));
+}
 
 dsa_status dsa_profile_start(int32_t capacity) {
   if (capacity < 1) return DSA_ERR_INVALID_ARG;
