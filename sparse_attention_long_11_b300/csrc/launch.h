@@ -20,4 +20,16 @@ cudaError_t launch_attn_simt(const QueryBatch& qb, const CacheMap& cm, const dsa
                              const int32_t* idx, int k, void* out, float* lse, int* err,
                              cudaStream_t stream);
 
+// Sparse attention on tcgen05 tensor cores: bf16, 128 heads, d_qk 576, d_v 512.
+cudaError_t launch_attn_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_attn_inputs& at,
+                           const int32_t* idx, int k, void* out, float* lse, int* err, cudaStream_t stream);
+
+// Stage dispatch: the tensor-core kernel for the bf16 latent shape, the
+// CUDA-core kernel for fp32 operands.
+inline cudaError_t launch_attn(const QueryBatch& qb, const CacheMap& cm, const dsa_attn_inputs& at,
+                               const int32_t* idx, int k, void* out, float* lse, int* err, cudaStream_t stream) {
+  if (at.dtype == DSA_BF16) return launch_attn_tc(qb, cm, at, idx, k, out, lse, err, stream);
+  return launch_attn_simt(qb, cm, at, idx, k, out, lse, err, stream);
+}
+
 }  // namespace dsa
