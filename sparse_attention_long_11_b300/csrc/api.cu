@@ -160,7 +160,7 @@ dsa_status dsa_index_scores(const dsa_query_desc* qd, const dsa_cache_desc* cd, 
   if (!err) return DSA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return cuda_status(launch(DSA_STAGE_INDEXER, st, [&] {
-    return launch_indexer_simt(to_batch(qd), to_map(cd), *ix, scores, ld_scores, err, st);
+    return launch_indexer(to_batch(qd), to_map(cd), *ix, scores, ld_scores, err, st);
   }));
 }
 
@@ -229,7 +229,7 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const
     sub.q = static_cast<const uint8_t*>(ix->q) + r0 * qi_row;
     sub.w = ix->w + r0 * ix->heads;
     if (ix->q_scale) sub.q_scale = ix->q_scale + r0 * ix->heads;
-    cudaError_t e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer_simt(qb, cm, sub, scores, ld, err, st); });
+    cudaError_t e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer(qb, cm, sub, scores, ld, err, st); });
     if (e != cudaSuccess) return DSA_ERR_CUDA;
     e = launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(qb, scores, ld, k, idx + r0 * k, err, st); });
     if (e != cudaSuccess) return DSA_ERR_CUDA;
@@ -327,7 +327,7 @@ dsa_status dsa_forward_noalloc(const dsa_query_desc* qd, const dsa_cache_desc* c
     sub.q = static_cast<const uint8_t*>(ix->q) + r0 * qi_row;
     sub.w = ix->w + r0 * ix->heads;
     if (ix->q_scale) sub.q_scale = ix->q_scale + r0 * ix->heads;
-    cudaError_t e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer_simt(qb, cm, sub, scores, ld, err, st); });
+    cudaError_t e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer(qb, cm, sub, scores, ld, err, st); });
     if (e != cudaSuccess) return DSA_ERR_CUDA;
     e = launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(qb, scores, ld, k, idx + r0 * k, err, st); });
     if (e != cudaSuccess) return DSA_ERR_CUDA;

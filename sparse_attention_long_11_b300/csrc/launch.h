@@ -20,6 +20,18 @@ cudaError_t launch_attn_simt(const QueryBatch& qb, const CacheMap& cm, const dsa
                              const int32_t* idx, int k, void* out, float* lse, int* err,
                              cudaStream_t stream);
 
+// Lightning indexer on tcgen05 tensor cores: FP8 e4m3, 64 heads x 128, contiguous
+// caches or paged caches whose block size is a multiple of 64.
+bool indexer_tc_supported(const CacheMap& cm, const dsa_indexer_inputs& ix);
+cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
+                              float* scores, int64_t ld, int* err, cudaStream_t stream);
+
+inline cudaError_t launch_indexer(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
+                                  float* scores, int64_t ld, int* err, cudaStream_t stream) {
+  if (indexer_tc_supported(cm, ix)) return launch_indexer_tc(qb, cm, ix, scores, ld, err, stream);
+  return launch_indexer_simt(qb, cm, ix, scores, ld, err, stream);
+}
+
 // Sparse attention on tcgen05 tensor cores: bf16, 128 heads, d_qk 576, d_v 512.
 cudaError_t launch_attn_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_attn_inputs& at,
                            const int32_t* idx, int k, void* out, float* lse, int* err, cudaStream_t stream);
