@@ -1,0 +1,41 @@
+"""Runs one DSA workload through dsa_forward a few times, for profilers.
+
+    python -m sparse_attention_long_11_b300.profile_case --workload prefill --reps 2
+
+Workloads: tiny, prefill (L=4096), long (L=32768, 8 chunks), decode
+(64 x 65536), mixed (8 paged sequences).  Exits non-zero on a device error.
+"""
+import argparse
+import sys
+
+import torch
+
+from . import api, inputs
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="prefill", choices=inputs.CONFIG_NAMES)
+    ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--seed", type=int, default=0)
+    a = ap.parse_args()
+    wl = inputs.make_config(inputs.CONFIG_NAMES.index(a.workload), seed=a.seed, device="cuda")
+    prob = api.Problem(wl)
+    idx = torch.empty((wl.num_q, wl.topk), dtype=torch.int32, device="cuda")
+    out = torch.empty((wl.num_q, wl.H, wl.d_v), dtype=prob.out_dtype(), device="cuda")
+    lse = torch.empty((wl.num_q, wl.H), dtype=torch.float32, device="cuda")
+    calls = [(a_, b_) + prob.rows(a_, b_) for a_, b_ in wl.chunks]
+    wsb = max(api.dsa_forward_workspace_size(qd, ix, wl.topk, at) for _, _, qd, ix, at in calls)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    cache = prob.cache.desc()
+    for _ in range(a.reps):
+        for r0, r1, qd, ix, at in calls:
+            api.dsa_forward(qd, cache, ix, wl.topk, at, idx[r0:r1], out[r0:r1], lse[r0:r1], ws)
+    st = api.dsa_check_device_error()
+    print(f"{a.workload}: {wl.num_q} queries x {a.reps} reps, launches={api.dsa_launch_count()}, "
+          f"status={api.status_string(st)}")
+    return 0 if st == api.DSA_OK else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
