@@ -234,7 +234,7 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const
     e = launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(qb, scores, ld, k, idx + r0 * k, err, st); });
     if (e != cudaSuccess) return DSA_ERR_CUDA;
   }
-  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st); }));
+  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
 }
 
 dsa_status dsa_check_device_error(dsa_stream_t stream) {
@@ -332,7 +332,7 @@ dsa_status dsa_forward_noalloc(const dsa_query_desc* qd, const dsa_cache_desc* c
     e = launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(qb, scores, ld, k, idx + r0 * k, err, st); });
     if (e != cudaSuccess) return DSA_ERR_CUDA;
   }
-  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st); }));
+  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
 }
 
 dsa_status dsa_profile_start(int32_t capacity) {

@@ -41,4 +41,20 @@ inline bool make_tmap_rows128(CUtensorMap* m, const void* base, uint64_t rows, u
   return r == CUDA_SUCCESS;
 }
 
+// Row-major bf16 matrix [rows, cols]; boxes of box_rows x box_cols elements
+// (box_cols * 2 bytes = 128 with the 128-byte swizzle, 64 with the 64-byte one).
+inline bool make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                           uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace dsa
