@@ -163,7 +163,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     for (int s = 0; s < 2; ++s) {
       mbar_init(&B.s_full[s], 1);
       mbar_init(&B.s_empty[s], 256);   // the exchange warps and the softmax warps both read S
-      mbar_init(&B.xf[s], 128);        // arrivals of the peer's exchange warps
+      mbar_init(&B.xf[s], 1);          // armed by our softmax thread 0; the peer's st.async credit the bytes
       mbar_init(&B.xe[s], 128);        // arrivals of the peer's softmax warps
     }
     mbar_init(&B.q_full, 129);       // 128 TMEM writers + the rope TMA (with its bytes)
@@ -174,6 +174,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     mbar_init(&B.fin, 1);
     B.abort = 0;
     fence_mbar_init();
+    mbar_arrive_expect_tx(&B.xf[0], kXBytes);   // arm the first phase of both receive tiles
+    mbar_arrive_expect_tx(&B.xf[1], kXBytes);
   }
   if (warp == 12) {
     tmem_alloc(&B.tmem_base, kTmemCols);
@@ -222,9 +224,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         if (!(ok = mbar_wait<true>(&B.xf[b], par, abort))) break;   // the peer's partial is in X[b]
         ATTN_TRACE(0, g, 1, h == 0);
         if (!(ok = mbar_wait(&B.s_full[b], par, abort))) break;
+        ATTN_TRACE(0, g, 6, h == 0);
         tc_fence_after();
         float s[64];
         load_s(tmem + lane_base + kTmemS + b * 64, s);
+        ATTN_TRACE(0, g, 7, h == 0);
         {
           const float4* X4 = reinterpret_cast<const float4*>(sm + kOffX + b * kXBytes);
 #pragma unroll
@@ -239,9 +243,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
             }
           }
         }
+        ATTN_TRACE(1, g, 4, h == 0 && s[0] != 12345.f);   // after the partial read (value dependency)
         tc_fence_before();
         mbar_arrive(&B.s_empty[b]);
-        mbar_arrive_remote(xe_peer[b]);   // X[b] consumed: the peer may write its next tile there
+        ATTN_TRACE(1, g, 5, h == 0);
+        // X[b] consumed (the loads above have returned and their values are in
+        // use): the peer may write its next tile there.  A release-ordered
+        // remote arrive costs ~1.5k clk here; relaxed is enough.
+        mbar_arrive_remote_relaxed(xe_peer[b]);
+        if (h == 0) mbar_arrive_expect_tx(&B.xf[b], kXBytes);   // arm the next phase of this receive tile
         ATTN_TRACE(0, g, 2, h == 0);
 
         uint32_t v_lo, v_hi;
@@ -342,6 +352,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t x_peer = mapa(smem_u32(sm + kOffX), peer);
     const uint32_t xf_peer[2] = {mapa(smem_u32(&B.xf[0]), peer), mapa(smem_u32(&B.xf[1]), peer)};
+    // (the peer arms its xf[b] with the tile's bytes; our st.async credit them)
     uint32_t g = 0;
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
       const QueryInfo qi = query_info(qb, idx, k, i, pv);
@@ -363,9 +374,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         const uint32_t dst = x_peer + b * kXBytes;
 #pragma unroll
         for (int jq = 0; jq < 16; ++jq)
-          st_cluster_v4(dst + (uint32_t)(jq * 128 + h) * 16u,
-                        make_float4(s[4 * jq], s[4 * jq + 1], s[4 * jq + 2], s[4 * jq + 3]));
-        mbar_arrive_remote(xf_peer[b]);
+          st_async_v4(dst + (uint32_t)(jq * 128 + h) * 16u,
+                      make_float4(s[4 * jq], s[4 * jq + 1], s[4 * jq + 2], s[4 * jq + 3]), xf_peer[b]);
         ATTN_TRACE(1, g, 3, h == 0);
       }
       if (!ok) break;

@@ -114,10 +114,24 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
                "f"(v.w)
                : "memory");
 }
+// Asynchronous 16-byte store into another CTA's shared memory; when the data
+// has landed it credits 16 transaction bytes to that CTA's mbarrier
+// `remote_bar` (whose expected bytes the receiver registers).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+               : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster
 // scope: this thread's earlier shared::cluster stores are visible first).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+// Relaxed remote arrive: orders nothing.  For "I have consumed your data"
+// signals whose loads have already returned their values (which the thread
+// has used), so no later write by the peer can affect them.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
