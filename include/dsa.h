@@ -89,7 +89,7 @@ typedef struct {
  *                                                  * block_size + s % block_size                       */
 typedef struct {
   int32_t num_seqs;            /* >= 1 */
-  int64_t num_rows;            /* physical rows in each cache tensor (>= 1) */
+  int64_t num_rows;            /* physical rows in each cache tensor (1 .. 2^31-1) */
   int64_t seq_stride;          /* contiguous: rows between sequences (>= 0) */
   const int32_t* block_table;  /* paged: [num_seqs, max_blocks_per_seq] physical block ids, or NULL */
   int32_t block_size;          /* paged: rows per block (> 0) */

@@ -43,6 +43,7 @@ dsa_status check_query(const dsa_query_desc* qd) {
 
 dsa_status check_cache(const dsa_cache_desc* cd, int max_kv) {
   if (!cd || cd->num_seqs < 1 || cd->num_rows < 1) return DSA_ERR_INVALID_ARG;
+  if (cd->num_rows > INT32_MAX) return DSA_ERR_INVALID_ARG;   // row ids travel as 32-bit values
   if (cd->block_table) {
     if (cd->block_size < 1 || cd->max_blocks_per_seq < 1 || !aligned(cd->block_table, 4)) return DSA_ERR_INVALID_ARG;
     if ((int64_t)cd->block_size * cd->max_blocks_per_seq < max_kv) return DSA_ERR_INVALID_ARG;

@@ -30,9 +30,10 @@
 //     128x64x16 for S and 4 MMAs 128x256x16 for P.V, with V read MN-major
 //     straight out of the gathered K-major latent slots.
 //   * Warp roles per CTA: 0-3 softmax/epilogue (thread = head = TMEM lane),
-//     4-7 score exchange, 8-11 gather (two groups of two warps alternate
-//     tiles; at each query the four warps write Q's latent part into TMEM
-//     and warp 8 loads the rope part with TMA), 12 TMEM owner + MMA issuer.
+//     4-7 score exchange, 8-13 gather (three groups of two warps, group j
+//     fills KV stage j with the tiles g = j mod 3; at each query warps 8-11
+//     write Q's latent part into TMEM and warp 8 loads the rope part with
+//     TMA), 14 TMEM owner + MMA issuer.
 //     Persistent: cluster j handles queries j, j+C, ...
 //   * Lazy rescaling: the running max used for the exponent only moves when
 //     a tile's max exceeds it by more than 8 (a factor 256).
@@ -63,7 +64,7 @@ constexpr uint32_t kOffX = kOffKV + kStages * kKVStageBytes;   // 116 KB
 constexpr uint32_t kOffP = kOffX + 2 * kXBytes;            // 180 KB
 constexpr uint32_t kSmemBytes = kOffP + kPBytes;           // 196 KB
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;         // + alignment slack
-constexpr int kThreads = 416;
+constexpr int kThreads = 480;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 384;  // S buffer b at kTmemS + 64 b
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -177,7 +178,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     mbar_arrive_expect_tx(&B.xf[0], kXBytes);   // arm the first phase of both receive tiles
     mbar_arrive_expect_tx(&B.xf[1], kXBytes);
   }
-  if (warp == 12) {
+  if (warp == 14) {
     tmem_alloc(&B.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -380,11 +381,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       }
       if (!ok) break;
     }
-  } else if (warp < 12) {
+  } else if (warp < 14) {
     // ------------------------------------------------------------ gather (cp.async) + Q (TMA)
-    // Group grp (warps 8+2grp, 9+2grp) fills the stage of the tiles g with
-    // g % 2 == grp; warp wg of the group copies rows 32wg .. 32wg+31.
+    // Group grp (warps 8+2grp, 9+2grp) fills stage grp with the tiles g with
+    // g % 3 == grp; warp wg of the group copies rows 32wg .. 32wg+31.
     const int grp = (warp - 8) >> 1, wg = (warp - 8) & 1;
+    const bool q_writer = warp < 12;                         // warps 8-11 cover the four TMEM lane quadrants
     const int hq = ((warp & 3) << 5) | lane;                 // TMEM lane (head) this thread writes Q for
     const uint32_t q_lane = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t g = 0, qv = 0;
@@ -395,38 +397,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       const int seq = __ldg(qb.q_seq + i);
       const int32_t* irow = idx + (int64_t)i * k;
       // Q of this query: every S MMA of the previous query has completed
-      if (!mbar_wait(&B.q_empty, (qv & 1) ^ 1, abort)) break;
+      if (q_writer && !mbar_wait(&B.q_empty, (qv & 1) ^ 1, abort)) break;
       if (warp == 8 && lane == 0) {
         mbar_arrive_expect_tx(&B.q_full, kQRopeBytes);
         tma_load_2d(sQr, &tm_q_rope, 512 + 32 * crank, i * kH, &B.q_full);
+        if (i + ncl < qb.num_q) tma_prefetch_2d(&tm_q_rope, 512 + 32 * crank, (i + ncl) * kH);
       }
-      {
+      if (q_writer) {
         // latent dims [256c, 256c+256) of head hq -> TMEM columns kTmemQ .. kTmemQ+127
         const uint4* qrow = reinterpret_cast<const uint4*>(q + ((int64_t)i * kH + hq) * kDqk + crank * 256);
         tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint4 v[8];
+        for (int c0 = 0; c0 < 128; c0 += 64) {
+          uint4 v[16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) v[j] = __ldg(qrow + c0 / 4 + j);
-          uint32_t r[2][16];
+          for (int j = 0; j < 16; ++j) v[j] = __ldg(qrow + c0 / 4 + j);
+          uint32_t r[4][16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < 16; ++j) {
             r[j >> 2][4 * (j & 3) + 0] = v[j].x;
             r[j >> 2][4 * (j & 3) + 1] = v[j].y;
             r[j >> 2][4 * (j & 3) + 2] = v[j].z;
             r[j >> 2][4 * (j & 3) + 3] = v[j].w;
           }
-          tmem_st16(tmem + q_lane + kTmemQ + c0, r[0]);
-          tmem_st16(tmem + q_lane + kTmemQ + c0 + 16, r[1]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) tmem_st16(tmem + q_lane + kTmemQ + c0 + 16 * u, r[u]);
         }
         tmem_st_wait();
+        // warm L2 with this thread's row of the next query this cluster handles
+        if (i + ncl < qb.num_q) {
+          const char* nrow = reinterpret_cast<const char*>(q + ((int64_t)(i + ncl) * kH + hq) * kDqk + crank * 256);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) prefetch_l2(nrow + 128 * j);
+        }
         tc_fence_before();
         mbar_arrive(&B.q_full);
       }
       bool ok = true;
       for (int t = 0; t < qi.nt; ++t, ++g) {
-        if ((int)(g & 1) != grp) continue;
+        if ((int)(g % kStages) != grp) continue;
         // row of this lane's entry (loaded before the wait so the latency overlaps it)
         const int e = t * kNK + 32 * wg + lane;
         int s_e = -1;
@@ -435,22 +444,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         const int st = g % kStages;
         if (!(ok = mbar_wait(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
         ATTN_TRACE(2, g, 1, lane == 0 && wg == 0);
-        int64_t row = -1;
-        if (s_e >= 0 && s_e <= qi.pos) row = cache_row(cm, seq, s_e, err);
+        int row = -1;                                         // physical rows fit in 31 bits
+        if (s_e >= 0 && s_e <= qi.pos) row = (int)cache_row(cm, seq, s_e, err);
         else if (s_e != -1) flag_error(err, DSA_ERR_BOUNDS);
         const uint32_t sb = sKV + st * kKVStageBytes;
-#pragma unroll 4
-        for (int ii = 0; ii < 32; ++ii) {
-          const long long r = __shfl_sync(0xffffffffu, (long long)row, ii);
-          const __nv_bfloat16* src = r >= 0 ? kv + r * kDqk + crank * 256 + lane * 8 : kv;
-          cp_async16(sb + (lane >> 3) * kKVSlotBytes + sw128_offset(32 * wg + ii, lane & 7), src, r >= 0 ? 16u : 0u);
-        }
+        const __nv_bfloat16* lat = kv + crank * 256 + lane * 8;
+        // one 32-bit broadcast per row; batches of 16 rows let the shuffles pipeline
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {   // rope halves: 8 rows x 4 chunks per instruction
-          const int ii = it * 8 + (lane >> 2), c = lane & 3;
-          const long long r = __shfl_sync(0xffffffffu, (long long)row, ii);
-          const __nv_bfloat16* src = r >= 0 ? kv + r * kDqk + 512 + 32 * crank + c * 8 : kv;
-          cp_async16(sb + 4 * kKVSlotBytes + sw64_offset(32 * wg + ii, c), src, r >= 0 ? 16u : 0u);
+        for (int b0 = 0; b0 < 32; b0 += 16) {
+          int rr[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) rr[j] = __shfl_sync(0xffffffffu, row, b0 + j);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            cp_async16(sb + (lane >> 3) * kKVSlotBytes + sw128_offset(32 * wg + b0 + j, lane & 7),
+                       rr[j] >= 0 ? lat + (int64_t)rr[j] * kDqk : kv, rr[j] >= 0 ? 16u : 0u);
+        }
+        {
+          const __nv_bfloat16* rope = kv + 512 + 32 * crank + (lane & 3) * 8;
+          int rr[4];
+#pragma unroll
+          for (int it = 0; it < 4; ++it) rr[it] = __shfl_sync(0xffffffffu, row, it * 8 + (lane >> 2));
+#pragma unroll
+          for (int it = 0; it < 4; ++it)   // rope halves: 8 rows x 4 chunks per instruction
+            cp_async16(sb + 4 * kKVSlotBytes + sw64_offset(32 * wg + it * 8 + (lane >> 2), lane & 3),
+                       rr[it] >= 0 ? rope + (int64_t)rr[it] * kDqk : kv, rr[it] >= 0 ? 16u : 0u);
         }
         cp_async_commit();
         cp_async_wait_all();
@@ -462,7 +480,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       ++qv;
     }
   } else {
-    // ------------------------------------------------------------ MMA issue (warp 12, lane 0 issues)
+    // ------------------------------------------------------------ MMA issue (warp 14, lane 0 issues)
     const uint32_t id_s = idesc_bf16(128, kNK, false);
     const uint32_t id_pv = idesc_bf16(128, 256, true);
     uint32_t g = 0, qv = 0;
@@ -529,7 +547,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
   tc_fence_before();
   __syncthreads();
   cluster_sync();       // the peer no longer reads or writes our shared memory
-  if (warp == 12) {
+  if (warp == 14) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
