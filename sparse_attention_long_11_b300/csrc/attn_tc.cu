@@ -61,8 +61,8 @@ constexpr int kStages = 3;
 constexpr uint32_t kOffQRope = 0;
 constexpr uint32_t kOffKV = kOffQRope + kQRopeBytes;       // 8 KB
 constexpr uint32_t kOffX = kOffKV + kStages * kKVStageBytes;   // 116 KB
-constexpr uint32_t kOffP = kOffX + 2 * kXBytes;            // 180 KB
-constexpr uint32_t kSmemBytes = kOffP + kPBytes;           // 196 KB
+constexpr uint32_t kOffP = kOffX + 2 * kXBytes;            // 180 KB: P[0], P[1]
+constexpr uint32_t kSmemBytes = kOffP + 2 * kPBytes;       // 212 KB (P double buffered)
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;         // + alignment slack
 constexpr int kThreads = 480;
 constexpr uint32_t kTmemCols = 512;
@@ -86,7 +86,8 @@ __device__ long long g_attn_trace[4][512][8];
 
 struct Bars {
   uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], s_empty[2], xf[2], xe[2];
-  uint64_t q_full, q_empty, p_full, pv_done, o_empty, fin;
+  uint64_t p_full[2], pv_done[2];
+  uint64_t q_full, q_empty, o_empty, fin;
   uint32_t tmem_base;
   int abort;
 };
@@ -169,8 +170,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     }
     mbar_init(&B.q_full, 129);       // 128 TMEM writers + the rope TMA (with its bytes)
     mbar_init(&B.q_empty, 1);
-    mbar_init(&B.p_full, 128);
-    mbar_init(&B.pv_done, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&B.p_full[s], 128);
+      mbar_init(&B.pv_done[s], 1);
+    }
     mbar_init(&B.o_empty, 128);
     mbar_init(&B.fin, 1);
     B.abort = 0;
@@ -296,8 +299,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         l = l * alpha + psum;
         ATTN_TRACE(0, g, 3, h == 0);
 
-        // P.V of the previous tile must be done before P and O are touched
-        if (!(ok = mbar_wait(&B.pv_done, (g & 1) ^ 1, abort))) break;
+        // P[b] is free once the P.V of tile g-2 is done; rescaling O also
+        // needs the P.V of tile g-1 to be done
+        if (!(ok = mbar_wait(&B.pv_done[b], par ^ 1, abort))) break;
+        if (rescale && t > 0 && !(ok = mbar_wait(&B.pv_done[b ^ 1], ((g - 1) >> 1) & 1, abort))) break;
         ATTN_TRACE(0, g, 4, h == 0);
         tc_fence_after();
         if (rescale && t > 0) {
@@ -312,19 +317,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
           }
           tmem_st_wait();
         }
-        uint8_t* prow = sm + kOffP;
+        uint8_t* prow = sm + kOffP + b * kPBytes;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
           *reinterpret_cast<uint4*>(prow + sw128_offset(h, cc)) =
               make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&B.p_full);
+        mbar_arrive(&B.p_full[b]);
         ATTN_TRACE(0, g, 5, h == 0);
       }
       if (!ok) break;
       // epilogue: O row of this head, normalised, bf16
-      if (!mbar_wait(&B.pv_done, (g - 1) & 1, abort)) break;
+      if (!mbar_wait(&B.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort)) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* o4 = reinterpret_cast<uint4*>(orow);
@@ -481,22 +486,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     }
   } else {
     // ------------------------------------------------------------ MMA issue (warp 14, lane 0 issues)
+    // Order per tile g: the score MMAs of g, then the P.V of g-1 as soon as
+    // its P is ready (issuing score tiles further ahead was measured slower:
+    // they queue in front of the P.V in the tensor pipe).
     const uint32_t id_s = idesc_bf16(128, kNK, false);
     const uint32_t id_pv = idesc_bf16(128, 256, true);
     uint32_t g = 0, qv = 0;
     auto issue_pv = [&](uint32_t gp, int tp) -> bool {
       ATTN_TRACE(3, gp, 3, lane == 0);
-      if (!mbar_wait(&B.p_full, gp & 1, abort)) return false;
+      if (!mbar_wait(&B.p_full[gp & 1], (gp >> 1) & 1, abort)) return false;
       ATTN_TRACE(3, gp, 4, lane == 0);
       if (tp == 0 && !mbar_wait(&B.o_empty, (qv & 1) ^ 1, abort)) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t skv = sKV + (gp % kStages) * kKVStageBytes;
+        const uint32_t sp = sP + (gp & 1) * kPBytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16(tmem + kTmemO, sdesc(sP + kk * 32, 16, 1024), sdesc(skv + kk * 2048, kKVSlotBytes, 1024), id_pv,
+          mma_bf16(tmem + kTmemO, sdesc(sp + kk * 32, 16, 1024), sdesc(skv + kk * 2048, kKVSlotBytes, 1024), id_pv,
                    (tp > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&B.pv_done);
+        mma_commit(&B.pv_done[gp & 1]);
         mma_commit(&B.kv_empty[gp % kStages]);
       }
       __syncwarp();
