@@ -210,6 +210,11 @@ DSA_API dsa_status dsa_forward_noalloc(const dsa_query_desc* qd, const dsa_cache
  * if the synchronisation itself failed). */
 DSA_API dsa_status dsa_check_device_error(dsa_stream_t stream);
 
+/* Text of the last CUDA error this library saw on the calling host thread
+ * (which call, the CUDA error name and message), or "no error".  The pointer
+ * stays valid until the next call into the library on this thread. */
+DSA_API const char* dsa_last_error_detail(void);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 DSA_API const char* dsa_status_string(dsa_status status);
 

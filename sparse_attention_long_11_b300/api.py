@@ -69,6 +69,7 @@ _SIGS = {
                                            ctypes.c_void_p]),
     "dsa_check_device_error": (ctypes.c_int, [ctypes.c_void_p]),
     "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "dsa_last_error_detail": (ctypes.c_char_p, []),
     "dsa_version": (ctypes.c_int32, []),
     "dsa_profile_start": (ctypes.c_int, [ctypes.c_int32]),
     "dsa_profile_stop": (ctypes.c_int32, []),
@@ -104,7 +105,8 @@ def status_string(status: int) -> str:
 
 def _check(status: int, where: str) -> None:
     if status != DSA_OK:
-        raise DSAError(status, where)
+        detail = lib().dsa_last_error_detail().decode() if status == DSA_ERR_CUDA else ""
+        raise DSAError(status, where + (f" [{detail}]" if detail else ""))
 
 
 def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:

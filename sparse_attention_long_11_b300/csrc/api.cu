@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -127,6 +128,13 @@ std::vector<ProfRec> g_prof;
 size_t g_prof_n = 0;
 bool g_prof_on = false;
 
+thread_local char g_last_detail[256] = "no error";
+
+void note_cuda_error(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return;
+  snprintf(g_last_detail, sizeof(g_last_detail), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
 template <typename F>
 cudaError_t launch(int stage, cudaStream_t st, F&& f) {
   const bool rec = g_prof_on && g_prof_n < g_prof.size();
@@ -135,6 +143,8 @@ cudaError_t launch(int stage, cudaStream_t st, F&& f) {
     cudaEventRecord(g_prof[g_prof_n].a, st);
   }
   cudaError_t e = f();
+  note_cuda_error(e, stage == DSA_STAGE_INDEXER ? "indexer launch" : stage == DSA_STAGE_TOPK ? "top-k launch"
+                                                                                           : "attention launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (rec) {
     cudaEventRecord(g_prof[g_prof_n].b, st);
@@ -238,8 +248,14 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const
   return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
 }
 
+const char* dsa_last_error_detail(void) { return g_last_detail; }
+
 dsa_status dsa_check_device_error(dsa_stream_t stream) {
-  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+  const cudaError_t se = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (se != cudaSuccess) {
+    note_cuda_error(se, "stream synchronize");
+    return DSA_ERR_CUDA;
+  }
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
   if (v != 0) {

@@ -18,8 +18,15 @@ def main() -> int:
     ap.add_argument("--workload", default="prefill", choices=inputs.CONFIG_NAMES)
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--q-rows", default=None,
+                    help="a:b -- keep only query positions [a, b) of the prefill workloads (all keys stay cached)")
     a = ap.parse_args()
-    wl = inputs.make_config(inputs.CONFIG_NAMES.index(a.workload), seed=a.seed, device="cuda")
+    if a.q_rows and a.workload in ("prefill", "long"):
+        r0, r1 = (int(x) for x in a.q_rows.split(":"))
+        L = 4096 if a.workload == "prefill" else 32768
+        wl = inputs.make_prefill(seed=a.seed, device="cuda", L=L, name=a.workload, q_rows=(r0, r1))
+    else:
+        wl = inputs.make_config(inputs.CONFIG_NAMES.index(a.workload), seed=a.seed, device="cuda")
     prob = api.Problem(wl)
     idx = torch.empty((wl.num_q, wl.topk), dtype=torch.int32, device="cuda")
     out = torch.empty((wl.num_q, wl.H, wl.d_v), dtype=prob.out_dtype(), device="cuda")
