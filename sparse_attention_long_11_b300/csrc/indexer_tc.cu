@@ -147,6 +147,22 @@ __device__ __forceinline__ int item_tiles(const Group& G, int c, int ch) {
   return n;
 }
 
+// Two fp32 lanes in one 64-bit register pair, and d = a * b + c on both
+// lanes with one packed instruction (PTX fma.rn.f32x2).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
   const long long t0 = clock64();
@@ -334,7 +350,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               const int qq = uni ? uq : G.pass_q[p];
               const uint32_t col = 256 * b + (uni ? qq * 64 : 0);
               const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][qq]);
-              float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+              // packed fp32x2 FMAs: two heads per instruction, four independent accumulators
+              uint64_t a2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
               for (int half = 0; half < 2; ++half) {
                 uint32_t r[2][16];
@@ -346,14 +363,24 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                   for (int j4 = 0; j4 < 4; ++j4) {
                     const float4 wv = wq4[half * 8 + cc * 4 + j4];
-                    const int ai = (j4 & 1) * 4;
-                    a[ai + 0] = fmaf(wv.x, fmaxf(__uint_as_float(r[cc][4 * j4 + 0]), 0.f), a[ai + 0]);
-                    a[ai + 1] = fmaf(wv.y, fmaxf(__uint_as_float(r[cc][4 * j4 + 1]), 0.f), a[ai + 1]);
-                    a[ai + 2] = fmaf(wv.z, fmaxf(__uint_as_float(r[cc][4 * j4 + 2]), 0.f), a[ai + 2]);
-                    a[ai + 3] = fmaf(wv.w, fmaxf(__uint_as_float(r[cc][4 * j4 + 3]), 0.f), a[ai + 3]);
+                    const int ai = (j4 & 1) * 2;
+                    a2[ai] = ffma2(pack2(wv.x, wv.y),
+                                   pack2(fmaxf(__uint_as_float(r[cc][4 * j4 + 0]), 0.f),
+                                         fmaxf(__uint_as_float(r[cc][4 * j4 + 1]), 0.f)),
+                                   a2[ai]);
+                    a2[ai + 1] = ffma2(pack2(wv.z, wv.w),
+                                       pack2(fmaxf(__uint_as_float(r[cc][4 * j4 + 2]), 0.f),
+                                             fmaxf(__uint_as_float(r[cc][4 * j4 + 3]), 0.f)),
+                                       a2[ai + 1]);
                   }
               }
-              const float acc = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+              float acc = 0.f;
+              {
+                float lo[4], hi[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) unpack2(a2[u], lo[u], hi[u]);
+                acc = ((lo[0] + hi[0]) + (lo[1] + hi[1])) + ((lo[2] + hi[2]) + (lo[3] + hi[3]));
+              }
               const int row_q = gi * kQG + qq;
               if (s < qb.max_kv && row_q < qb.num_q) {
                 const bool live = G.active[qq] && key_ok && s <= G.pos[qq];
