@@ -44,6 +44,26 @@ BYTES_PER_IDX_KEY = 128 + 4                       # FP8 key row + its scale
 BYTES_PER_ATTN_KEY = 576 * 2                      # gathered bf16 latent row
 
 
+def _traffic(entry: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when no capture exists or the kernel's sources changed since it was taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        d = json.load(open(p))[entry]
+    except (OSError, KeyError, ValueError):
+        return None
+    if d.get("kernel", "").split("_")[0] != kernel.split("_")[0]:
+        return None
+    for rel, h in d["sources_sha256"].items():
+        try:
+            if hashlib.sha256(open(os.path.join(ROOT, rel), "rb").read()).hexdigest() != h:
+                return None
+        except OSError:
+            return None
+    return d["bytes_per_launch"]
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -199,7 +219,8 @@ def _roofline_prefill(wl, per_stage, steps, peaks):
     if dom == "attention":
         achieved = per_launch_units * FLOP_PER_ATTN_PAIR / avg_s / 1e12
         return {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sus"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sus"], "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sus"],
+                "traffic": _traffic("prefill_attention", "attn"),
                 "peak_src": f"{peaks['src']} bf16 sustained", "avg_launch_ms": tot / cnt, "launches": cnt}
     if dom == "indexer":
         # FP8 peak = measured bf16 peak x the nominal fp8/bf16 ratio (2)
@@ -227,7 +248,8 @@ def _roofline_decode(wl, per_stage, steps, peaks):
         byts = n_idx * 4 * steps / cnt
     achieved = byts / avg_s / 1e9
     return {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm"], "traffic": None, "peak_src": f"{peaks['src']} hbm burst",
+            "frac": achieved / peaks["hbm"], "traffic": _traffic("decode_indexer", dom) if dom == "indexer" else None,
+            "peak_src": f"{peaks['src']} hbm burst",
             "avg_launch_ms": tot / cnt, "launches": cnt}
 
 

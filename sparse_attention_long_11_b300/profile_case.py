@@ -20,11 +20,15 @@ def main() -> int:
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--q-rows", default=None,
                     help="a:b -- keep only query positions [a, b) of the prefill workloads (all keys stay cached)")
+    ap.add_argument("--decode-batch", type=int, default=64,
+                    help="sequences of the decode workload (65536 cached rows each)")
     a = ap.parse_args()
     if a.q_rows and a.workload in ("prefill", "long"):
         r0, r1 = (int(x) for x in a.q_rows.split(":"))
         L = 4096 if a.workload == "prefill" else 32768
         wl = inputs.make_prefill(seed=a.seed, device="cuda", L=L, name=a.workload, q_rows=(r0, r1))
+    elif a.workload == "decode":
+        wl = inputs.make_decode(seed=a.seed, device="cuda", batch=a.decode_batch)
     else:
         wl = inputs.make_config(inputs.CONFIG_NAMES.index(a.workload), seed=a.seed, device="cuda")
     prob = api.Problem(wl)
