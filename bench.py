@@ -141,9 +141,18 @@ def _max_over_ranks(x: float, ws: int) -> float:
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(tokens_per_rank: int, ms_local: float, ws: int):
+    """Whole-job throughput of N independent replicas: every rank processed
+    `tokens_per_rank` tokens; the job took the slowest rank's time.
+    Returns (tokens/s over all ranks, ms per step of the slowest rank)."""
+    ms = _max_over_ranks(ms_local, ws)
+    return tokens_per_rank * ws / (ms / 1e3), ms
 
 
 class Runner:
@@ -369,9 +378,7 @@ def main():
     wl = inputs.make_long(seed=0, device=dev)
     r = Runner(wl)
     ms, per_stage, launches, clocks = _time_steps(r, args.steps, args.warmup, ws, local)
-    ms = _max_over_ranks(ms, ws)
-    tokens = wl.num_q * ws
-    value = tokens / (ms / 1e3)
+    value, ms = aggregate(wl.num_q, ms, ws)
     roof = _roofline_prefill(wl, per_stage, args.steps, peaks)
     stages = {k: {"launches": v[0], "ms_per_step": v[1] / args.steps} for k, v in per_stage.items()}
     del r
@@ -394,8 +401,8 @@ def main():
         wd = inputs.make_decode(seed=0, device=dev)
         rd = Runner(wd)
         dms, dstage, dl, dclk = _time_steps(rd, max(args.steps, 10), args.warmup, ws, local)
-        dms = _max_over_ranks(dms, ws)
-        decode = {"workload": "decode B=64, ctx 65536 each, k=2048", "value": wd.num_q * ws / (dms / 1e3),
+        dval, dms = aggregate(wd.num_q, dms, ws)
+        decode = {"workload": "decode B=64, ctx 65536 each, k=2048", "value": dval,
                   "unit": "tokens/s", "ms_per_step": dms, "gpu_launches": dl,
                   "stages": {k: {"launches": v[0], "ms_per_step": v[1] / max(args.steps, 10)}
                              for k, v in dstage.items()},
