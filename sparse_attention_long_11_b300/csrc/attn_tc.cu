@@ -17,21 +17,26 @@
 //   * The score contraction is split by dims: CTA c contracts latent dims
 //     [256c, 256c+256) and rope dims [512+32c, 512+32c+32) (288 of 576), so
 //     every KV byte is gathered exactly once per query, by one CTA.  The two
-//     fp32 partial score tiles are exchanged through distributed shared
-//     memory and summed in the same order in both CTAs, so both run the same
-//     online softmax and scale their half of O consistently.  DSMEM moves
-//     only ~15-19 B/clk per SM on B300, so the exchange runs on its own warps
-//     with double-buffered receive tiles and overlaps the softmax and MMAs.
+//     partial logit tiles (base-2 units, rounded to fp16 to halve the
+//     distributed-shared-memory traffic, which moves only ~15-19 B/clk per
+//     SM) are exchanged and both CTAs add the same two fp16 values, so both
+//     run the same online softmax and scale their half of O consistently.  The receive
+//     tiles are double buffered, so the exchange of tile g overlaps the MMAs
+//     of tile g+1.
 //   * Tiles of 64 selected keys, gathered with coalesced 16-byte cp.async
 //     (a warp moves 512 contiguous bytes of one row per instruction) into
 //     128B-swizzled latent slots and a 64B-swizzled rope half.  (TMA
 //     tile::gather4 measured ~64 clk per 4-row instruction on B300, slower
 //     than this path.)  Heads are the MMA's M (=128); per tile each CTA issues 18 MMAs
-//     128x64x16 for S and 4 MMAs 128x256x16 for P.V, with V read MN-major
-//     straight out of the gathered K-major latent slots.
-//   * Warp roles per CTA: 0-3 softmax/epilogue (thread = head = TMEM lane),
-//     4-7 score exchange, 8-13 gather (three groups of two warps, group j
-//     fills KV stage j with the tiles g = j mod 3; at each query warps 8-11
+//     128x64x16 for S and 4 MMAs 128x256x16 for P.V.  P (bf16) is written
+//     back into TMEM over the tile's S columns and is the A operand of the
+//     P.V MMAs; V is read MN-major straight out of the gathered K-major
+//     latent slots.
+//   * Warp roles per CTA: 0-7 exchange + softmax + epilogue (thread = head
+//     = TMEM lane; warps w and w+4 take the two 32-key halves of each tile,
+//     which halves the per-thread latency of the exchange and the softmax),
+//     8-13 gather (three groups of two warps, group j
+//     fills the tiles g = j mod 3 into KV stage g mod 4; at each query warps 8-11
 //     write Q's latent part into TMEM and warp 8 loads the rope part with
 //     TMA), 14 TMEM owner + MMA issuer.
 //     Persistent: cluster j handles queries j, j+C, ...
@@ -55,16 +60,17 @@ constexpr uint32_t kQRopeBytes = 128 * 64;                 // rope half: 128 hea
 constexpr uint32_t kKVSlotBytes = kNK * 128;               // 64 keys x 128 B
 constexpr uint32_t kKVRopeBytes = kNK * 64;                // 64 keys x 64 B
 constexpr uint32_t kKVStageBytes = 4 * kKVSlotBytes + kKVRopeBytes;   // 36 KB
-constexpr uint32_t kXBytes = kH * kNK * 4;                 // one partial score tile from the peer
-constexpr uint32_t kPBytes = kH * 128;                     // 128 x 64 bf16 probabilities (SW128)
-constexpr int kStages = 3;
+constexpr uint32_t kXBytes = kH * kNK * 2;                 // one partial logit tile from the peer (fp16)
+constexpr int kStages = 4;
 constexpr uint32_t kOffQRope = 0;
 constexpr uint32_t kOffKV = kOffQRope + kQRopeBytes;       // 8 KB
-constexpr uint32_t kOffX = kOffKV + kStages * kKVStageBytes;   // 116 KB
-constexpr uint32_t kOffP = kOffX + 2 * kXBytes;            // 180 KB: P[0], P[1]
-constexpr uint32_t kSmemBytes = kOffP + 2 * kPBytes;       // 212 KB (P double buffered)
+constexpr uint32_t kOffX = kOffKV + kStages * kKVStageBytes;   // 152 KB
+constexpr uint32_t kSmemBytes = kOffX + 2 * kXBytes;       // 184 KB
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;         // + alignment slack
-constexpr int kThreads = 480;
+constexpr int kGatherWarp0 = 8;
+constexpr int kGatherGroups = 3;                           // of two warps; group j gathers the tiles g = j mod 3
+constexpr int kMmaWarp = kGatherWarp0 + 2 * kGatherGroups; // 14
+constexpr int kThreads = (kMmaWarp + 1) * 32;              // 480: at most 4 warps per SM sub-partition
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 384;  // S buffer b at kTmemS + 64 b
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -85,9 +91,10 @@ __device__ long long g_attn_trace[4][512][8];
 #endif
 
 struct Bars {
-  uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], s_empty[2], xf[2], xe[2];
-  uint64_t p_full[2], pv_done[2];
+  uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], xf[2], xe[2];
+  uint64_t p_full[2], pv_done[2], pair[4];
   uint64_t q_full, q_empty, o_empty, fin;
+  float red[3][2][128];   // [tile parity][key half][head] tile maxima; [2] the halves' sums
   uint32_t tmem_base;
   int abort;
 };
@@ -116,18 +123,6 @@ __device__ __forceinline__ bool wait_fin(uint64_t* bar) {   // bounded, ignores 
   while (!mbar_try_wait(a, 0))
     if (clock64() - t0 > kWaitLimitCycles) return false;
   return true;
-}
-
-// Own partial score row of this thread's head (64 fp32 from TMEM).
-__device__ __forceinline__ void load_s(uint32_t taddr, float (&s)[64]) {
-  uint32_t r[4][16];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) tmem_ld16(taddr + c * 16, r[c]);
-  tmem_ld_wait();
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-#pragma unroll
-    for (int j = 0; j < 16; ++j) s[c * 16 + j] = __uint_as_float(r[c][j]);
 }
 
 struct QueryInfo {
@@ -164,24 +159,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&B.s_full[s], 1);
-      mbar_init(&B.s_empty[s], 256);   // the exchange warps and the softmax warps both read S
-      mbar_init(&B.xf[s], 1);          // armed by our softmax thread 0; the peer's st.async credit the bytes
-      mbar_init(&B.xe[s], 128);        // arrivals of the peer's softmax warps
+      mbar_init(&B.xf[s], 1);          // armed by our thread 0; the peer's st.async credit the bytes
+      mbar_init(&B.xe[s], 256);        // arrivals of the peer's softmax warps
     }
     mbar_init(&B.q_full, 129);       // 128 TMEM writers + the rope TMA (with its bytes)
     mbar_init(&B.q_empty, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&B.p_full[s], 128);
+      mbar_init(&B.p_full[s], 256);
       mbar_init(&B.pv_done[s], 1);
     }
-    mbar_init(&B.o_empty, 128);
+    for (int q = 0; q < 4; ++q) mbar_init(&B.pair[q], 64);
+    mbar_init(&B.o_empty, 256);
     mbar_init(&B.fin, 1);
     B.abort = 0;
     fence_mbar_init();
     mbar_arrive_expect_tx(&B.xf[0], kXBytes);   // arm the first phase of both receive tiles
     mbar_arrive_expect_tx(&B.xf[1], kXBytes);
   }
-  if (warp == 14) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&B.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -191,92 +186,125 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
   tc_fence_after();
   const uint32_t tmem = B.tmem_base;
   const uint32_t sQr = smem_u32(sm + kOffQRope), sKV = smem_u32(sm + kOffKV);
-  const uint32_t sP = smem_u32(sm + kOffP);
 
-  if (warp < 4) {
-    // ------------------------------------------------------------ softmax / epilogue
-    const int h = tid;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  if (warp < 8) {
+    // ------------------------------------------------------------ exchange, softmax, epilogue
+    // Warps w and w+4 share TMEM lane quadrant w%4 (heads 32(w%4)..+31) and
+    // split every tile's 64 keys: warp w the first 32, warp w+4 the last 32.
+    // Each pushes its half of this CTA's partial scores to the peer, adds the
+    // peer's half, and the pair agrees on the tile maximum through shared
+    // memory.  P (bf16) goes back into TMEM over the tile's S columns: the
+    // A operand of the P.V MMA.
+    const int q4 = warp & 3, half = warp >> 2;
+    const int h = (q4 << 5) | lane;
+    const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
+    const uint32_t x_peer = mapa(smem_u32(sm + kOffX), peer);
+    const uint32_t xf_peer[2] = {mapa(smem_u32(&B.xf[0]), peer), mapa(smem_u32(&B.xf[1]), peer)};
     const uint32_t xe_peer[2] = {mapa(smem_u32(&B.xe[0]), peer), mapa(smem_u32(&B.xe[1]), peer)};
-    uint32_t g = 0;
+    uint64_t* pair = &B.pair[q4];
+    uint32_t g = 0, pu = 0;   // tile counter, uses of the pair barrier
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
       const QueryInfo qi = query_info(qb, idx, k, i, pv);
       const int pos = qi.pos, nt = qi.nt;
       const int32_t* irow = idx + (int64_t)i * k;
-      __nv_bfloat16* orow = out + ((int64_t)i * kH + h) * kDv + crank * 256;
+      __nv_bfloat16* orow = out + ((int64_t)i * kH + h) * kDv + crank * 256 + half * 128;
       if (nt == 0) {
         uint4* o4 = reinterpret_cast<uint4*>(orow);
 #pragma unroll 4
-        for (int c = 0; c < 32; ++c) o4[c] = make_uint4(0, 0, 0, 0);
-        if (crank == 0) lse[(int64_t)i * kH + h] = -INFINITY;
-        if (!qi.ok && h == 0 && crank == 0) flag_error(err, DSA_ERR_BOUNDS);
+        for (int c = 0; c < 16; ++c) o4[c] = make_uint4(0, 0, 0, 0);
+        if (crank == 0 && half == 0) lse[(int64_t)i * kH + h] = -INFINITY;
+        if (!qi.ok && h == 0 && crank == 0 && half == 0) flag_error(err, DSA_ERR_BOUNDS);
         continue;
       }
       const int n_valid = min(k, pos + 1);
-      float m_use = -INFINITY, l = 0.f;
+      float m_use = -INFINITY, l = 0.f;   // running max (shared by the pair), this half's running sum
       bool ok = true;
       for (int t = 0; t < nt; ++t, ++g) {
         const int b = g & 1;
         const uint32_t par = (g >> 1) & 1;
-        int s0 = 0, s1 = 0;
-        if (!pv) {   // loads issued early; their latency hides behind the waits below
-          const int e0 = t * kNK + lane, e1 = e0 + 32;
-          s0 = e0 < k ? __ldg(irow + e0) : -1;
-          s1 = e1 < k ? __ldg(irow + e1) : -1;
+        int s_e = 0;
+        if (!pv) {   // this lane's entry of the own half (loaded early; latency hides behind the waits)
+          const int e = t * kNK + 32 * half + lane;
+          s_e = e < k ? __ldg(irow + e) : -1;
         }
-        ATTN_TRACE(0, g, 0, h == 0);
-        if (!(ok = mbar_wait<true>(&B.xf[b], par, abort))) break;   // the peer's partial is in X[b]
-        ATTN_TRACE(0, g, 1, h == 0);
+        ATTN_TRACE(half, g, 0, lane == 0 && q4 == 0);
         if (!(ok = mbar_wait(&B.s_full[b], par, abort))) break;
-        ATTN_TRACE(0, g, 6, h == 0);
         tc_fence_after();
-        float s[64];
-        load_s(tmem + lane_base + kTmemS + b * 64, s);
-        ATTN_TRACE(0, g, 7, h == 0);
+        float s[32];
         {
-          const float4* X4 = reinterpret_cast<const float4*>(sm + kOffX + b * kXBytes);
+          uint32_t r[2][16];
+          tmem_ld16(tmem + lane_base + kTmemS + b * 64 + half * 32, r[0]);
+          tmem_ld16(tmem + lane_base + kTmemS + b * 64 + half * 32 + 16, r[1]);
+          tmem_ld_wait();
 #pragma unroll
-          for (int jq = 0; jq < 16; ++jq) {
-            const float4 v = X4[jq * 128 + h];
-            // CTA 0's partial first, so both CTAs form the identical fp32 sum
-            if (crank == 0) {
-              s[4 * jq] += v.x; s[4 * jq + 1] += v.y; s[4 * jq + 2] += v.z; s[4 * jq + 3] += v.w;
-            } else {
-              s[4 * jq] = v.x + s[4 * jq]; s[4 * jq + 1] = v.y + s[4 * jq + 1];
-              s[4 * jq + 2] = v.z + s[4 * jq + 2]; s[4 * jq + 3] = v.w + s[4 * jq + 3];
+          for (int j = 0; j < 16; ++j) {
+            s[j] = __uint_as_float(r[0][j]);
+            s[16 + j] = __uint_as_float(r[1][j]);
+          }
+        }
+        ATTN_TRACE(half, g, 1, lane == 0 && q4 == 0);
+        // partial logits in base-2 units, rounded to fp16: the form both CTAs
+        // add, so the two sums (and softmax states) are identical
+        uint32_t xh[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) xh[j] = f16x2_sat(s[2 * j] * scale_log2, s[2 * j + 1] * scale_log2);
+        // own partial -> the peer's X[b], once the peer has consumed what we wrote there two tiles ago
+        if (!(ok = mbar_wait<true>(&B.xe[b], par ^ 1, abort))) break;
+        {
+          const uint32_t dst = x_peer + b * kXBytes;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+            st_async_v4_b32(dst + (uint32_t)((4 * half + jj) * 128 + h) * 16u,
+                            make_uint4(xh[4 * jj], xh[4 * jj + 1], xh[4 * jj + 2], xh[4 * jj + 3]), xf_peer[b]);
+        }
+        ATTN_TRACE(half, g, 2, lane == 0 && q4 == 0);
+        if (!(ok = mbar_wait<true>(&B.xf[b], par, abort))) break;   // the peer's partial is in X[b]
+        // arm the next phase of X[b]: the peer writes it only after all our
+        // threads have read this phase and said so (below)
+        if (tid == 0) mbar_arrive_expect_tx(&B.xf[b], kXBytes);
+        ATTN_TRACE(half, g, 3, lane == 0 && q4 == 0);
+        {
+          // x = own + peer in fp32 (a two-term sum is the same in either order)
+          const uint4* X4 = reinterpret_cast<const uint4*>(sm + kOffX + b * kXBytes);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint4 v = X4[(4 * half + jj) * 128 + h];
+            const uint32_t pv4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 o = f16x2_to_f32x2(xh[4 * jj + e]), p = f16x2_to_f32x2(pv4[e]);
+              s[8 * jj + 2 * e] = o.x + p.x;
+              s[8 * jj + 2 * e + 1] = o.y + p.y;
             }
           }
         }
-        ATTN_TRACE(1, g, 4, h == 0 && s[0] != 12345.f);   // after the partial read (value dependency)
-        tc_fence_before();
-        mbar_arrive(&B.s_empty[b]);
-        ATTN_TRACE(1, g, 5, h == 0);
-        // X[b] consumed (the loads above have returned and their values are in
-        // use): the peer may write its next tile there.  A release-ordered
-        // remote arrive costs ~1.5k clk here; relaxed is enough.
-        mbar_arrive_remote_relaxed(xe_peer[b]);
-        if (h == 0) mbar_arrive_expect_tx(&B.xf[b], kXBytes);   // arm the next phase of this receive tile
-        ATTN_TRACE(0, g, 2, h == 0);
 
-        uint32_t v_lo, v_hi;
+        uint32_t vmask;
         if (pv) {
-          const int rem = n_valid - t * kNK;   // the valid entries of this tile form a prefix
-          v_lo = rem >= 32 ? 0xffffffffu : (rem <= 0 ? 0u : (1u << rem) - 1u);
-          v_hi = rem >= 64 ? 0xffffffffu : (rem <= 32 ? 0u : (1u << (rem - 32)) - 1u);
+          const int rem = n_valid - t * kNK - 32 * half;   // the valid entries of this tile form a prefix
+          vmask = rem >= 32 ? 0xffffffffu : (rem <= 0 ? 0u : (1u << rem) - 1u);
         } else {
-          v_lo = __ballot_sync(0xffffffffu, s0 >= 0 && s0 <= pos);
-          v_hi = __ballot_sync(0xffffffffu, s1 >= 0 && s1 <= pos);
+          vmask = __ballot_sync(0xffffffffu, s_e >= 0 && s_e <= pos);
         }
-
-        // online softmax in base 2: logits x = scale * log2(e) * S
+        // online softmax in base 2 (s already holds x = scale * log2(e) * S)
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const bool valid = ((j < 32 ? v_lo >> j : v_hi >> (j - 32)) & 1u) != 0;
-          s[j] = valid ? s[j] * scale_log2 : -INFINITY;
+        for (int j = 0; j < 32; ++j) {
+          s[j] = ((vmask >> j) & 1u) ? s[j] : -INFINITY;
           m4[j & 3] = fmaxf(m4[j & 3], s[j]);
         }
-        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        const float mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        B.red[b][half][h] = mh;
+        // X[b] consumed: the store above needs mh, which depends on every
+        // value loaded from X[b], and instructions issue in order, so this
+        // relaxed arrive follows those loads (a release-ordered remote arrive
+        // costs ~1.5k clk)
+        mbar_arrive_remote_relaxed(xe_peer[b]);
+        // the pair's maxima (the barrier also orders both warps' S loads before any P store)
+        mbar_arrive(pair);
+        if (!(ok = mbar_wait(pair, pu & 1, abort))) break;
+        ++pu;
+        const float mt = fmaxf(B.red[b][0][h], B.red[b][1][h]);
         float alpha = 1.f;
         bool rescale = false;
         if (mt > m_use + 8.f) {
@@ -285,58 +313,54 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
           rescale = true;
         }
         const float msub = m_use == -INFINITY ? 0.f : m_use;   // all p are 0 while nothing is valid
-        uint32_t pk[32];
+        uint32_t pk[16];
         float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 64; j += 2) {
+        for (int j = 0; j < 32; j += 2) {
           const float p0 = ex2_approx(s[j] - msub);
           const float p1 = ex2_approx(s[j + 1] - msub);
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
           ps4[(j >> 1) & 3] += __low2float(pb) + __high2float(pb);
           pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
         }
-        const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
-        l = l * alpha + psum;
-        ATTN_TRACE(0, g, 3, h == 0);
-
-        // P[b] is free once the P.V of tile g-2 is done; rescaling O also
-        // needs the P.V of tile g-1 to be done
-        if (!(ok = mbar_wait(&B.pv_done[b], par ^ 1, abort))) break;
-        if (rescale && t > 0 && !(ok = mbar_wait(&B.pv_done[b ^ 1], ((g - 1) >> 1) & 1, abort))) break;
-        ATTN_TRACE(0, g, 4, h == 0);
-        tc_fence_after();
+        l = l * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
+        ATTN_TRACE(half, g, 4, lane == 0 && q4 == 0);
         if (rescale && t > 0) {
+          // O holds the P.V of tiles < g; that of tile g-1 must be complete
+          if (!(ok = mbar_wait(&B.pv_done[b ^ 1], ((g - 1) >> 1) & 1, abort))) break;
+          tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 256; c += 16) {
+          for (int c = 0; c < 128; c += 16) {
             uint32_t r[16];
-            tmem_ld16(tmem + lane_base + kTmemO + c, r);
+            tmem_ld16(tmem + lane_base + kTmemO + half * 128 + c, r);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-            tmem_st16(tmem + lane_base + kTmemO + c, r);
+            tmem_st16(tmem + lane_base + kTmemO + half * 128 + c, r);
           }
-          tmem_st_wait();
         }
-        uint8_t* prow = sm + kOffP + b * kPBytes;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          *reinterpret_cast<uint4*>(prow + sw128_offset(h, cc)) =
-              make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        fence_proxy_async_smem();
+        // P of this half: keys 32*half.. -> TMEM columns kTmemS + 64b + 16*half (bf16 pairs)
+        tmem_st16(tmem + lane_base + kTmemS + b * 64 + half * 16, pk);
+        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&B.p_full[b]);
-        ATTN_TRACE(0, g, 5, h == 0);
+        ATTN_TRACE(half, g, 5, lane == 0 && q4 == 0);
       }
       if (!ok) break;
-      // epilogue: O row of this head, normalised, bf16
+      // epilogue: this half of the O row of this head, normalised, bf16
+      B.red[2][half][h] = l;
+      mbar_arrive(pair);
+      if (!mbar_wait(pair, pu & 1, abort)) break;
+      ++pu;
+      const float lt = B.red[2][0][h] + B.red[2][1][h];
       if (!mbar_wait(&B.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort)) break;
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       uint4* o4 = reinterpret_cast<uint4*>(orow);
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 16) {
+      for (int c = 0; c < 128; c += 16) {
         uint32_t r[16];
-        tmem_ld16(tmem + lane_base + kTmemO + c, r);
+        tmem_ld16(tmem + lane_base + kTmemO + half * 128 + c, r);
         tmem_ld_wait();
         uint32_t w[8];
 #pragma unroll
@@ -348,49 +372,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         o4[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
         o4[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      if (crank == 0) lse[(int64_t)i * kH + h] = l > 0.f ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+      if (crank == 0 && half == 0) lse[(int64_t)i * kH + h] = lt > 0.f ? (m_use + log2f(lt)) * kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(&B.o_empty);
     }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ score exchange
-    const int h = ((warp & 3) << 5) | lane;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t x_peer = mapa(smem_u32(sm + kOffX), peer);
-    const uint32_t xf_peer[2] = {mapa(smem_u32(&B.xf[0]), peer), mapa(smem_u32(&B.xf[1]), peer)};
-    // (the peer arms its xf[b] with the tile's bytes; our st.async credit them)
-    uint32_t g = 0;
-    for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
-      const QueryInfo qi = query_info(qb, idx, k, i, pv);
-      bool ok = true;
-      for (int t = 0; t < qi.nt; ++t, ++g) {
-        const int b = g & 1;
-        const uint32_t par = (g >> 1) & 1;
-        ATTN_TRACE(1, g, 0, h == 0);
-        if (!(ok = mbar_wait(&B.s_full[b], par, abort))) break;
-        ATTN_TRACE(1, g, 1, h == 0);
-        tc_fence_after();
-        float s[64];
-        load_s(tmem + lane_base + kTmemS + b * 64, s);
-        tc_fence_before();
-        mbar_arrive(&B.s_empty[b]);
-        // the peer has consumed what we wrote into its X[b] two tiles ago
-        if (!(ok = mbar_wait<true>(&B.xe[b], par ^ 1, abort))) break;
-        ATTN_TRACE(1, g, 2, h == 0);
-        const uint32_t dst = x_peer + b * kXBytes;
-#pragma unroll
-        for (int jq = 0; jq < 16; ++jq)
-          st_async_v4(dst + (uint32_t)(jq * 128 + h) * 16u,
-                      make_float4(s[4 * jq], s[4 * jq + 1], s[4 * jq + 2], s[4 * jq + 3]), xf_peer[b]);
-        ATTN_TRACE(1, g, 3, h == 0);
-      }
-      if (!ok) break;
-    }
-  } else if (warp < 14) {
+  } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ gather (cp.async) + Q (TMA)
     // Group grp (warps 8+2grp, 9+2grp) fills stage grp with the tiles g with
     // g % 3 == grp; warp wg of the group copies rows 32wg .. 32wg+31.
-    const int grp = (warp - 8) >> 1, wg = (warp - 8) & 1;
+    const int grp = (warp - kGatherWarp0) >> 1, wg = (warp - kGatherWarp0) & 1;
     const bool q_writer = warp < 12;                         // warps 8-11 cover the four TMEM lane quadrants
     const int hq = ((warp & 3) << 5) | lane;                 // TMEM lane (head) this thread writes Q for
     const uint32_t q_lane = (uint32_t)((warp & 3) * 32) << 16;
@@ -440,15 +430,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       }
       bool ok = true;
       for (int t = 0; t < qi.nt; ++t, ++g) {
-        if ((int)(g % kStages) != grp) continue;
+        if ((int)(g % kGatherGroups) != grp) continue;
         // row of this lane's entry (loaded before the wait so the latency overlaps it)
         const int e = t * kNK + 32 * wg + lane;
         int s_e = -1;
         if (e < k) s_e = __ldg(irow + e);
-        ATTN_TRACE(2, g, 0, lane == 0 && wg == 0);
+        ATTN_TRACE(2, g, 0 + 3 * wg, lane == 0);
         const int st = g % kStages;
         if (!(ok = mbar_wait(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
-        ATTN_TRACE(2, g, 1, lane == 0 && wg == 0);
+        ATTN_TRACE(2, g, 1 + 3 * wg, lane == 0);
         int row = -1;                                         // physical rows fit in 31 bits
         if (s_e >= 0 && s_e <= qi.pos) row = (int)cache_row(cm, seq, s_e, err);
         else if (s_e != -1) flag_error(err, DSA_ERR_BOUNDS);
@@ -479,7 +469,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         cp_async_wait_all();
         fence_proxy_async_smem();
         mbar_arrive(&B.kv_full[st]);
-        ATTN_TRACE(2, g, 2, lane == 0 && wg == 0);
+        ATTN_TRACE(2, g, 2 + 3 * wg, lane == 0);
       }
       if (!ok) break;
       ++qv;
@@ -500,15 +490,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       tc_fence_after();
       if (lane == 0) {
         const uint32_t skv = sKV + (gp % kStages) * kKVStageBytes;
-        const uint32_t sp = sP + (gp & 1) * kPBytes;
+        const uint32_t tp_col = tmem + kTmemS + 64 * (gp & 1);   // P (bf16 pairs) over the tile's S columns
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16(tmem + kTmemO, sdesc(sp + kk * 32, 16, 1024), sdesc(skv + kk * 2048, kKVSlotBytes, 1024), id_pv,
-                   (tp > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + kTmemO, tp_col + kk * 8, sdesc(skv + kk * 2048, kKVSlotBytes, 1024), id_pv,
+                      (tp > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&B.pv_done[gp & 1]);
         mma_commit(&B.kv_empty[gp % kStages]);
       }
       __syncwarp();
+      ATTN_TRACE(3, gp, 6, lane == 0);
       return true;
     };
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
@@ -522,7 +513,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         ATTN_TRACE(3, g, 0, lane == 0);
         if (!(ok = mbar_wait(&B.kv_full[st], (g / kStages) & 1, abort))) break;
         ATTN_TRACE(3, g, 1, lane == 0);
-        if (!(ok = mbar_wait(&B.s_empty[sb], ((g >> 1) & 1) ^ 1, abort))) break;
+        // S buffer sb last held P(g-2): the P.V reading it was issued before
+        // this MMA (tensor-pipe order), and P(g-2) was written only after
+        // both warps of each pair had loaded S(g-2)
         ATTN_TRACE(3, g, 2, lane == 0);
         tc_fence_after();
         if (lane == 0) {
@@ -543,6 +536,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
           if (t == nt - 1) mma_commit(&B.q_empty);
         }
         __syncwarp();
+        ATTN_TRACE(3, g, 5, lane == 0);
         if (t > 0 && !(ok = issue_pv(g - 1, t - 1))) break;
       }
       if (!ok || !issue_pv(g - 1, nt - 1)) break;
@@ -556,7 +550,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
   tc_fence_before();
   __syncthreads();
   cluster_sync();       // the peer no longer reads or writes our shared memory
-  if (warp == 14) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -133,6 +133,25 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t re
                "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
                : "memory");
 }
+__device__ __forceinline__ void st_async_v4_b32(uint32_t addr, uint4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+               : "memory");
+}
+// Two fp32 -> packed fp16x2 (lo = a), round to nearest even, saturated to
+// the finite range; and back.
+__device__ __forceinline__ uint32_t f16x2_sat(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t v) {
+  float2 r;
+  asm("{\n .reg .f16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.f32.f16 %0, lo;\n cvt.f32.f16 %1, hi;\n}\n"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(v));
+  return r;
+}
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster
 // scope: this thread's earlier shared::cluster stores are visible first).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
