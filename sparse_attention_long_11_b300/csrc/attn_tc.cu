@@ -19,8 +19,8 @@
 //     every KV byte is gathered exactly once per query, by one CTA.  The two
 //     partial logit tiles (base-2 units, rounded to fp16 to halve the
 //     distributed-shared-memory traffic, which moves only ~15-19 B/clk per
-//     SM) are exchanged and both CTAs add the same two fp16 values, so both
-//     run the same online softmax and scale their half of O consistently.  The receive
+//     SM) are exchanged; each CTA adds the peer's fp16 partial to its own
+//     fp32 one and runs the online softmax for its half of O.  The receive
 //     tiles are double buffered, so the exchange of tile g overlaps the MMAs
 //     of tile g+1.
 //   * Tiles of 64 selected keys, gathered with coalesced 16-byte cp.async
@@ -32,9 +32,9 @@
 //     back into TMEM over the tile's S columns and is the A operand of the
 //     P.V MMAs; V is read MN-major straight out of the gathered K-major
 //     latent slots.
-//   * Warp roles per CTA: 0-7 exchange + softmax + epilogue (thread = head
-//     = TMEM lane; warps w and w+4 take the two 32-key halves of each tile,
-//     which halves the per-thread latency of the exchange and the softmax),
+//   * Warp roles per CTA: 0-7 exchange + softmax + epilogue in two groups
+//     that take alternate tiles (thread = head = TMEM lane), so that one
+//     group computes while the other waits for the peer's partial logits,
 //     8-13 gather (three groups of two warps, group j
 //     fills the tiles g = j mod 3 into KV stage g mod 4; at each query warps 8-11
 //     write Q's latent part into TMEM and warp 8 loads the rope part with
@@ -92,9 +92,12 @@ __device__ long long g_attn_trace[4][512][8];
 
 struct Bars {
   uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], xf[2], xe[2];
-  uint64_t p_full[2], pv_done[2], pair[4];
-  uint64_t q_full, q_empty, o_empty, fin;
-  float red[3][2][128];   // [tile parity][key half][head] tile maxima; [2] the halves' sums
+  uint64_t p_full[2], pv_done[2], mdone[2];
+  uint64_t q_full, q_empty, o_empty, qend, fin;
+  float mtile[2][128];          // [group][head] scratch: the tile maximum
+  float mpub[2][128];           // [tile parity][head] running maximum after the group's latest tile
+  float lsum[2][2][128];        // [query parity][group][head] the groups' sums at the end of a query
+  float mseen[2][2][128];       // ... and the maxima they are relative to
   uint32_t tmem_base;
   int abort;
 };
@@ -160,16 +163,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     for (int s = 0; s < 2; ++s) {
       mbar_init(&B.s_full[s], 1);
       mbar_init(&B.xf[s], 1);          // armed by our thread 0; the peer's st.async credit the bytes
-      mbar_init(&B.xe[s], 256);        // arrivals of the peer's softmax warps
+      mbar_init(&B.xe[s], 128);        // arrivals of the peer's softmax group of this parity
     }
     mbar_init(&B.q_full, 129);       // 128 TMEM writers + the rope TMA (with its bytes)
     mbar_init(&B.q_empty, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&B.p_full[s], 256);
+      mbar_init(&B.p_full[s], 128);
       mbar_init(&B.pv_done[s], 1);
+      mbar_init(&B.mdone[s], 128);
     }
-    for (int q = 0; q < 4; ++q) mbar_init(&B.pair[q], 64);
     mbar_init(&B.o_empty, 256);
+    mbar_init(&B.qend, 256);
     mbar_init(&B.fin, 1);
     B.abort = 0;
     fence_mbar_init();
@@ -189,170 +193,185 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
 
   if (warp < 8) {
     // ------------------------------------------------------------ exchange, softmax, epilogue
-    // Warps w and w+4 share TMEM lane quadrant w%4 (heads 32(w%4)..+31) and
-    // split every tile's 64 keys: warp w the first 32, warp w+4 the last 32.
-    // Each pushes its half of this CTA's partial scores to the peer, adds the
-    // peer's half, and the pair agrees on the tile maximum through shared
-    // memory.  P (bf16) goes back into TMEM over the tile's S columns: the
-    // A operand of the P.V MMA.
-    const int q4 = warp & 3, half = warp >> 2;
+    // Two groups of four warps take alternate tiles (group b the tiles g with
+    // g % 2 == b, which use S/P buffer b and receive tile X[b]); in a group,
+    // thread = head = TMEM lane, over all 64 keys.  While one group waits for
+    // the peer's partial logits of its tile, the other computes.  The running
+    // maximum passes from tile to tile (so from group to group) through
+    // shared memory; each group keeps its own running sum, relative to the
+    // maximum it last saw, and the two sums meet at the end of the query.
+    // P (bf16) goes back into TMEM over the tile's S columns: the A operand
+    // of the P.V MMA.
+    const int grp = warp >> 2, q4 = warp & 3;
     const int h = (q4 << 5) | lane;
+    const int gtid = tid & 127;
     const uint32_t lane_base = (uint32_t)(q4 * 32) << 16;
-    const uint32_t x_peer = mapa(smem_u32(sm + kOffX), peer);
-    const uint32_t xf_peer[2] = {mapa(smem_u32(&B.xf[0]), peer), mapa(smem_u32(&B.xf[1]), peer)};
-    const uint32_t xe_peer[2] = {mapa(smem_u32(&B.xe[0]), peer), mapa(smem_u32(&B.xe[1]), peer)};
-    uint64_t* pair = &B.pair[q4];
-    uint32_t g = 0, pu = 0;   // tile counter, uses of the pair barrier
+    const uint32_t tS = tmem + lane_base + kTmemS + grp * 64;   // this group's S / P buffer
+    const uint32_t x_peer = mapa(smem_u32(sm + kOffX + grp * kXBytes), peer);
+    const uint32_t xf_peer = mapa(smem_u32(&B.xf[grp]), peer);
+    const uint32_t xe_peer = mapa(smem_u32(&B.xe[grp]), peer);
+    const uint4* X4 = reinterpret_cast<const uint4*>(sm + kOffX + grp * kXBytes);
+    uint32_t g = 0, qv = 0;   // tiles and queries (with tiles) so far, counted alike by both groups
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
       const QueryInfo qi = query_info(qb, idx, k, i, pv);
       const int pos = qi.pos, nt = qi.nt;
       const int32_t* irow = idx + (int64_t)i * k;
-      __nv_bfloat16* orow = out + ((int64_t)i * kH + h) * kDv + crank * 256 + half * 128;
+      __nv_bfloat16* orow = out + ((int64_t)i * kH + h) * kDv + crank * 256 + grp * 128;
       if (nt == 0) {
         uint4* o4 = reinterpret_cast<uint4*>(orow);
 #pragma unroll 4
         for (int c = 0; c < 16; ++c) o4[c] = make_uint4(0, 0, 0, 0);
-        if (crank == 0 && half == 0) lse[(int64_t)i * kH + h] = -INFINITY;
-        if (!qi.ok && h == 0 && crank == 0 && half == 0) flag_error(err, DSA_ERR_BOUNDS);
+        if (crank == 0 && grp == 0) lse[(int64_t)i * kH + h] = -INFINITY;
+        if (!qi.ok && h == 0 && crank == 0 && grp == 0) flag_error(err, DSA_ERR_BOUNDS);
         continue;
       }
       const int n_valid = min(k, pos + 1);
-      float m_use = -INFINITY, l = 0.f;   // running max (shared by the pair), this half's running sum
+      float m_seen = -INFINITY, l = 0.f;   // the maximum this group last used, its sum relative to it
       bool ok = true;
-      for (int t = 0; t < nt; ++t, ++g) {
-        const int b = g & 1;
-        const uint32_t par = (g >> 1) & 1;
-        int s_e = 0;
-        if (!pv) {   // this lane's entry of the own half (loaded early; latency hides behind the waits)
-          const int e = t * kNK + 32 * half + lane;
-          s_e = e < k ? __ldg(irow + e) : -1;
+      const uint32_t g0 = g;
+      for (int t = ((g0 & 1u) == (uint32_t)grp) ? 0 : 1; t < nt; t += 2) {
+        const uint32_t gt = g0 + t;
+        const uint32_t par = (gt >> 1) & 1;
+        int s_e0 = 0, s_e1 = 0;
+        if (!pv) {   // this lane's entries (keys lane, lane+32 of the tile), loaded early
+          const int e0 = t * kNK + lane, e1 = e0 + 32;
+          s_e0 = e0 < k ? __ldg(irow + e0) : -1;
+          s_e1 = e1 < k ? __ldg(irow + e1) : -1;
         }
-        ATTN_TRACE(half, g, 0, lane == 0 && q4 == 0);
-        if (!(ok = mbar_wait(&B.s_full[b], par, abort))) break;
+        ATTN_TRACE(grp, gt, 0, lane == 0 && q4 == 0);
+        if (!(ok = mbar_wait(&B.s_full[grp], par, abort))) break;
         tc_fence_after();
-        float s[32];
+        // own partial logits in base-2 units (fp32); the peer gets them rounded to fp16
+        float x[64];
         {
-          uint32_t r[2][16];
-          tmem_ld16(tmem + lane_base + kTmemS + b * 64 + half * 32, r[0]);
-          tmem_ld16(tmem + lane_base + kTmemS + b * 64 + half * 32 + 16, r[1]);
+          uint32_t r[4][16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld16(tS + c * 16, r[c]);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            s[j] = __uint_as_float(r[0][j]);
-            s[16 + j] = __uint_as_float(r[1][j]);
-          }
+          for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(r[j >> 4][j & 15]) * scale_log2;
         }
-        ATTN_TRACE(half, g, 1, lane == 0 && q4 == 0);
-        // partial logits in base-2 units, rounded to fp16: the form both CTAs
-        // add, so the two sums (and softmax states) are identical
-        uint32_t xh[16];
+        ATTN_TRACE(grp, gt, 1, lane == 0 && q4 == 0);
+        // own partial -> the peer's X[grp], once the peer has consumed what we wrote there two tiles ago
+        if (!(ok = mbar_wait<true>(&B.xe[grp], par ^ 1, abort))) break;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) xh[j] = f16x2_sat(s[2 * j] * scale_log2, s[2 * j + 1] * scale_log2);
-        // own partial -> the peer's X[b], once the peer has consumed what we wrote there two tiles ago
-        if (!(ok = mbar_wait<true>(&B.xe[b], par ^ 1, abort))) break;
-        {
-          const uint32_t dst = x_peer + b * kXBytes;
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj)
-            st_async_v4_b32(dst + (uint32_t)((4 * half + jj) * 128 + h) * 16u,
-                            make_uint4(xh[4 * jj], xh[4 * jj + 1], xh[4 * jj + 2], xh[4 * jj + 3]), xf_peer[b]);
-        }
-        ATTN_TRACE(half, g, 2, lane == 0 && q4 == 0);
-        if (!(ok = mbar_wait<true>(&B.xf[b], par, abort))) break;   // the peer's partial is in X[b]
-        // arm the next phase of X[b]: the peer writes it only after all our
-        // threads have read this phase and said so (below)
-        if (tid == 0) mbar_arrive_expect_tx(&B.xf[b], kXBytes);
-        ATTN_TRACE(half, g, 3, lane == 0 && q4 == 0);
-        {
-          // x = own + peer in fp32 (a two-term sum is the same in either order)
-          const uint4* X4 = reinterpret_cast<const uint4*>(sm + kOffX + b * kXBytes);
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const uint4 v = X4[(4 * half + jj) * 128 + h];
-            const uint32_t pv4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 o = f16x2_to_f32x2(xh[4 * jj + e]), p = f16x2_to_f32x2(pv4[e]);
-              s[8 * jj + 2 * e] = o.x + p.x;
-              s[8 * jj + 2 * e + 1] = o.y + p.y;
-            }
-          }
-        }
-
-        uint32_t vmask;
+        for (int jq = 0; jq < 8; ++jq)
+          st_async_v4_b32(x_peer + (uint32_t)(jq * 128 + h) * 16u,
+                          make_uint4(f16x2_sat(x[8 * jq], x[8 * jq + 1]), f16x2_sat(x[8 * jq + 2], x[8 * jq + 3]),
+                                     f16x2_sat(x[8 * jq + 4], x[8 * jq + 5]), f16x2_sat(x[8 * jq + 6], x[8 * jq + 7])),
+                          xf_peer);
+        ATTN_TRACE(grp, gt, 2, lane == 0 && q4 == 0);
+        if (!(ok = mbar_wait<true>(&B.xf[grp], par, abort))) break;   // the peer's partial is in X[grp]
+        // arm the next phase: the peer writes X[grp] again only after all of
+        // this group has read it and said so (below)
+        if (gtid == 0) mbar_arrive_expect_tx(&B.xf[grp], kXBytes);
+        ATTN_TRACE(grp, gt, 3, lane == 0 && q4 == 0);
+        uint32_t vm_lo, vm_hi;
         if (pv) {
-          const int rem = n_valid - t * kNK - 32 * half;   // the valid entries of this tile form a prefix
-          vmask = rem >= 32 ? 0xffffffffu : (rem <= 0 ? 0u : (1u << rem) - 1u);
+          const int rem = n_valid - t * kNK;   // the valid entries of this tile form a prefix
+          vm_lo = rem >= 32 ? 0xffffffffu : (rem <= 0 ? 0u : (1u << rem) - 1u);
+          vm_hi = rem >= 64 ? 0xffffffffu : (rem <= 32 ? 0u : (1u << (rem - 32)) - 1u);
         } else {
-          vmask = __ballot_sync(0xffffffffu, s_e >= 0 && s_e <= pos);
+          vm_lo = __ballot_sync(0xffffffffu, s_e0 >= 0 && s_e0 <= pos);
+          vm_hi = __ballot_sync(0xffffffffu, s_e1 >= 0 && s_e1 <= pos);
         }
-        // online softmax in base 2 (s already holds x = scale * log2(e) * S)
+        // x = own (fp32) + peer (fp16).  The two CTAs' logits differ by the
+        // fp16 rounding of one partial; each CTA's half of O stays consistent
+        // with its own P and sum, which is all the normalisation needs.
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          s[j] = ((vmask >> j) & 1u) ? s[j] : -INFINITY;
-          m4[j & 3] = fmaxf(m4[j & 3], s[j]);
+        for (int jq = 0; jq < 8; ++jq) {
+          const uint4 v = X4[jq * 128 + h];
+          const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 p = f16x2_to_f32x2(pw[e]);
+            const int j = 8 * jq + 2 * e;
+            const uint32_t vm = j < 32 ? vm_lo : vm_hi;
+            x[j] = ((vm >> (j & 31)) & 1u) ? x[j] + p.x : -INFINITY;
+            x[j + 1] = ((vm >> ((j + 1) & 31)) & 1u) ? x[j + 1] + p.y : -INFINITY;
+            m4[e] = fmaxf(m4[e], fmaxf(x[j], x[j + 1]));
+          }
         }
-        const float mh = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-        B.red[b][half][h] = mh;
-        // X[b] consumed: the store above needs mh, which depends on every
-        // value loaded from X[b], and instructions issue in order, so this
-        // relaxed arrive follows those loads (a release-ordered remote arrive
+        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        // X[grp] consumed: the store below needs mt, which depends on every
+        // value loaded from X, and instructions issue in order, so the relaxed
+        // arrive after it follows those loads (a release-ordered remote arrive
         // costs ~1.5k clk)
-        mbar_arrive_remote_relaxed(xe_peer[b]);
-        // the pair's maxima (the barrier also orders both warps' S loads before any P store)
-        mbar_arrive(pair);
-        if (!(ok = mbar_wait(pair, pu & 1, abort))) break;
-        ++pu;
-        const float mt = fmaxf(B.red[b][0][h], B.red[b][1][h]);
-        float alpha = 1.f;
-        bool rescale = false;
-        if (mt > m_use + 8.f) {
-          alpha = ex2_approx(m_use - mt);
-          m_use = mt;
-          rescale = true;
+        B.mtile[grp][h] = mt;
+        mbar_arrive_remote_relaxed(xe_peer);
+        // the running maximum after tile gt-1 (waiting also at a query's first
+        // tile keeps the two groups within one tile of each other)
+        float m_prev = -INFINITY;
+        if (gt > 0) {
+          if (!(ok = mbar_wait(&B.mdone[grp ^ 1], ((gt - 1) >> 1) & 1, abort))) break;
+          if (t > 0) m_prev = B.mpub[grp ^ 1][h];
+        }
+        // lazy rescaling: the maximum used only moves when exceeded by more than 8 (a factor 256)
+        const float m_use = mt > m_prev + 8.f ? mt : m_prev;
+        B.mpub[grp][h] = m_use;
+        mbar_arrive(&B.mdone[grp]);
+        if (m_use != m_seen) {   // this group's sum follows the maximum
+          l *= ex2_approx(m_seen - m_use);
+          m_seen = m_use;
         }
         const float msub = m_use == -INFINITY ? 0.f : m_use;   // all p are 0 while nothing is valid
-        uint32_t pk[16];
+        uint32_t pk[32];
         float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float p0 = ex2_approx(s[j] - msub);
-          const float p1 = ex2_approx(s[j + 1] - msub);
+        for (int j = 0; j < 64; j += 2) {
+          const float p0 = ex2_approx(x[j] - msub);
+          const float p1 = ex2_approx(x[j + 1] - msub);
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          ps4[(j >> 1) & 3] += __low2float(pb) + __high2float(pb);
+          ps4[(j >> 1) & 3] += p0 + p1;   // the sum of the fp32 probabilities
           pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
         }
-        l = l * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
-        ATTN_TRACE(half, g, 4, lane == 0 && q4 == 0);
-        if (rescale && t > 0) {
-          // O holds the P.V of tiles < g; that of tile g-1 must be complete
-          if (!(ok = mbar_wait(&B.pv_done[b ^ 1], ((g - 1) >> 1) & 1, abort))) break;
+        l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+        ATTN_TRACE(grp, gt, 4, lane == 0 && q4 == 0);
+        if (t > 0 && m_use != m_prev) {
+          // O holds the P.V of tiles < gt relative to m_prev; that of tile gt-1 must be complete
+          if (!(ok = mbar_wait(&B.pv_done[grp ^ 1], ((gt - 1) >> 1) & 1, abort))) break;
           tc_fence_after();
+          const float alpha = ex2_approx(m_prev - m_use);
 #pragma unroll 1
-          for (int c = 0; c < 128; c += 16) {
+          for (int c = 0; c < 256; c += 16) {
             uint32_t r[16];
-            tmem_ld16(tmem + lane_base + kTmemO + half * 128 + c, r);
+            tmem_ld16(tmem + lane_base + kTmemO + c, r);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-            tmem_st16(tmem + lane_base + kTmemO + half * 128 + c, r);
+            tmem_st16(tmem + lane_base + kTmemO + c, r);
           }
         }
-        // P of this half: keys 32*half.. -> TMEM columns kTmemS + 64b + 16*half (bf16 pairs)
-        tmem_st16(tmem + lane_base + kTmemS + b * 64 + half * 16, pk);
+        // P -> TMEM columns 0..31 of the tile's S buffer (bf16 pairs)
+        {
+          uint32_t lo[16], hi[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            lo[j] = pk[j];
+            hi[j] = pk[16 + j];
+          }
+          tmem_st16(tS, lo);
+          tmem_st16(tS + 16, hi);
+        }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&B.p_full[b]);
-        ATTN_TRACE(half, g, 5, lane == 0 && q4 == 0);
+        mbar_arrive(&B.p_full[grp]);
+        ATTN_TRACE(grp, gt, 5, lane == 0 && q4 == 0);
       }
+      g = g0 + nt;
       if (!ok) break;
-      // epilogue: this half of the O row of this head, normalised, bf16
-      B.red[2][half][h] = l;
-      mbar_arrive(pair);
-      if (!mbar_wait(pair, pu & 1, abort)) break;
-      ++pu;
-      const float lt = B.red[2][0][h] + B.red[2][1][h];
+      // epilogue: the two groups' sums relative to the final maximum; each
+      // group normalises and stores half of this CTA's O columns
+      const int qb2 = qv & 1;
+      B.lsum[qb2][grp][h] = l;
+      B.mseen[qb2][grp][h] = m_seen;
+      mbar_arrive(&B.qend);
+      if (!mbar_wait(&B.qend, qb2, abort)) break;
+      const float ma = B.mseen[qb2][0][h], mb = B.mseen[qb2][1][h];
+      const float mf = fmaxf(ma, mb);
+      const float lt = mf == -INFINITY ? 0.f
+                                       : B.lsum[qb2][0][h] * ex2_approx(ma - mf) + B.lsum[qb2][1][h] * ex2_approx(mb - mf);
       if (!mbar_wait(&B.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort)) break;
       tc_fence_after();
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
@@ -360,7 +379,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
 #pragma unroll 1
       for (int c = 0; c < 128; c += 16) {
         uint32_t r[16];
-        tmem_ld16(tmem + lane_base + kTmemO + half * 128 + c, r);
+        tmem_ld16(tmem + lane_base + kTmemO + grp * 128 + c, r);
         tmem_ld_wait();
         uint32_t w[8];
 #pragma unroll
@@ -372,9 +391,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         o4[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
         o4[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
-      if (crank == 0 && half == 0) lse[(int64_t)i * kH + h] = lt > 0.f ? (m_use + log2f(lt)) * kLn2 : -INFINITY;
+      if (crank == 0 && grp == 0) lse[(int64_t)i * kH + h] = lt > 0.f ? (mf + log2f(lt)) * kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(&B.o_empty);
+      ++qv;
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ gather (cp.async) + Q (TMA)
