@@ -28,17 +28,17 @@
 //     128B-swizzled latent slots and a 64B-swizzled rope half.  (TMA
 //     tile::gather4 measured ~64 clk per 4-row instruction on B300, slower
 //     than this path.)  Heads are the MMA's M (=128); per tile each CTA issues 18 MMAs
-//     128x64x16 for S and 4 MMAs 128x256x16 for P.V.  P (bf16) is written
-//     back into TMEM over the tile's S columns and is the A operand of the
-//     P.V MMAs; V is read MN-major straight out of the gathered K-major
-//     latent slots.
+//     128x64x16 for S and 4 MMAs 128x256x16 for P.V, with V read MN-major
+//     straight out of the gathered K-major latent slots.  An S buffer is
+//     released as soon as its tile's scores are loaded (P goes through
+//     shared memory), so score MMAs run ahead of the softmax.
 //   * Warp roles per CTA: 0-7 exchange + softmax + epilogue in two groups
 //     that take alternate tiles (thread = head = TMEM lane), so that one
 //     group computes while the other waits for the peer's partial logits,
 //     8-13 gather (three groups of two warps, group j
 //     fills the tiles g = j mod 3 into KV stage g mod 4; at each query warps 8-11
 //     write Q's latent part into TMEM and warp 8 loads the rope part with
-//     TMA), 14 TMEM owner + MMA issuer.
+//     TMA), 14 TMEM owner + score MMA issuer, 15 P.V MMA issuer.
 //     Persistent: cluster j handles queries j, j+C, ...
 //   * Lazy rescaling: the running max used for the exponent only moves when
 //     a tile's max exceeds it by more than 8 (a factor 256).
@@ -65,12 +65,14 @@ constexpr int kStages = 4;
 constexpr uint32_t kOffQRope = 0;
 constexpr uint32_t kOffKV = kOffQRope + kQRopeBytes;       // 8 KB
 constexpr uint32_t kOffX = kOffKV + kStages * kKVStageBytes;   // 152 KB
-constexpr uint32_t kSmemBytes = kOffX + 2 * kXBytes;       // 184 KB
+constexpr uint32_t kPBytes = kH * 128;                     // 128 x 64 bf16 probabilities (SW128)
+constexpr uint32_t kOffP = kOffX + 2 * kXBytes;            // 184 KB: P[0], P[1]
+constexpr uint32_t kSmemBytes = kOffP + 2 * kPBytes;       // 216 KB
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;         // + alignment slack
 constexpr int kGatherWarp0 = 8;
 constexpr int kGatherGroups = 3;                           // of two warps; group j gathers the tiles g = j mod 3
-constexpr int kMmaWarp = kGatherWarp0 + 2 * kGatherGroups; // 14
-constexpr int kThreads = (kMmaWarp + 1) * 32;              // 480: at most 4 warps per SM sub-partition
+constexpr int kMmaWarp = kGatherWarp0 + 2 * kGatherGroups; // 14: TMEM owner, score MMAs; 15: P.V MMAs
+constexpr int kThreads = (kMmaWarp + 2) * 32;              // 512: at most 4 warps per SM sub-partition
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 384;  // S buffer b at kTmemS + 64 b
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -92,8 +94,8 @@ __device__ long long g_attn_trace[4][512][8];
 
 struct Bars {
   uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], xf[2], xe[2];
-  uint64_t p_full[2], pv_done[2], mdone[2];
-  uint64_t q_full, q_empty, o_empty, qend, fin;
+  uint64_t s_empty[2], p_full[2], pv_done[2], mdone[2];
+  uint64_t q_full, q_empty, o_empty, qend, fin[2];
   float mtile[2][128];          // [group][head] scratch: the tile maximum
   float mpub[2][128];           // [tile parity][head] running maximum after the group's latest tile
   float lsum[2][2][128];        // [query parity][group][head] the groups' sums at the end of a query
@@ -171,10 +173,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       mbar_init(&B.p_full[s], 128);
       mbar_init(&B.pv_done[s], 1);
       mbar_init(&B.mdone[s], 128);
+      mbar_init(&B.s_empty[s], 128);   // the softmax group of this parity has loaded S
     }
     mbar_init(&B.o_empty, 256);
     mbar_init(&B.qend, 256);
-    mbar_init(&B.fin, 1);
+    mbar_init(&B.fin[0], 1);
+    mbar_init(&B.fin[1], 1);
     B.abort = 0;
     fence_mbar_init();
     mbar_arrive_expect_tx(&B.xf[0], kXBytes);   // arm the first phase of both receive tiles
@@ -189,7 +193,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
   cluster_sync();   // the peer's barriers exist before anyone arrives on them remotely
   tc_fence_after();
   const uint32_t tmem = B.tmem_base;
-  const uint32_t sQr = smem_u32(sm + kOffQRope), sKV = smem_u32(sm + kOffKV);
+  const uint32_t sQr = smem_u32(sm + kOffQRope), sKV = smem_u32(sm + kOffKV), sP = smem_u32(sm + kOffP);
 
   if (warp < 8) {
     // ------------------------------------------------------------ exchange, softmax, epilogue
@@ -200,8 +204,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     // maximum passes from tile to tile (so from group to group) through
     // shared memory; each group keeps its own running sum, relative to the
     // maximum it last saw, and the two sums meet at the end of the query.
-    // P (bf16) goes back into TMEM over the tile's S columns: the A operand
-    // of the P.V MMA.
+    // The S buffer is released as soon as the group has loaded it, so the
+    // score MMAs of later tiles do not wait for this tile's P.V; P (bf16)
+    // goes to shared memory, the A operand of the P.V MMA.
     const int grp = warp >> 2, q4 = warp & 3;
     const int h = (q4 << 5) | lane;
     const int gtid = tid & 127;
@@ -251,6 +256,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
 #pragma unroll
           for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(r[j >> 4][j & 15]) * scale_log2;
         }
+        tc_fence_before();
+        mbar_arrive(&B.s_empty[grp]);   // S(gt+2) may be computed into this buffer
         ATTN_TRACE(grp, gt, 1, lane == 0 && q4 == 0);
         // own partial -> the peer's X[grp], once the peer has consumed what we wrote there two tiles ago
         if (!(ok = mbar_wait<true>(&B.xe[grp], par ^ 1, abort))) break;
@@ -343,18 +350,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
             tmem_st16(tmem + lane_base + kTmemO + c, r);
           }
         }
-        // P -> TMEM columns 0..31 of the tile's S buffer (bf16 pairs)
+        // P -> shared memory (SW128, row = head); P[grp] is free once the
+        // P.V of tile gt-2 has completed
+        if (!(ok = mbar_wait(&B.pv_done[grp], par ^ 1, abort))) break;
         {
-          uint32_t lo[16], hi[16];
+          uint8_t* prow = sm + kOffP + grp * kPBytes;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            lo[j] = pk[j];
-            hi[j] = pk[16 + j];
-          }
-          tmem_st16(tS, lo);
-          tmem_st16(tS + 16, hi);
+          for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<uint4*>(prow + sw128_offset(h, cc)) =
+                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         }
-        tmem_st_wait();
+        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&B.p_full[grp]);
         ATTN_TRACE(grp, gt, 5, lane == 0 && q4 == 0);
@@ -494,34 +500,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       if (!ok) break;
       ++qv;
     }
-  } else {
-    // ------------------------------------------------------------ MMA issue (warp 14, lane 0 issues)
-    // Order per tile g: the score MMAs of g, then the P.V of g-1 as soon as
-    // its P is ready (issuing score tiles further ahead was measured slower:
-    // they queue in front of the P.V in the tensor pipe).
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ score MMA issue (lane 0)
+    // S(g) goes into buffer g % 2 once the softmax group has loaded S(g-2)
+    // from it.  The tensor core accepts only a couple of MMAs ahead, so a
+    // second issuing warp lets the P.V MMAs slot in between the score MMAs
+    // instead of waiting behind them.
     const uint32_t id_s = idesc_bf16(128, kNK, false);
-    const uint32_t id_pv = idesc_bf16(128, 256, true);
     uint32_t g = 0, qv = 0;
-    auto issue_pv = [&](uint32_t gp, int tp) -> bool {
-      ATTN_TRACE(3, gp, 3, lane == 0);
-      if (!mbar_wait(&B.p_full[gp & 1], (gp >> 1) & 1, abort)) return false;
-      ATTN_TRACE(3, gp, 4, lane == 0);
-      if (tp == 0 && !mbar_wait(&B.o_empty, (qv & 1) ^ 1, abort)) return false;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t skv = sKV + (gp % kStages) * kKVStageBytes;
-        const uint32_t tp_col = tmem + kTmemS + 64 * (gp & 1);   // P (bf16 pairs) over the tile's S columns
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16_ts(tmem + kTmemO, tp_col + kk * 8, sdesc(skv + kk * 2048, kKVSlotBytes, 1024), id_pv,
-                      (tp > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&B.pv_done[gp & 1]);
-        mma_commit(&B.kv_empty[gp % kStages]);
-      }
-      __syncwarp();
-      ATTN_TRACE(3, gp, 6, lane == 0);
-      return true;
-    };
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
       const QueryInfo qi = query_info(qb, idx, k, i, pv);
       const int nt = qi.nt;
@@ -533,9 +519,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         ATTN_TRACE(3, g, 0, lane == 0);
         if (!(ok = mbar_wait(&B.kv_full[st], (g / kStages) & 1, abort))) break;
         ATTN_TRACE(3, g, 1, lane == 0);
-        // S buffer sb last held P(g-2): the P.V reading it was issued before
-        // this MMA (tensor-pipe order), and P(g-2) was written only after
-        // both warps of each pair had loaded S(g-2)
+        if (!(ok = mbar_wait(&B.s_empty[sb], ((g >> 1) & 1) ^ 1, abort))) break;
         ATTN_TRACE(3, g, 2, lane == 0);
         tc_fence_after();
         if (lane == 0) {
@@ -557,14 +541,48 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         }
         __syncwarp();
         ATTN_TRACE(3, g, 5, lane == 0);
-        if (t > 0 && !(ok = issue_pv(g - 1, t - 1))) break;
       }
-      if (!ok || !issue_pv(g - 1, nt - 1)) break;
+      if (!ok) break;
       ++qv;
     }
-    if (lane == 0) mma_commit(&B.fin);
+    if (lane == 0) mma_commit(&B.fin[0]);
     __syncwarp();
-    wait_fin(&B.fin);   // every MMA issued by this CTA has completed
+    wait_fin(&B.fin[0]);   // every MMA issued by this warp has completed
+  } else {
+    // ------------------------------------------------------------ P.V MMA issue (warp 15, lane 0)
+    const uint32_t id_pv = idesc_bf16(128, 256, true);
+    uint32_t g = 0, qv = 0;
+    for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
+      const QueryInfo qi = query_info(qb, idx, k, i, pv);
+      const int nt = qi.nt;
+      if (nt == 0) continue;
+      bool ok = true;
+      for (int t = 0; t < nt; ++t, ++g) {
+        ATTN_TRACE(3, g, 3, lane == 0);
+        if (!(ok = mbar_wait(&B.p_full[g & 1], (g >> 1) & 1, abort))) break;
+        ATTN_TRACE(3, g, 4, lane == 0);
+        // the epilogue of the previous query has read O
+        if (t == 0 && !(ok = mbar_wait(&B.o_empty, (qv & 1) ^ 1, abort))) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t skv = sKV + (g % kStages) * kKVStageBytes;
+          const uint32_t sp = sP + (g & 1) * kPBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16(tmem + kTmemO, sdesc(sp + kk * 32, 16, 1024), sdesc(skv + kk * 2048, kKVSlotBytes, 1024), id_pv,
+                     (t > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&B.pv_done[g & 1]);
+          mma_commit(&B.kv_empty[g % kStages]);
+        }
+        __syncwarp();
+        ATTN_TRACE(3, g, 6, lane == 0);
+      }
+      if (!ok) break;
+      ++qv;
+    }
+    if (lane == 0) mma_commit(&B.fin[1]);
+    __syncwarp();
+    wait_fin(&B.fin[1]);   // every MMA issued by this warp has completed
   }
 
   tc_fence_before();
