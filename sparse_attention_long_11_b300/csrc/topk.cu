@@ -3,69 +3,56 @@
 // DeepSeek-V3.2: the fine-grained selector keeps the top-k key/value
 // positions of every query).
 //
-// One 1024-thread block per query row.  Scores become order-preserving
-// 32-bit keys (-0 folded onto +0).  A three-round radix select (11 + 11 + 10
-// bits, shared-memory histograms) finds the exact key T of the k-th largest
-// candidate and how many candidates equal to T are still needed.  An ordered
-// compaction then writes, in ascending position, every candidate above T and
-// the lowest-positioned `need` candidates equal to T: ties resolve to the
-// lower position and the selected set is unique.  Rows of up to
-// kCacheCap candidates keep their keys in shared memory; longer rows are
-// re-read from global memory on every round.
+// One block per query row.  Scores become order-preserving 32-bit keys (-0
+// folded onto +0).  A three-round radix select (11 + 11 + 10 bits,
+// shared-memory histograms) finds the exact key T of the k-th largest
+// candidate and how many candidates equal to T are still needed.  The first
+// round reads the whole row; the two finer rounds run over the keys of the
+// threshold bin alone, gathered into a compact list (or over the whole row
+// when that bin is very large).  An ordered compaction then writes, in
+// ascending position, every candidate above T and the lowest-positioned
+// `need` candidates equal to T: ties resolve to the lower position and the
+// selected set is unique.
+//
+// Rows are read with 16-byte loads straight from global memory on every
+// pass: inside the fused forward they were just written by the indexer and
+// sit in L2.  Keeping no per-row cache in shared memory lets several rows
+// (blocks of 256 threads) share an SM, so one row's barriers and load
+// latencies hide behind the others'; batches with few rows use 1024-thread
+// blocks instead.
 #include "launch.h"
 
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
-constexpr int kCacheCap = 40960;   // keys cached in shared memory (160 KiB)
-constexpr int kCandCap = 8192;     // threshold-bin keys gathered for the finer rounds (32 KiB)
+constexpr int kCandCap = 8192;   // threshold-bin keys gathered for the finer rounds (32 KiB)
+constexpr int kManyRowsThreads = 256, kFewRowsThreads = 1024;
 
+template <int NT>
 __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t* warp_tot) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+    const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += t;
   }
   if (lane == 31) warp_tot[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    uint32_t t = warp_tot[lane];
+    uint32_t t = lane < NW ? warp_tot[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      uint32_t u = __shfl_up_sync(0xffffffffu, t, o);
+      const uint32_t u = __shfl_up_sync(0xffffffffu, t, o);
       if (lane >= o) t += u;
     }
-    warp_tot[lane] = t;   // inclusive over warps
+    if (lane < NW) warp_tot[lane] = t;   // inclusive over warps
   }
   __syncthreads();
-  uint32_t r = v + (warp > 0 ? warp_tot[warp - 1] : 0u);
+  const uint32_t r = v + (warp > 0 ? warp_tot[warp - 1] : 0u);
   __syncthreads();
   return r;
-}
-
-// Selects, among the nb bins of `hist` (counts of candidates sharing a
-// digit), the one holding the krem-th largest candidate: sets *sel_bin and
-// *sel_above (candidates in higher bins).  Thread t owns the bins of
-// descending rank 2t and 2t+1.  Ends with a barrier.
-__device__ __forceinline__ void select_bin(const uint32_t* hist, int nb, uint32_t krem, uint32_t* warp_tot,
-                                           uint32_t* sel_bin, uint32_t* sel_above) {
-  const int tid = threadIdx.x;
-  const int b0 = nb - 1 - 2 * tid, b1 = b0 - 1;
-  const uint32_t h0 = b0 >= 0 ? hist[b0] : 0u, h1 = b1 >= 0 ? hist[b1] : 0u;
-  const uint32_t incl = block_incl_scan(h0 + h1, warp_tot);
-  const uint32_t excl = incl - h0 - h1;
-  if (excl < krem && krem <= excl + h0) {
-    *sel_bin = (uint32_t)b0;
-    *sel_above = excl;
-  } else if (excl + h0 < krem && krem <= incl) {
-    *sel_bin = (uint32_t)b1;
-    *sel_above = excl + h0;
-  }
-  __syncthreads();
 }
 
 // Warp-wide exclusive prefix sum of v (and the warp total in *tot).
@@ -81,17 +68,45 @@ __device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, uint32_t* tot) {
   return x - v;
 }
 
-// Keys of candidates j .. j+3 (j a multiple of 4; entries >= n are don't-care).
+// Selects, among the nb bins of `hist` (counts of candidates sharing a
+// digit), the one holding the krem-th largest candidate: sets *sel_bin and
+// *sel_above (candidates in higher bins).  Thread t owns the nb / NT bins of
+// descending rank nb/NT * t onwards.  Ends with a barrier.
+template <int NT>
+__device__ __forceinline__ void select_bin(const uint32_t* hist, int nb, uint32_t krem, uint32_t* warp_tot,
+                                           uint32_t* sel_bin, uint32_t* sel_above) {
+  constexpr int BMAX = kBins / NT;
+  const int tid = threadIdx.x;
+  const int nper = nb / NT;   // nb is 2048 or 1024, NT at most 1024: at least one bin each
+  uint32_t h[BMAX], sum = 0;
+#pragma unroll
+  for (int r = 0; r < BMAX; ++r) {
+    h[r] = r < nper ? hist[nb - 1 - (nper * tid + r)] : 0u;
+    sum += h[r];
+  }
+  const uint32_t incl = block_incl_scan<NT>(sum, warp_tot);
+  const uint32_t excl = incl - sum;
+  if (excl < krem && krem <= incl) {   // exactly one thread's bins hold the krem-th candidate
+    uint32_t c = excl;
+#pragma unroll
+    for (int r = 0; r < BMAX; ++r) {
+      if (r < nper && c < krem && krem <= c + h[r]) {
+        *sel_bin = (uint32_t)(nb - 1 - (nper * tid + r));
+        *sel_above = c;
+      }
+      c += h[r];
+    }
+  }
+  __syncthreads();
+}
+
+// Keys of candidates j .. j+3 of one score row (j a multiple of 4; entries
+// >= n read as 0 and must be masked by the caller).
 struct RowKeys {
   const float* row;
-  const uint32_t* skey;
   int n;
-  bool cached, vec;
+  bool vec;   // row start 16-byte aligned
   __device__ __forceinline__ uint4 load4(int j) const {
-    if (cached) return *reinterpret_cast<const uint4*>(skey + j);
-    return load4_global(j);
-  }
-  __device__ __forceinline__ uint4 load4_global(int j) const {
     if (vec && j + 3 < n) {
       const float4 x = __ldg(reinterpret_cast<const float4*>(row + j));
       return make_uint4(score_key(x.x), score_key(x.y), score_key(x.z), score_key(x.w));
@@ -103,16 +118,16 @@ struct RowKeys {
   }
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
-topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k,
-            int32_t* __restrict__ idx, int cache_cap, int* err) {
-  extern __shared__ __align__(16) uint32_t smem[];   // [cache_cap] keys, then [kCandCap] candidates
-  uint32_t* skey = smem;
-  uint32_t* cand = smem + cache_cap;
+template <int NT>
+__global__ void __launch_bounds__(NT)
+topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, int32_t* __restrict__ idx,
+            int* err) {
+  constexpr int NW = NT / 32;
   __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t cand[kCandCap];
   __shared__ uint32_t warp_tot[32];
   __shared__ uint32_t sel_bin, sel_above, n_cand;
-  __shared__ uint32_t w_gt[kWarps], w_eq[kWarps], w_selbase[kWarps], w_eqbase[kWarps];
+  __shared__ uint32_t w_gt[NW], w_eq[NW], w_selbase[NW], w_eqbase[NW];
 
   const int i = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -120,44 +135,46 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k,
   const int pos = __ldg(qb.q_pos + i);
   if (pos < 0 || pos >= qb.max_kv) {
     if (tid == 0) flag_error(err, DSA_ERR_BOUNDS);
-    for (int j = tid; j < k; j += kThreads) out[j] = -1;
+    for (int j = tid; j < k; j += NT) out[j] = -1;
     return;
   }
   const int n = pos + 1;
   if (n <= k) {
-    for (int j = tid; j < k; j += kThreads) out[j] = j < n ? j : -1;
+    for (int j = tid; j < k; j += NT) out[j] = j < n ? j : -1;
     return;
   }
   const float* row = scores + (int64_t)i * ld;
-  const bool cached = n <= cache_cap;
-  const bool vec = (reinterpret_cast<uintptr_t>(row) & 15) == 0;
-  const RowKeys rk{row, skey, n, cached, vec};
+  const RowKeys rk{row, n, (reinterpret_cast<uintptr_t>(row) & 15) == 0};
   const int n4 = (n + 3) >> 2;   // groups of four candidates
 
-  // ---- round 0: histogram of the top 11 bits over the whole row (keys cached on the way)
-  for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
-  if (tid == 0) n_cand = 0;
+  // ---- round 0: histogram of the top 11 bits over the whole row
+  for (int b = tid; b < kBins; b += NT) hist[b] = 0;
+  if (tid == 0) {
+    n_cand = 0;
+    sel_bin = 0;   // always overwritten by a consistent select; never left undefined
+    sel_above = 0;
+  }
   __syncthreads();
 #pragma unroll 1
-  for (int q0 = tid; q0 < n4; q0 += 2 * kThreads) {
-    const int q1 = q0 + kThreads;
-    // both loads in flight before any use; round 0 always reads the scores themselves
-    const uint4 a = rk.load4_global(4 * q0);
-    const uint4 c = q1 < n4 ? rk.load4_global(4 * q1) : make_uint4(0, 0, 0, 0);
-    const uint32_t ua[4] = {a.x, a.y, a.z, a.w}, uc[4] = {c.x, c.y, c.z, c.w};
-    if (cached) {
-      reinterpret_cast<uint4*>(skey)[q0] = a;
-      if (q1 < n4) reinterpret_cast<uint4*>(skey)[q1] = c;
+  for (int q = tid; q < n4; q += 4 * NT) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {   // four 16-byte loads in flight before any use
+      const int qq = q + u * NT;
+      v[u] = qq < n4 ? rk.load4(4 * qq) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (4 * q0 + e < n) atomicAdd(&hist[ua[e] >> 21], 1u);
-      if (q1 < n4 && 4 * q1 + e < n) atomicAdd(&hist[uc[e] >> 21], 1u);
+    for (int u = 0; u < 4; ++u) {
+      const int qq = q + u * NT;
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (qq < n4 && 4 * qq + e < n) atomicAdd(&hist[w[e] >> 21], 1u);
     }
   }
   __syncthreads();
   uint32_t krem = (uint32_t)k;
-  select_bin(hist, kBins, krem, warp_tot, &sel_bin, &sel_above);
+  select_bin<NT>(hist, kBins, krem, warp_tot, &sel_bin, &sel_above);
   uint32_t prefix = sel_bin << 21, pmask = 0xffe00000u;
   krem -= sel_above;
   const uint32_t c1 = hist[sel_bin];   // candidates in the threshold bin (>= 1)
@@ -168,7 +185,7 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k,
   const bool compact = c1 <= (uint32_t)kCandCap;
   if (compact) {
 #pragma unroll 1
-    for (int q = tid; q - tid < n4; q += kThreads) {   // warp-uniform bound: every lane takes part in the scan
+    for (int q = tid; q - tid < n4; q += NT) {   // warp-uniform bound: every lane takes part in the scan
       uint4 v = make_uint4(0, 0, 0, 0);
       if (q < n4) v = rk.load4(4 * q);
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
@@ -191,15 +208,15 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k,
   for (int round = 1; round < 3; ++round) {
     const int shift = round == 1 ? 10 : 0;
     const int nb = round == 1 ? 2048 : 1024;
-    for (int b = tid; b < kBins; b += kThreads) hist[b] = 0;
+    for (int b = tid; b < kBins; b += NT) hist[b] = 0;
     __syncthreads();
     if (compact) {
-      for (int j = tid; j < (int)c1; j += kThreads) {
+      for (int j = tid; j < (int)c1; j += NT) {
         const uint32_t u = cand[j];
         if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
       }
     } else {
-      for (int q = tid; q < n4; q += kThreads) {
+      for (int q = tid; q < n4; q += NT) {
         const uint4 v = rk.load4(4 * q);
         const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -208,7 +225,7 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k,
       }
     }
     __syncthreads();
-    select_bin(hist, nb, krem, warp_tot, &sel_bin, &sel_above);
+    select_bin<NT>(hist, nb, krem, warp_tot, &sel_bin, &sel_above);
     prefix |= sel_bin << shift;
     pmask |= (uint32_t)(nb - 1) << shift;
     krem -= sel_above;
@@ -219,7 +236,7 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k,
 
   // ---- ordered compaction: warp w owns the contiguous segment [w*seg, (w+1)*seg)
   // (seg a multiple of 128: each warp step covers 128 candidates, four per lane)
-  const int seg = ((n + kWarps - 1) / kWarps + 127) & ~127;
+  const int seg = ((n + NW - 1) / NW + 127) & ~127;
   const int beg = warp * seg, end = min(n, beg + seg);
   uint32_t gt = 0, eq = 0;
   for (int j = beg + 4 * lane; j < end; j += 128) {
@@ -237,18 +254,24 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k,
     gt += __shfl_xor_sync(0xffffffffu, gt, o);
     eq += __shfl_xor_sync(0xffffffffu, eq, o);
   }
-  if (lane == 0) { w_gt[warp] = gt; w_eq[warp] = eq; }
+  if (lane == 0) {
+    w_gt[warp] = gt;
+    w_eq[warp] = eq;
+  }
   __syncthreads();
   if (warp == 0) {
     // exclusive scans over the warps: equal keys before each segment, and
     // selected entries before it (all greater keys + the first `need` equal ones)
-    const uint32_t e_w = w_eq[lane], g_w = w_gt[lane];
+    const uint32_t e_w = lane < NW ? w_eq[lane] : 0u, g_w = lane < NW ? w_gt[lane] : 0u;
     uint32_t e_tot;
     const uint32_t e_ex = warp_excl_scan(e_w, &e_tot);
     const uint32_t take = need > e_ex ? min(need - e_ex, e_w) : 0u;
     uint32_t s_tot;
-    w_selbase[lane] = warp_excl_scan(g_w + take, &s_tot);
-    w_eqbase[lane] = e_ex;
+    const uint32_t s_ex = warp_excl_scan(g_w + take, &s_tot);
+    if (lane < NW) {
+      w_selbase[lane] = s_ex;
+      w_eqbase[lane] = e_ex;
+    }
   }
   __syncthreads();
   uint32_t eq_run = w_eqbase[warp], sel_run = w_selbase[warp];
@@ -287,15 +310,28 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k,
   }
 }
 
+int sm_count_topk() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const QueryBatch& qb, const float* scores, int64_t ld, int k, int32_t* idx,
                         int* err, cudaStream_t stream) {
-  int cap = qb.max_kv <= kCacheCap ? ((qb.max_kv + 3) & ~3) : 0;   // a multiple of 4: the list behind it stays 16-B aligned
-  size_t smem = ((size_t)cap + kCandCap) * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  topk_kernel<<<qb.num_q, kThreads, smem, stream>>>(qb, scores, ld, k, idx, cap, err);
+  // many rows: small blocks, several per SM; few rows: wide blocks
+  if (qb.num_q >= 2 * sm_count_topk())
+    topk_kernel<kManyRowsThreads><<<qb.num_q, kManyRowsThreads, 0, stream>>>(qb, scores, ld, k, idx, err);
+  else
+    topk_kernel<kFewRowsThreads><<<qb.num_q, kFewRowsThreads, 0, stream>>>(qb, scores, ld, k, idx, err);
   return cudaGetLastError();
 }
 
