@@ -4,29 +4,34 @@
 // positions of every query).
 //
 // One block per query row.  Scores become order-preserving 32-bit keys (-0
-// folded onto +0).  A three-round radix select (11 + 11 + 10 bits,
-// shared-memory histograms) finds the exact key T of the k-th largest
-// candidate and how many candidates equal to T are still needed.  The first
-// round reads the whole row; the two finer rounds run over the keys of the
-// threshold bin alone, gathered into a compact list (or over the whole row
-// when that bin is very large).  An ordered compaction then writes, in
-// ascending position, every candidate above T and the lowest-positioned
-// `need` candidates equal to T: ties resolve to the lower position and the
-// selected set is unique.
+// folded onto +0).
 //
-// Rows are read with 16-byte loads straight from global memory on every
-// pass: inside the fused forward they were just written by the indexer and
-// sit in L2.  Keeping no per-row cache in shared memory lets several rows
-// (blocks of 256 threads) share an SM, so one row's barriers and load
-// latencies hide behind the others'; batches with few rows use 1024-thread
-// blocks instead.
+//   1. A threshold guess G: of 1024 evenly spaced samples of the row, the
+//      r-th largest, r a few standard deviations above the expected rank of
+//      the k-th largest key (1024 k / n).
+//   2. One pass over the row collects every key >= G with its position into
+//      a per-warp list (warp w owns a contiguous segment, so the lists hold
+//      positions in ascending order).  With at least k of them, the row's
+//      top k are all among them.
+//   3. Three radix rounds (11 + 11 + 10 bits) over the collected keys find
+//      the exact key T of the k-th largest and how many keys equal to T are
+//      still needed; the output is every collected key above T and the
+//      lowest-positioned `need` keys equal to T, in ascending position: ties
+//      resolve to the lower position and the selected set is unique.
+//
+// When the guess misses (fewer than k collected, or a list overflows) the
+// block falls back to the same radix rounds over the whole row, followed by
+// an ordered compaction of the whole row.  Rows are read with 16-byte loads
+// straight from global memory: inside the fused forward they were just
+// written by the indexer and sit in L2.  Blocks of 256 threads let several
+// rows share an SM; batches with few rows use 1024-thread blocks instead.
 #include "launch.h"
 
 namespace dsa {
 namespace {
 
 constexpr int kBins = 2048;
-constexpr int kCandCap = 8192;   // threshold-bin keys gathered for the finer rounds (32 KiB)
+constexpr int kCandCap = 6144;   // threshold-bin keys gathered for the finer rounds (the candidate-list buffer)
 constexpr int kManyRowsThreads = 256, kFewRowsThreads = 1024;
 
 template <int NT>
@@ -77,11 +82,12 @@ __device__ __forceinline__ void select_bin(const uint32_t* hist, int nb, uint32_
                                            uint32_t* sel_bin, uint32_t* sel_above) {
   constexpr int BMAX = kBins / NT;
   const int tid = threadIdx.x;
-  const int nper = nb / NT;   // nb is 2048 or 1024, NT at most 1024: at least one bin each
+  const int nper = (nb + NT - 1) / NT;   // nb a power of two up to kBins: at most BMAX bins each
   uint32_t h[BMAX], sum = 0;
 #pragma unroll
   for (int r = 0; r < BMAX; ++r) {
-    h[r] = r < nper ? hist[nb - 1 - (nper * tid + r)] : 0u;
+    const int rank = nper * tid + r;
+    h[r] = (r < nper && rank < nb) ? hist[nb - 1 - rank] : 0u;
     sum += h[r];
   }
   const uint32_t incl = block_incl_scan<NT>(sum, warp_tot);
@@ -90,7 +96,7 @@ __device__ __forceinline__ void select_bin(const uint32_t* hist, int nb, uint32_
     uint32_t c = excl;
 #pragma unroll
     for (int r = 0; r < BMAX; ++r) {
-      if (r < nper && c < krem && krem <= c + h[r]) {
+      if (r < nper && nper * tid + r < nb && c < krem && krem <= c + h[r]) {
         *sel_bin = (uint32_t)(nb - 1 - (nper * tid + r));
         *sel_above = c;
       }
@@ -118,35 +124,37 @@ struct RowKeys {
   }
 };
 
+constexpr int kSamples = 1024;
+
+// Per-warp capacity of the candidate list (the list is 48 or 64 KiB of
+// dynamic shared memory: keys and positions).
+template <int NT> struct Region;   // per-warp list capacity; NW * kPerWarp >= kCandCap
+template <> struct Region<256> { static constexpr int kPerWarp = 768; };
+template <> struct Region<1024> { static constexpr int kPerWarp = 256; };
+
 template <int NT>
-__global__ void __launch_bounds__(NT)
-topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, int32_t* __restrict__ idx,
-            int* err) {
+struct TopkShared {
+  uint32_t sel_bin, sel_above, n_cand, overflow;
+  uint32_t w_cnt[NT / 32], w_gt[NT / 32], w_eq[NT / 32], w_selbase[NT / 32], w_eqbase[NT / 32];
+};
+
+// Exact selection over the whole row by radix rounds (used when the sampled
+// threshold misses): writes the row's output.  `cand` holds kCandCap keys.
+template <int NT>
+__device__ __noinline__ void radix_path(const RowKeys rk, int k, int32_t* __restrict__ out, int* err,
+                                        uint32_t* hist, uint32_t* cand, uint32_t* warp_tot, TopkShared<NT>& S) {
   constexpr int NW = NT / 32;
-  __shared__ uint32_t hist[kBins];
-  __shared__ uint32_t cand[kCandCap];
-  __shared__ uint32_t warp_tot[32];
-  __shared__ uint32_t sel_bin, sel_above, n_cand;
-  __shared__ uint32_t w_gt[NW], w_eq[NW], w_selbase[NW], w_eqbase[NW];
-
-  const int i = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int32_t* out = idx + (int64_t)i * k;
-  const int pos = __ldg(qb.q_pos + i);
-  if (pos < 0 || pos >= qb.max_kv) {
-    if (tid == 0) flag_error(err, DSA_ERR_BOUNDS);
-    for (int j = tid; j < k; j += NT) out[j] = -1;
-    return;
-  }
-  const int n = pos + 1;
-  if (n <= k) {
-    for (int j = tid; j < k; j += NT) out[j] = j < n ? j : -1;
-    return;
-  }
-  const float* row = scores + (int64_t)i * ld;
-  const RowKeys rk{row, n, (reinterpret_cast<uintptr_t>(row) & 15) == 0};
-  const int n4 = (n + 3) >> 2;   // groups of four candidates
-
+  const int n = rk.n;
+  const int n4 = (n + 3) >> 2;
+  uint32_t& sel_bin = S.sel_bin;
+  uint32_t& sel_above = S.sel_above;
+  uint32_t& n_cand = S.n_cand;
+  uint32_t* w_gt = S.w_gt;
+  uint32_t* w_eq = S.w_eq;
+  uint32_t* w_selbase = S.w_selbase;
+  uint32_t* w_eqbase = S.w_eqbase;
+  __syncthreads();
   // ---- round 0: histogram of the top 11 bits over the whole row
   for (int b = tid; b < kBins; b += NT) hist[b] = 0;
   if (tid == 0) {
@@ -310,6 +318,186 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, 
   }
 }
 
+// Exact k-th largest key of a list held in shared memory: three radix rounds
+// (11 + 11 + 10 bits) over the entries i < total for which get(i) is valid.
+// Returns the key T; *need = how many entries equal to T belong to the top k_rank.
+template <int NT, class Get>
+__device__ __forceinline__ uint32_t select_in_list(int total, Get get, uint32_t k_rank, uint32_t* hist,
+                                                   uint32_t* warp_tot, TopkShared<NT>& S, uint32_t* need) {
+  const int tid = threadIdx.x;
+  uint32_t prefix = 0, pmask = 0, krem = k_rank;
+#pragma unroll 1
+  for (int round = 0; round < 3; ++round) {
+    const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
+    const int nb = round == 2 ? 1024 : 2048;
+    for (int b = tid; b < kBins; b += NT) hist[b] = 0;
+    __syncthreads();
+    for (int i = tid; i < total; i += NT) {
+      uint32_t u;
+      if (get(i, u) && (u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    select_bin<NT>(hist, nb, krem, warp_tot, &S.sel_bin, &S.sel_above);
+    prefix |= S.sel_bin << shift;
+    pmask |= (uint32_t)(nb - 1) << shift;
+    krem -= S.sel_above;
+    __syncthreads();
+  }
+  *need = krem;
+  return prefix;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(NT)
+topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, int32_t* __restrict__ idx,
+            int* err) {
+  constexpr int NW = NT / 32;
+  constexpr int R = Region<NT>::kPerWarp;
+  extern __shared__ __align__(16) uint32_t dsm[];   // [NW * R] candidate keys, then [NW * R] positions
+  uint32_t* ckey = dsm;
+  uint32_t* cpos = dsm + NW * R;
+  __shared__ uint32_t hist[kBins];
+  __shared__ uint32_t samp[kSamples];
+  __shared__ uint32_t warp_tot[32];
+  __shared__ TopkShared<NT> S;
+
+  const int i = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int32_t* out = idx + (int64_t)i * k;
+  const int pos = __ldg(qb.q_pos + i);
+  if (pos < 0 || pos >= qb.max_kv) {
+    if (tid == 0) flag_error(err, DSA_ERR_BOUNDS);
+    for (int j = tid; j < k; j += NT) out[j] = -1;
+    return;
+  }
+  const int n = pos + 1;
+  if (n <= k) {
+    for (int j = tid; j < k; j += NT) out[j] = j < n ? j : -1;
+    return;
+  }
+  const float* row = scores + (int64_t)i * ld;
+  const RowKeys rk{row, n, (reinterpret_cast<uintptr_t>(row) & 15) == 0};
+
+  // ---- 1. a threshold guess from evenly spaced samples: the r-th largest
+  // sample, r a safe margin above the expected rank of the k-th largest key
+  for (int s = tid; s < kSamples; s += NT) samp[s] = score_key(__ldg(row + (int)(((int64_t)s * n) / kSamples)));
+  if (tid == 0) {
+    S.overflow = 0;
+    S.sel_bin = 0;   // always overwritten by a consistent select; never left undefined
+    S.sel_above = 0;
+  }
+  __syncthreads();
+  const float f = (float)kSamples * (float)k / (float)n;
+  const int r = min(kSamples, (int)ceilf(f + 4.f * sqrtf(f) + 16.f));
+  uint32_t unused;
+  const uint32_t G = select_in_list<NT>(kSamples, [&](int s, uint32_t& u) { u = samp[s]; return true; }, (uint32_t)r,
+                                        hist, warp_tot, S, &unused);
+
+  // ---- 2. one pass over the row: every key >= G with its position, into
+  // the warp's region of the list, in position order (warp w scans the
+  // contiguous segment [w*seg, (w+1)*seg); seg a multiple of 128, four
+  // candidates per lane and step)
+  const int seg = ((n + NW - 1) / NW + 127) & ~127;
+  const int beg = warp * seg, end = min(n, beg + seg);
+  uint32_t cnt = 0;
+  for (int j0 = beg; j0 < end; j0 += 128) {   // warp-uniform bound
+    const int j = j0 + 4 * lane;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (j < end) v = rk.load4(j);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (j + e < end && u[e] >= G) m |= 1u << e;
+    uint32_t tot;
+    uint32_t slot = cnt + warp_excl_scan(__popc(m), &tot);
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (m & (1u << e)) {
+        if (slot < (uint32_t)R) {
+          ckey[warp * R + slot] = u[e];
+          cpos[warp * R + slot] = (uint32_t)(j + e);
+        }
+        ++slot;
+      }
+    cnt += tot;
+  }
+  if (lane == 0) {
+    S.w_cnt[warp] = cnt;
+    if (cnt > (uint32_t)R) S.overflow = 1;
+  }
+  __syncthreads();
+  uint32_t total = 0;
+#pragma unroll 1
+  for (int w = 0; w < NW; ++w) total += S.w_cnt[w];
+  if (S.overflow || total < (uint32_t)k) {   // the guess missed (block-uniform): exact radix rounds over the row
+    radix_path<NT>(rk, k, out, err, hist, ckey, warp_tot, S);
+    return;
+  }
+
+  // ---- 3. the exact k-th largest key among the candidates (all keys >= G,
+  // at least k of them, so the row's top k are among them)
+  uint32_t need;
+  const uint32_t T = select_in_list<NT>(
+      NW * R,
+      [&](int c, uint32_t& u) {
+        const int w = c / R;
+        if ((uint32_t)(c - w * R) >= S.w_cnt[w]) return false;
+        u = ckey[c];
+        return true;
+      },
+      (uint32_t)k, hist, warp_tot, S, &need);
+
+  // ---- 4. ordered output: warp w walks its region (positions ascending)
+  uint32_t gt = 0, eq = 0;
+  for (uint32_t c = lane; c < cnt; c += 32) {
+    const uint32_t u = ckey[warp * R + c];
+    gt += u > T;
+    eq += u == T;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    gt += __shfl_xor_sync(0xffffffffu, gt, o);
+    eq += __shfl_xor_sync(0xffffffffu, eq, o);
+  }
+  if (lane == 0) {
+    S.w_gt[warp] = gt;
+    S.w_eq[warp] = eq;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t e_w = lane < NW ? S.w_eq[lane] : 0u, g_w = lane < NW ? S.w_gt[lane] : 0u;
+    uint32_t e_tot;
+    const uint32_t e_ex = warp_excl_scan(e_w, &e_tot);
+    const uint32_t take = need > e_ex ? min(need - e_ex, e_w) : 0u;
+    uint32_t s_tot;
+    const uint32_t s_ex = warp_excl_scan(g_w + take, &s_tot);
+    if (lane < NW) {
+      S.w_selbase[lane] = s_ex;
+      S.w_eqbase[lane] = e_ex;
+    }
+  }
+  __syncthreads();
+  uint32_t eq_run = S.w_eqbase[warp], sel_run = S.w_selbase[warp];
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (uint32_t c0 = 0; c0 < cnt; c0 += 32) {   // warp-uniform bound
+    const uint32_t c = c0 + lane;
+    uint32_t u = 0;
+    if (c < cnt) u = ckey[warp * R + c];
+    const bool is_eq = c < cnt && u == T;
+    const uint32_t eqb = __ballot_sync(0xffffffffu, is_eq);
+    const bool take = (c < cnt && u > T) || (is_eq && eq_run + __popc(eqb & lt_mask) < need);
+    const uint32_t selb = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const uint32_t slot = sel_run + __popc(selb & lt_mask);
+      if (slot < (uint32_t)k) out[slot] = (int32_t)cpos[warp * R + c];
+      else flag_error(err, DSA_ERR_BOUNDS);   // cannot happen for a consistent select; never write past the row
+    }
+    eq_run += __popc(eqb);
+    sel_run += __popc(selb);
+  }
+}
+
 int sm_count_topk() {
   static int cache[64] = {0};
   int dev = 0;
@@ -328,10 +516,19 @@ int sm_count_topk() {
 cudaError_t launch_topk(const QueryBatch& qb, const float* scores, int64_t ld, int k, int32_t* idx,
                         int* err, cudaStream_t stream) {
   // many rows: small blocks, several per SM; few rows: wide blocks
-  if (qb.num_q >= 2 * sm_count_topk())
-    topk_kernel<kManyRowsThreads><<<qb.num_q, kManyRowsThreads, 0, stream>>>(qb, scores, ld, k, idx, err);
-  else
-    topk_kernel<kFewRowsThreads><<<qb.num_q, kFewRowsThreads, 0, stream>>>(qb, scores, ld, k, idx, err);
+  if (qb.num_q >= 2 * sm_count_topk()) {
+    constexpr int NT = kManyRowsThreads;
+    const int smem = 2 * (NT / 32) * Region<NT>::kPerWarp * (int)sizeof(uint32_t);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    topk_kernel<NT><<<qb.num_q, NT, smem, stream>>>(qb, scores, ld, k, idx, err);
+  } else {
+    constexpr int NT = kFewRowsThreads;
+    const int smem = 2 * (NT / 32) * Region<NT>::kPerWarp * (int)sizeof(uint32_t);
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    topk_kernel<NT><<<qb.num_q, NT, smem, stream>>>(qb, scores, ld, k, idx, err);
+  }
   return cudaGetLastError();
 }
 
