@@ -23,9 +23,11 @@
 // block size is a multiple of 64 are read block by block.
 //
 // Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2..17 = epilogue
-// (warp w reads TMEM lane quadrant w%4 and handles query (w-2)/4 of the
-// group: four warps per quadrant keep enough independent work in flight to
-// hide the TMEM-load and FMA latencies).  All waits are bounded (see tc.cuh).
+// (warp w reads TMEM lane quadrant w%4; in a shared pass it sums the 64
+// heads of query (w-2)/4 of the group, in a per-query pass the four warps of
+// a quadrant take 16 heads each; both modes add four 16-head partials in
+// the same order, so a query's scores do not depend on its batch).  All
+// waits are bounded (see tc.cuh).
 #include <algorithm>
 #include <cstddef>
 
@@ -53,6 +55,8 @@ struct __align__(16) Shared {
   uint64_t a_full[kStagesA], a_empty[kStagesA], d_full[2], d_empty[2];
   uint64_t b_full[2], b_empty[2], epi_sync[2], fin;
   alignas(16) float wq[2][kQG][kHI];   // w * q_scale of the item's group (double buffered; read as float4)
+  uint64_t qred[4];                    // per TMEM lane quadrant: its four epilogue warps' partial head sums are in
+  float red[2][4][4][32];              // [use parity][quadrant][warp of the quadrant][lane] partial head sums
   uint32_t tmem_base;
   int abort;
 };
@@ -163,6 +167,25 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   return d;
 }
 
+// Weighted ReLU sum over 16 heads: r[i] is the raw score of head h0 + i,
+// w4[0..3] the folded weights of those heads.  Two packed accumulators
+// (heads 4m, 4m+1 and 4m+2, 4m+3), added at the end.
+__device__ __forceinline__ float head_partial(const uint32_t (&r)[16], const float4* w4) {
+  uint64_t a = 0ull, b = 0ull;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const float4 wv = w4[m];
+    a = ffma2(pack2(wv.x, wv.y),
+              pack2(fmaxf(__uint_as_float(r[4 * m]), 0.f), fmaxf(__uint_as_float(r[4 * m + 1]), 0.f)), a);
+    b = ffma2(pack2(wv.z, wv.w),
+              pack2(fmaxf(__uint_as_float(r[4 * m + 2]), 0.f), fmaxf(__uint_as_float(r[4 * m + 3]), 0.f)), b);
+  }
+  float alo, ahi, blo, bhi;
+  unpack2(a, alo, ahi);
+  unpack2(b, blo, bhi);
+  return (alo + ahi) + (blo + bhi);
+}
+
 __device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
   const long long t0 = clock64();
@@ -197,6 +220,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(&S.epi_sync[b], kEpiThreads);
     }
     mbar_init(&S.fin, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&S.qred[q], 128);
     S.abort = 0;
     fence_mbar_init();
   }
@@ -309,7 +333,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // ------------------------------------------------------------ epilogue
     const int qd = warp & 3, uq = (warp - 2) >> 2, et = tid - 64;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-    uint32_t g = 0, j = 0;
+    uint32_t g = 0, j = 0, nred = 0;   // tiles, items with tiles, uses of the quadrant barrier
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
       const int gi = item % ngroups, c = item / ngroups;
       Group G;
@@ -333,10 +357,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           pass_range(G, p, c, ch, t0, t1);
           for (int t = t0; t < t1; ++t, ++g) {
             const int b = g & 1;
-            IDX_TRACE(2, g, 0, et == 0);
-            if (!(ok = mbar_wait(&S.d_full[b], (g >> 1) & 1, abort))) break;
-            IDX_TRACE(2, g, 1, et == 0);
-            tc_fence_after();
+            // this lane's key and its scale, fetched before the wait so that
+            // the load (from HBM when every key is read once) overlaps the MMA
             const int s = t * kKT + qd * 32 + lane;
             float sk = 0.f;
             bool key_ok = s <= G.pass_maxpos[p];
@@ -345,42 +367,48 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               key_ok = row >= 0;
               if (key_ok) sk = __ldg(k_scale + row);
             }
-            // uniform: this warp's query; one pass per query otherwise (done by the uq == 0 warps)
-            if (uni || uq == 0) {
-              const int qq = uni ? uq : G.pass_q[p];
-              const uint32_t col = 256 * b + (uni ? qq * 64 : 0);
-              const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][qq]);
-              // packed fp32x2 FMAs: two heads per instruction, four independent accumulators
-              uint64_t a2[4] = {0ull, 0ull, 0ull, 0ull};
+            IDX_TRACE(2, g, 0, et == 0);
+            if (!(ok = mbar_wait(&S.d_full[b], (g >> 1) & 1, abort))) break;
+            IDX_TRACE(2, g, 1, et == 0);
+            tc_fence_after();
+            // The head sum is four 16-head partials added as (P0 + P1) + (P2 + P3)
+            // in both modes, so a query scores the same bits either way.
+            // uniform: this warp sums all 64 heads of its own query; per-query
+            // passes: the four warps of the quadrant take 16 heads each of the
+            // pass's query and meet in shared memory.
+            const int qq = uni ? uq : G.pass_q[p];
+            const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][qq]);
+            float acc = 0.f;
+            bool write = false;
+            if (uni) {
+              float P[4];
 #pragma unroll
-              for (int half = 0; half < 2; ++half) {
+              for (int uh = 0; uh < 2; ++uh) {   // two 16-column loads at a time
                 uint32_t r[2][16];
-                tmem_ld16(tmem + lane_base + col + half * 32, r[0]);
-                tmem_ld16(tmem + lane_base + col + half * 32 + 16, r[1]);
+                tmem_ld16(tmem + lane_base + 256 * b + qq * 64 + 32 * uh, r[0]);
+                tmem_ld16(tmem + lane_base + 256 * b + qq * 64 + 32 * uh + 16, r[1]);
                 tmem_ld_wait();
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-                  for (int j4 = 0; j4 < 4; ++j4) {
-                    const float4 wv = wq4[half * 8 + cc * 4 + j4];
-                    const int ai = (j4 & 1) * 2;
-                    a2[ai] = ffma2(pack2(wv.x, wv.y),
-                                   pack2(fmaxf(__uint_as_float(r[cc][4 * j4 + 0]), 0.f),
-                                         fmaxf(__uint_as_float(r[cc][4 * j4 + 1]), 0.f)),
-                                   a2[ai]);
-                    a2[ai + 1] = ffma2(pack2(wv.z, wv.w),
-                                       pack2(fmaxf(__uint_as_float(r[cc][4 * j4 + 2]), 0.f),
-                                             fmaxf(__uint_as_float(r[cc][4 * j4 + 3]), 0.f)),
-                                       a2[ai + 1]);
-                  }
+                P[2 * uh] = head_partial(r[0], wq4 + 8 * uh);
+                P[2 * uh + 1] = head_partial(r[1], wq4 + 8 * uh + 4);
               }
-              float acc = 0.f;
-              {
-                float lo[4], hi[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) unpack2(a2[u], lo[u], hi[u]);
-                acc = ((lo[0] + hi[0]) + (lo[1] + hi[1])) + ((lo[2] + hi[2]) + (lo[3] + hi[3]));
+              acc = (P[0] + P[1]) + (P[2] + P[3]);
+              write = true;
+            } else {
+              uint32_t r[16];
+              tmem_ld16(tmem + lane_base + 256 * b + 16 * uq, r);
+              tmem_ld_wait();
+              const int rb = nred & 1;
+              S.red[rb][qd][uq][lane] = head_partial(r, wq4 + 4 * uq);
+              mbar_arrive(&S.qred[qd]);
+              if (!(ok = mbar_wait(&S.qred[qd], nred & 1, abort))) break;
+              ++nred;
+              if (uq == 0) {
+                acc = (S.red[rb][qd][0][lane] + S.red[rb][qd][1][lane]) +
+                      (S.red[rb][qd][2][lane] + S.red[rb][qd][3][lane]);
+                write = true;
               }
+            }
+            if (write) {
               const int row_q = gi * kQG + qq;
               if (s < qb.max_kv && row_q < qb.num_q) {
                 const bool live = G.active[qq] && key_ok && s <= G.pos[qq];

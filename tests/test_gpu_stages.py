@@ -84,6 +84,41 @@ def test_topk_exact(kind, n, k):
         assert np.array_equal(got[i], want), f"row {i} pos {p}"
 
 
+@pytest.mark.parametrize("kind", ["normal", "ties", "const"])
+def test_topk_exact_many_rows(kind):
+    """Enough rows that the kernel runs several narrow blocks per SM."""
+    nq, n, k = 400, 6000, 2048
+    sc = inputs.make_scores(nq, n, seed=77, device=DEV, kind=kind)
+    pos = torch.linspace(0, n - 1, nq).round().to(torch.int32)
+    batch = api.Batch(torch.zeros(nq, dtype=torch.int32, device=DEV), pos.to(DEV), n)
+    idx = torch.empty((nq, k), dtype=torch.int32, device=DEV)
+    api.dsa_topk(batch.desc(), sc, k, idx)
+    assert api.dsa_check_device_error() == api.DSA_OK
+    got, s_np = idx.cpu().numpy(), sc.cpu().numpy()
+    for i in range(0, nq, 7):
+        p = int(pos[i])
+        assert np.array_equal(got[i], O.topk_select(s_np[i, :p + 1], k)), f"row {i} pos {p}"
+
+
+@pytest.mark.parametrize("nq", [4, 400])
+def test_topk_exact_when_evenly_spaced_positions_hold_the_largest_scores(nq):
+    """Rows whose largest scores sit exactly at evenly spaced positions (every
+    n/1024-th): a threshold estimated from such positions overshoots, and
+    the selection must still be exact."""
+    n, k = 70000, 2048
+    sc = inputs.make_scores(nq, n, seed=5, device=DEV)
+    s_pos = (torch.arange(1024, dtype=torch.int64) * n) // 1024
+    sc[:, s_pos.to(DEV)] += 100.0
+    pos = torch.full((nq,), n - 1, dtype=torch.int32)
+    batch = api.Batch(torch.zeros(nq, dtype=torch.int32, device=DEV), pos.to(DEV), n)
+    idx = torch.empty((nq, k), dtype=torch.int32, device=DEV)
+    api.dsa_topk(batch.desc(), sc, k, idx)
+    assert api.dsa_check_device_error() == api.DSA_OK
+    got, s_np = idx.cpu().numpy(), sc.cpu().numpy()
+    for i in range(0, nq, max(1, nq // 8)):
+        assert np.array_equal(got[i], O.topk_select(s_np[i], k)), f"row {i}"
+
+
 def test_topk_ignores_scores_beyond_position():
     n, k = 4096, 64
     sc = inputs.make_scores(2, n, seed=9, device=DEV)
