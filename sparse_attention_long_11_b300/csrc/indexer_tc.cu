@@ -22,12 +22,16 @@
 // Key tiles are loaded by TMA: 2 boxes of 64 rows, so paged caches whose
 // block size is a multiple of 64 are read block by block.
 //
+// An accumulator buffer holds one shared-pass tile (N = 256) or up to four
+// consecutive per-query tiles (N = 64 each, in 64-column slices), so that
+// per-query work (decode batches) keeps eight tiles in flight.
+//
 // Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2..17 = epilogue
-// (warp w reads TMEM lane quadrant w%4; in a shared pass it sums the 64
-// heads of query (w-2)/4 of the group, in a per-query pass the four warps of
-// a quadrant take 16 heads each; both modes add four 16-head partials in
-// the same order, so a query's scores do not depend on its batch).  All
-// waits are bounded (see tc.cuh).
+// (warp w reads TMEM lane quadrant w%4 and the 64 columns of slice (w-2)/4:
+// the slice's query of a shared pass, or the slice's own per-query tile).
+// A score is the sum of four 16-head partials in one fixed order in both
+// modes, so a query's scores do not depend on its batch.  All waits are
+// bounded (see tc.cuh).
 #include <algorithm>
 #include <cstddef>
 
@@ -55,8 +59,6 @@ struct __align__(16) Shared {
   uint64_t a_full[kStagesA], a_empty[kStagesA], d_full[2], d_empty[2];
   uint64_t b_full[2], b_empty[2], epi_sync[2], fin;
   alignas(16) float wq[2][kQG][kHI];   // w * q_scale of the item's group (double buffered; read as float4)
-  uint64_t qred[4];                    // per TMEM lane quadrant: its four epilogue warps' partial head sums are in
-  float red[2][4][4][32];              // [use parity][quadrant][warp of the quadrant][lane] partial head sums
   uint32_t tmem_base;
   int abort;
 };
@@ -141,6 +143,23 @@ __device__ __forceinline__ void pass_range(const Group& G, int p, int c, int ch,
   t1 = min(t0 + ch, G.pass_T[p]);
 }
 
+// Entry e of an item (its tiles in pass order) -> pass and tile.
+__device__ __forceinline__ void entry_at(const Group& G, int c, int ch, int e, int& p_out, int& t_out) {
+  p_out = 0;
+  t_out = 0;
+  for (int p = 0; p < G.npass; ++p) {
+    int t0, t1;
+    pass_range(G, p, c, ch, t0, t1);
+    const int n = max(0, t1 - t0);
+    if (e < n) {
+      p_out = p;
+      t_out = t0 + e;
+      return;
+    }
+    e -= n;
+  }
+}
+
 __device__ __forceinline__ int item_tiles(const Group& G, int c, int ch) {
   int n = 0;
   for (int p = 0; p < G.npass; ++p) {
@@ -220,7 +239,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(&S.epi_sync[b], kEpiThreads);
     }
     mbar_init(&S.fin, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(&S.qred[q], 128);
     S.abort = 0;
     fence_mbar_init();
   }
@@ -288,7 +306,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    uint32_t g = 0, j = 0;
+    uint32_t g = 0, j = 0, dq = 0;   // key tiles, items with tiles, accumulator-buffer uses
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
       const int gi = item % ngroups, c = item / ngroups;
       Group G;
@@ -297,17 +315,22 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const int bb = j & 1;
       if (!mbar_wait(&S.b_full[bb], (j >> 1) & 1, abort)) break;
       bool ok = true;
-      for (int p = 0; p < G.npass && ok; ++p) {
-        const uint32_t idesc = idesc_e4m3(128, G.uniform ? 256 : 64);
-        const uint32_t boff = bb * kBBytes + (G.uniform ? 0u : (uint32_t)G.pass_q[p] * (kHI * 128));
+      // One accumulator buffer holds one shared-pass tile (4 queries x 64
+      // heads) or up to four consecutive per-query tiles (64 columns each),
+      // so that per-query work keeps eight tiles in flight, not two.
+      const bool uni = G.uniform;
+      const int ne = item_tiles(G, c, ch), per_d = uni ? 1 : 4;
+      const uint32_t idesc = idesc_e4m3(128, uni ? 256 : 64);
+      if (uni) {   // one pass, one tile per buffer
         int t0, t1;
-        pass_range(G, p, c, ch, t0, t1);
-        for (int t = t0; t < t1; ++t, ++g) {
-          const int st = g % kStagesA, b = g & 1;
+        pass_range(G, 0, c, ch, t0, t1);
+        const uint32_t boff = bb * kBBytes;
+        for (int t = t0; t < t1; ++t, ++g, ++dq) {
+          const int st = g % kStagesA, b = dq & 1;
           IDX_TRACE(1, g, 0, lane == 0);
           if (!(ok = mbar_wait(&S.a_full[st], (g / kStagesA) & 1, abort))) break;
           IDX_TRACE(1, g, 1, lane == 0);
-          if (!(ok = mbar_wait(&S.d_empty[b], ((g >> 1) & 1) ^ 1, abort))) break;
+          if (!(ok = mbar_wait(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort))) break;
           IDX_TRACE(1, g, 2, lane == 0);
           tc_fence_after();
           if (lane == 0) {
@@ -321,6 +344,31 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           __syncwarp();
         }
       }
+      for (int e0 = 0; e0 < ne && ok && !uni; e0 += per_d, ++dq) {
+        const int b = dq & 1, nsub = min(per_d, ne - e0);
+        if (!(ok = mbar_wait(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort))) break;
+        for (int u = 0; u < nsub; ++u, ++g) {
+          int p, t;
+          entry_at(G, c, ch, e0 + u, p, t);
+          const uint32_t boff = bb * kBBytes + (uni ? 0u : (uint32_t)G.pass_q[p] * (kHI * 128));
+          const int st = g % kStagesA;
+          IDX_TRACE(1, g, 0, lane == 0);
+          if (!(ok = mbar_wait(&S.a_full[st], (g / kStagesA) & 1, abort))) break;
+          IDX_TRACE(1, g, 1, lane == 0);
+          tc_fence_after();
+          if (lane == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_e4m3(tmem + 256 * b + 64 * u, sdesc(sA + st * kABytes + kk * 32, 16, 1024),
+                       sdesc(sB + boff + kk * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+            mma_commit(&S.a_empty[st]);
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(&S.d_full[b]);
+        __syncwarp();
+      }
       if (!ok) break;
       if (lane == 0) mma_commit(&S.b_empty[bb]);   // this item's query tile is no longer read
       __syncwarp();
@@ -333,7 +381,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // ------------------------------------------------------------ epilogue
     const int qd = warp & 3, uq = (warp - 2) >> 2, et = tid - 64;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-    uint32_t g = 0, j = 0, nred = 0;   // tiles, items with tiles, uses of the quadrant barrier
+    uint32_t dq = 0, j = 0;   // accumulator-buffer uses, items with tiles
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
       const int gi = item % ngroups, c = item / ngroups;
       Group G;
@@ -350,75 +398,96 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           if (!mbar_wait(&S.epi_sync[bb], (j >> 1) & 1, abort)) break;
         }
         bool ok = true;
-        for (int p = 0; p < G.npass && ok; ++p) {
-          const bool uni = G.uniform;
-          const int seq = G.pass_seq[p];
+        const bool uni = G.uniform;
+        const int ne = item_tiles(G, c, ch), per_d = uni ? 1 : 4;
+        if (uni) {   // one pass, one tile per buffer: this warp's query is uq
           int t0, t1;
-          pass_range(G, p, c, ch, t0, t1);
-          for (int t = t0; t < t1; ++t, ++g) {
-            const int b = g & 1;
-            // this lane's key and its scale, fetched before the wait so that
-            // the load (from HBM when every key is read once) overlaps the MMA
+          pass_range(G, 0, c, ch, t0, t1);
+          const int seq = G.pass_seq[0], maxpos = G.pass_maxpos[0];
+          const bool q_act = G.active[uq];
+          const int q_pos = G.pos[uq], row_q = gi * kQG + uq;
+          const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][uq]);
+          for (int t = t0; t < t1; ++t, ++dq) {
+            const int b = dq & 1;
+            // this lane's key and its scale, fetched before the wait
             const int s = t * kKT + qd * 32 + lane;
             float sk = 0.f;
-            bool key_ok = s <= G.pass_maxpos[p];
+            bool key_ok = s <= maxpos;
             if (key_ok) {
               const int64_t row = cache_row(cm, seq, s, err);
               key_ok = row >= 0;
               if (key_ok) sk = __ldg(k_scale + row);
             }
-            IDX_TRACE(2, g, 0, et == 0);
-            if (!(ok = mbar_wait(&S.d_full[b], (g >> 1) & 1, abort))) break;
-            IDX_TRACE(2, g, 1, et == 0);
+            IDX_TRACE(2, dq, 0, et == 0);
+            if (!(ok = mbar_wait(&S.d_full[b], (dq >> 1) & 1, abort))) break;
+            IDX_TRACE(2, dq, 1, et == 0);
             tc_fence_after();
-            // The head sum is four 16-head partials added as (P0 + P1) + (P2 + P3)
-            // in both modes, so a query scores the same bits either way.
-            // uniform: this warp sums all 64 heads of its own query; per-query
-            // passes: the four warps of the quadrant take 16 heads each of the
-            // pass's query and meet in shared memory.
-            const int qq = uni ? uq : G.pass_q[p];
-            const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][qq]);
-            float acc = 0.f;
-            bool write = false;
-            if (uni) {
-              float P[4];
+            float P[4];
 #pragma unroll
-              for (int uh = 0; uh < 2; ++uh) {   // two 16-column loads at a time
-                uint32_t r[2][16];
-                tmem_ld16(tmem + lane_base + 256 * b + qq * 64 + 32 * uh, r[0]);
-                tmem_ld16(tmem + lane_base + 256 * b + qq * 64 + 32 * uh + 16, r[1]);
-                tmem_ld_wait();
-                P[2 * uh] = head_partial(r[0], wq4 + 8 * uh);
-                P[2 * uh + 1] = head_partial(r[1], wq4 + 8 * uh + 4);
-              }
-              acc = (P[0] + P[1]) + (P[2] + P[3]);
-              write = true;
-            } else {
-              uint32_t r[16];
-              tmem_ld16(tmem + lane_base + 256 * b + 16 * uq, r);
+            for (int uh = 0; uh < 2; ++uh) {   // two 16-column loads at a time
+              uint32_t r[2][16];
+              tmem_ld16(tmem + lane_base + 256 * b + uq * 64 + 32 * uh, r[0]);
+              tmem_ld16(tmem + lane_base + 256 * b + uq * 64 + 32 * uh + 16, r[1]);
               tmem_ld_wait();
-              const int rb = nred & 1;
-              S.red[rb][qd][uq][lane] = head_partial(r, wq4 + 4 * uq);
-              mbar_arrive(&S.qred[qd]);
-              if (!(ok = mbar_wait(&S.qred[qd], nred & 1, abort))) break;
-              ++nred;
-              if (uq == 0) {
-                acc = (S.red[rb][qd][0][lane] + S.red[rb][qd][1][lane]) +
-                      (S.red[rb][qd][2][lane] + S.red[rb][qd][3][lane]);
-                write = true;
-              }
+              P[2 * uh] = head_partial(r[0], wq4 + 8 * uh);
+              P[2 * uh + 1] = head_partial(r[1], wq4 + 8 * uh + 4);
             }
-            if (write) {
-              const int row_q = gi * kQG + qq;
-              if (s < qb.max_kv && row_q < qb.num_q) {
-                const bool live = G.active[qq] && key_ok && s <= G.pos[qq];
-                scores[(int64_t)row_q * ld + s] = live ? acc * sk : -INFINITY;
-              }
+            const float acc = (P[0] + P[1]) + (P[2] + P[3]);
+            if (s < qb.max_kv && row_q < qb.num_q) {
+              const bool live = q_act && key_ok && s <= q_pos;
+              scores[(int64_t)row_q * ld + s] = live ? acc * sk : -INFINITY;
             }
             tc_fence_before();
             mbar_arrive(&S.d_empty[b]);
-            IDX_TRACE(2, g, 2, et == 0);
+            IDX_TRACE(2, dq, 2, et == 0);
           }
+        }
+        for (int e0 = 0; e0 < ne && ok && !uni; e0 += per_d, ++dq) {
+          const int b = dq & 1, nsub = min(per_d, ne - e0);
+          // this warp's part of the buffer: query uq of a shared-pass tile, or
+          // per-query tile e0 + uq (both at columns 64 uq)
+          const bool mine = uni || uq < nsub;
+          int p = 0, t = 0;
+          entry_at(G, c, ch, uni ? e0 : e0 + min(uq, nsub - 1), p, t);
+          const int qq = uni ? uq : G.pass_q[p];
+          // this lane's key and its scale, fetched before the wait so that
+          // the load (from HBM when every key is read once) overlaps the MMA
+          const int s = t * kKT + qd * 32 + lane;
+          float sk = 0.f;
+          bool key_ok = mine && s <= G.pass_maxpos[p];
+          if (key_ok) {
+            const int64_t row = cache_row(cm, G.pass_seq[p], s, err);
+            key_ok = row >= 0;
+            if (key_ok) sk = __ldg(k_scale + row);
+          }
+          IDX_TRACE(2, dq, 0, et == 0);
+          if (!(ok = mbar_wait(&S.d_full[b], (dq >> 1) & 1, abort))) break;
+          IDX_TRACE(2, dq, 1, et == 0);
+          tc_fence_after();
+          if (mine) {
+            // four 16-head partials added as (P0 + P1) + (P2 + P3): the same
+            // arithmetic in both modes, so a query's scores do not depend on its batch
+            const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][qq]);
+            float P[4];
+#pragma unroll
+            for (int uh = 0; uh < 2; ++uh) {   // two 16-column loads at a time
+              uint32_t r[2][16];
+              tmem_ld16(tmem + lane_base + 256 * b + uq * 64 + 32 * uh, r[0]);
+              tmem_ld16(tmem + lane_base + 256 * b + uq * 64 + 32 * uh + 16, r[1]);
+              tmem_ld_wait();
+              P[2 * uh] = head_partial(r[0], wq4 + 8 * uh);
+              P[2 * uh + 1] = head_partial(r[1], wq4 + 8 * uh + 4);
+            }
+            const float acc = (P[0] + P[1]) + (P[2] + P[3]);
+            const int row_q = gi * kQG + qq;
+            if (s < qb.max_kv && row_q < qb.num_q) {
+              const bool live = G.active[qq] && key_ok && s <= G.pos[qq];
+              scores[(int64_t)row_q * ld + s] = live ? acc * sk : -INFINITY;
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&S.d_empty[b]);
+          IDX_TRACE(2, dq, 2, et == 0);
         }
         if (!ok) break;
         ++j;
