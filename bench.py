@@ -174,9 +174,14 @@ class Runner:
         self.cache = self.prob.cache.desc()
 
     def step(self):
-        k = self.wl.topk
-        for a, b, qd, ix, at in self.calls:
-            api.dsa_forward(qd, self.cache, ix, k, at, self.idx[a:b], self.out[a:b], self.lse[a:b], self.ws)
+        for ci in range(len(self.calls)):
+            self.chunk(ci)
+
+    def chunk(self, ci: int, stream=None):
+        """dsa_forward over call ci (one chunk of query rows)."""
+        a, b, qd, ix, at = self.calls[ci]
+        api.dsa_forward(qd, self.cache, ix, self.wl.topk, at, self.idx[a:b], self.out[a:b], self.lse[a:b], self.ws,
+                        stream=stream)
 
 
 def _pairs(wl):
@@ -263,38 +268,52 @@ def _roofline_decode(wl, per_stage, steps, peaks):
 
 
 def _e2e(wl, steps: int):
-    """Same metric through the public API with host buffers: every step copies
-    the step's inputs from pinned host memory, runs the forward and reads the
-    outputs back.  Returns (tokens/s, h2d bytes, d2h bytes)."""
-    dev = wl.q.device
-    names = ["q_idx", "q_scale", "w", "k_idx", "k_scale", "q", "kv", "q_seq", "q_pos"]
-    host = {n: getattr(wl, n).to("cpu").pin_memory() for n in names}
+    """Same metric through the public API with host buffers.  Every step
+    copies the step's inputs from pinned host memory, runs dsa_forward chunk
+    by chunk and copies the outputs back; a chunk's input copy, compute and
+    output copy run on three streams, so the copies of one chunk overlap the
+    compute of its neighbours (the host link, not the GPU, bounds this
+    number).  Steps are separated by a device synchronisation.
+    Returns (tokens/s, h2d bytes, d2h bytes, ms per step)."""
+    row_names = ["q_idx", "q_scale", "w", "q", "q_seq", "q_pos"]   # one entry per query row
+    cache_names = ["k_idx", "k_scale", "kv"]
+    host = {n: getattr(wl, n).to("cpu").pin_memory() for n in row_names + cache_names}
     r = Runner(wl)
-    dev_t = {n: getattr(wl, n) for n in names}
+    dev_t = {n: getattr(wl, n) for n in row_names + cache_names}
     out_h = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
     lse_h = torch.empty(r.lse.shape, dtype=r.lse.dtype).pin_memory()
     idx_h = torch.empty(r.idx.shape, dtype=r.idx.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in (out_h, lse_h, idx_h))
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
 
     def one():
-        for n in names:
-            dev_t[n].copy_(host[n], non_blocking=True)
-        r.step()
-        out_h.copy_(r.out, non_blocking=True)
-        lse_h.copy_(r.lse, non_blocking=True)
-        idx_h.copy_(r.idx, non_blocking=True)
+        with torch.cuda.stream(s_in):
+            for n in cache_names:
+                dev_t[n].copy_(host[n], non_blocking=True)
+        for ci, (a, b) in enumerate(wl.chunks):
+            with torch.cuda.stream(s_in):
+                for n in row_names:
+                    dev_t[n][a:b].copy_(host[n][a:b], non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            s_cmp.wait_event(ev_in)
+            r.chunk(ci, s_cmp)
+            ev_done = torch.cuda.Event()
+            ev_done.record(s_cmp)
+            s_out.wait_event(ev_done)
+            with torch.cuda.stream(s_out):
+                out_h[a:b].copy_(r.out[a:b], non_blocking=True)
+                lse_h[a:b].copy_(r.lse[a:b], non_blocking=True)
+                idx_h[a:b].copy_(r.idx[a:b], non_blocking=True)
 
     one()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
     for _ in range(steps):
         one()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+        torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / steps
     del host, out_h, lse_h, idx_h
     return wl.num_q / (ms / 1e3), h2d, d2h, ms
 
