@@ -253,8 +253,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld16(tS + c * 16, r[c]);
           tmem_ld_wait();
+          const uint64_t sl2 = f2(scale_log2, scale_log2);
 #pragma unroll
-          for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(r[j >> 4][j & 15]) * scale_log2;
+          for (int j = 0; j < 64; j += 2) {
+            const float2 v = f2_split(mul2(f2(__uint_as_float(r[j >> 4][j & 15]), __uint_as_float(r[j >> 4][(j & 15) + 1])), sl2));
+            x[j] = v.x;
+            x[j + 1] = v.y;
+          }
         }
         tc_fence_before();
         mbar_arrive(&B.s_empty[grp]);   // S(gt+2) may be computed into this buffer
@@ -286,6 +291,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         // fp16 rounding of one partial; each CTA's half of O stays consistent
         // with its own P and sum, which is all the normalisation needs.
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        const bool full = (vm_lo & vm_hi) == 0xffffffffu;   // almost every tile: no masking
 #pragma unroll
         for (int jq = 0; jq < 8; ++jq) {
           const uint4 v = X4[jq * 128 + h];
@@ -294,10 +300,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
           for (int e = 0; e < 4; ++e) {
             const float2 p = f16x2_to_f32x2(pw[e]);
             const int j = 8 * jq + 2 * e;
-            const uint32_t vm = j < 32 ? vm_lo : vm_hi;
-            x[j] = ((vm >> (j & 31)) & 1u) ? x[j] + p.x : -INFINITY;
-            x[j + 1] = ((vm >> ((j + 1) & 31)) & 1u) ? x[j + 1] + p.y : -INFINITY;
-            m4[e] = fmaxf(m4[e], fmaxf(x[j], x[j + 1]));
+            const float2 sum = f2_split(add2(f2(x[j], x[j + 1]), f2(p.x, p.y)));
+            x[j] = sum.x;
+            x[j + 1] = sum.y;
+            if (!full) {
+              const uint32_t vm = j < 32 ? vm_lo : vm_hi;
+              if (!((vm >> (j & 31)) & 1u)) x[j] = -INFINITY;
+              if (!((vm >> ((j + 1) & 31)) & 1u)) x[j + 1] = -INFINITY;
+            }
+            m4[e] = max3(m4[e], x[j], x[j + 1]);
           }
         }
         const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
@@ -324,16 +335,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         }
         const float msub = m_use == -INFINITY ? 0.f : m_use;   // all p are 0 while nothing is valid
         uint32_t pk[32];
-        float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint64_t ps2[2] = {0ull, 0ull};   // the sum of the fp32 probabilities, two packed accumulators
+        const uint64_t nm2 = f2(-msub, -msub);
 #pragma unroll
         for (int j = 0; j < 64; j += 2) {
-          const float p0 = ex2_approx(x[j] - msub);
-          const float p1 = ex2_approx(x[j + 1] - msub);
+          const float2 d = f2_split(add2(f2(x[j], x[j + 1]), nm2));
+          const float p0 = ex2_approx(d.x);
+          const float p1 = ex2_approx(d.y);
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          ps4[(j >> 1) & 3] += p0 + p1;   // the sum of the fp32 probabilities
+          ps2[(j >> 1) & 1] = add2(ps2[(j >> 1) & 1], f2(p0, p1));
           pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
         }
-        l += (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
+        {
+          const float2 a = f2_split(ps2[0]), b2 = f2_split(ps2[1]);
+          l += (a.x + a.y) + (b2.x + b2.y);
+        }
         ATTN_TRACE(grp, gt, 4, lane == 0 && q4 == 0);
         if (t > 0 && m_use != m_prev) {
           // O holds the P.V of tiles < gt relative to m_prev; that of tile gt-1 must be complete
