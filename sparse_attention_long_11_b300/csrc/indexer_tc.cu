@@ -33,6 +33,7 @@
 // modes, so a query's scores do not depend on its batch.  All waits are
 // bounded (see tc.cuh).
 #include <algorithm>
+#include <cstdint>
 #include <cstddef>
 
 #include "launch.h"
@@ -555,9 +556,20 @@ cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const ds
   const int sms = sm_count_here();
   const int ngroups = (qb.num_q + kQG - 1) / kQG;
   const int tmax = (qb.max_kv + kKT - 1) / kKT;
-  // chunks of ch key tiles, aiming at ~8 items per CTA for the largest group shape
-  const int64_t want = (int64_t)ngroups * tmax / ((int64_t)sms * 8);
-  const int ch = (int)std::max<int64_t>(2, std::min<int64_t>(64, want));
+  // chunks of ch key tiles: the CTAs take items round-robin, so pick the ch
+  // that minimises the busiest CTA's load (items x tiles, plus about one
+  // tile's worth of fixed cost per item); ties go to the larger chunk
+  int ch = 2;
+  int64_t best = INT64_MAX;
+  for (int c = 2; c <= 64; ++c) {
+    const int64_t nch = (tmax + c - 1) / c, items = (int64_t)ngroups * nch;
+    const int64_t per_cta = (items + sms - 1) / sms;
+    const int64_t cost = per_cta * (std::min<int64_t>(c, tmax) + 1);
+    if (cost <= best) {
+      best = cost;
+      ch = c;
+    }
+  }
   const int nchunk = (tmax + ch - 1) / ch;
   const int grid = (int)std::min<int64_t>(sms, (int64_t)ngroups * nchunk);
   cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
