@@ -31,7 +31,7 @@ namespace dsa {
 namespace {
 
 constexpr int kBins = 2048;
-constexpr int kCandCap = 6144;   // threshold-bin keys gathered for the finer rounds (the candidate-list buffer)
+constexpr int kCandCap = 4096;   // threshold-bin keys gathered for the finer rounds (the candidate-list buffer)
 constexpr int kManyRowsThreads = 256, kFewRowsThreads = 1024;
 
 template <int NT>
@@ -126,10 +126,10 @@ struct RowKeys {
 
 constexpr int kSamples = 1024;
 
-// Per-warp capacity of the candidate list (the list is 48 or 64 KiB of
+// Per-warp capacity of the candidate list (the list is 32 or 64 KiB of
 // dynamic shared memory: keys and positions).
 template <int NT> struct Region;   // per-warp list capacity; NW * kPerWarp >= kCandCap
-template <> struct Region<256> { static constexpr int kPerWarp = 768; };
+template <> struct Region<256> { static constexpr int kPerWarp = 512; };   // 44 KiB a block: five blocks per SM
 template <> struct Region<1024> { static constexpr int kPerWarp = 256; };
 
 template <int NT>
@@ -388,7 +388,7 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, 
   }
   __syncthreads();
   const float f = (float)kSamples * (float)k / (float)n;
-  const int r = min(kSamples, (int)ceilf(f + 4.f * sqrtf(f) + 16.f));
+  const int r = min(kSamples, (int)ceilf(f + 3.f * sqrtf(f) + 8.f));
   uint32_t unused;
   const uint32_t G = select_in_list<NT>(kSamples, [&](int s, uint32_t& u) { u = samp[s]; return true; }, (uint32_t)r,
                                         hist, warp_tot, S, &unused);
