@@ -7,8 +7,8 @@
 // folded onto +0).
 //
 //   1. A threshold guess G: of 1024 evenly spaced samples of the row, the
-//      r-th largest, r a few standard deviations above the expected rank of
-//      the k-th largest key (1024 k / n).
+//      r-th largest (its 22 leading bits: two radix rounds), r a few standard
+//      deviations above the expected rank of the k-th largest key (1024 k / n).
 //   2. One pass over the row collects every key >= G with its position into
 //      a per-warp list (warp w owns a contiguous segment, so the lists hold
 //      positions in ascending order).  With at least k of them, the row's
@@ -318,16 +318,19 @@ __device__ __noinline__ void radix_path(const RowKeys rk, int k, int32_t* __rest
   }
 }
 
-// Exact k-th largest key of a list held in shared memory: three radix rounds
-// (11 + 11 + 10 bits) over the entries i < total for which get(i) is valid.
-// Returns the key T; *need = how many entries equal to T belong to the top k_rank.
+// k-th largest key of a list held in shared memory: radix rounds (11 + 11
+// + 10 bits) over the entries i < total for which get(i) is valid.  With
+// all three rounds the result is exact: the key T, and *need = how many
+// entries equal to T belong to the top k_rank.  With two rounds it is the
+// 22-bit prefix of that key (a lower bound on it, exact to 2^-13 relative).
 template <int NT, class Get>
 __device__ __forceinline__ uint32_t select_in_list(int total, Get get, uint32_t k_rank, uint32_t* hist,
-                                                   uint32_t* warp_tot, TopkShared<NT>& S, uint32_t* need) {
+                                                   uint32_t* warp_tot, TopkShared<NT>& S, uint32_t* need,
+                                                   int rounds = 3) {
   const int tid = threadIdx.x;
   uint32_t prefix = 0, pmask = 0, krem = k_rank;
 #pragma unroll 1
-  for (int round = 0; round < 3; ++round) {
+  for (int round = 0; round < rounds; ++round) {
     const int shift = round == 0 ? 21 : (round == 1 ? 10 : 0);
     const int nb = round == 2 ? 1024 : 2048;
     for (int b = tid; b < kBins; b += NT) hist[b] = 0;
@@ -391,7 +394,7 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, 
   const int r = min(kSamples, (int)ceilf(f + 3.f * sqrtf(f) + 8.f));
   uint32_t unused;
   const uint32_t G = select_in_list<NT>(kSamples, [&](int s, uint32_t& u) { u = samp[s]; return true; }, (uint32_t)r,
-                                        hist, warp_tot, S, &unused);
+                                        hist, warp_tot, S, &unused, 2);
 
   // ---- 2. one pass over the row: every key >= G with its position, into
   // the warp's region of the list, in position order (warp w scans the
