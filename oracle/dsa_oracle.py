@@ -31,7 +31,11 @@ ascending s and padded with -1; attention
     O[t,h,:] = sum_{s in sel} softmax_s(tau * <q[t,h,:], kv[s,:]>) * kv[s,:d_v]
 plus LSE[t,h] = log sum_s exp(tau * <q, kv_s>) (natural log).
 
-Everything is computed in float64 from exactly decoded inputs.
+Everything is computed in float64 from exactly decoded inputs, except the
+key-cache encoding (quantize_e4m3_rows): the FP8 keys of the summary card's
+"cheap FP8 relevance scores" are written once per token as e4m3 codes with a
+per-row scale amax/448, and the codes that write produces are decided by its
+float32 scale and division, which the oracle therefore takes in float32.
 """
 from __future__ import annotations
 
@@ -63,6 +67,43 @@ E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
 def decode_e4m3(codes) -> np.ndarray:
     """uint8 e4m3 codes -> float64 values (exact)."""
     return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+# Positive finite codes 0x00..0x7E in increasing order of value (the code is
+# the index: e4m3 codes are monotonic in magnitude).
+_E4M3_POS = E4M3_TABLE[:0x7F]
+
+
+def encode_e4m3(y) -> np.ndarray:
+    """Float values -> OCP e4m3 ("fn") codes: round to the nearest
+    representable value, ties to the code with an even last mantissa bit,
+    magnitudes above 448 saturated to 448; the sign bit is kept (-0.0 ->
+    0x80).  The inputs are taken exactly as given (float32 values are exact
+    in float64)."""
+    y = np.asarray(y, dtype=np.float64)
+    a = np.minimum(np.abs(y), 448.0)
+    hi = np.searchsorted(_E4M3_POS, a, side="left")          # first code with value >= a
+    hi = np.minimum(hi, 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a == _E4M3_POS[hi], hi, code)             # exactly representable
+    return (code | np.where(np.signbit(y), 0x80, 0)).astype(np.uint8)
+
+
+def quantize_e4m3_rows(x) -> tuple:
+    """Indexer key-cache encoding of float32 rows (x [n, d]): per row
+    scale = amax(|row|) / 448 (1 for an all-zero row) and codes =
+    encode_e4m3(row / scale), the scale and the division taken in float32
+    -- the precision of the kernel that writes the cache, which decides the
+    codes.  Returns (uint8 codes [n, d], float32 scales [n])."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.abs(x).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    y = (x / scale[:, None]).astype(np.float32)
+    return encode_e4m3(y), scale
 
 
 def decode_bf16(bits) -> np.ndarray:

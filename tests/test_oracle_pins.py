@@ -47,6 +47,41 @@ def test_e4m3_matches_torch_float8():
     assert np.array_equal(ref[~nan], got[~nan])
 
 
+def test_e4m3_encoder_round_trip_and_ties():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = O.decode_e4m3(codes)
+    assert np.array_equal(O.encode_e4m3(vals), codes)             # every finite code (incl. -0) round-trips
+    pos = O.E4M3_TABLE[:0x7F]
+    mids = (pos[:-1] + pos[1:]) / 2                                # exact midpoints of neighbouring codes
+    got = O.encode_e4m3(mids)
+    lo = np.arange(0x7E)
+    want = np.where(lo % 2 == 0, lo, lo + 1)                       # ties to the even code
+    assert np.array_equal(got, want.astype(np.uint8))
+    assert np.array_equal(O.encode_e4m3([448.0, 449.0, 1e30, -1e30, -464.0]),
+                          np.array([0x7E, 0x7E, 0x7E, 0xFE, 0xFE], dtype=np.uint8))   # saturation
+
+
+def test_e4m3_encoder_matches_torch_float8_on_random_values():
+    g = torch.Generator().manual_seed(11)
+    x = (torch.randn(200000, generator=g) * torch.exp2(torch.randint(-12, 10, (200000,), generator=g).float()))
+    x = x.clamp(-448, 448)                                         # torch's cast does not saturate
+    want = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.encode_e4m3(x.numpy()), want)
+
+
+def test_row_quantisation_scale_and_extremes():
+    x = np.array([[0.5, -2.0, 1.0, 0.0], [0.0, 0.0, 0.0, 0.0], [-3.0, 1e-9, 2.0, -0.0]], dtype=np.float32)
+    codes, scale = O.quantize_e4m3_rows(x)
+    assert scale.dtype == np.float32
+    assert scale[0] == np.float32(2.0) / np.float32(448.0) and scale[1] == 1.0
+    assert codes[0, 1] == 0xFE and codes[2, 0] == 0xFE             # each row's largest magnitude -> -448
+    assert np.all(codes[1] == 0) and codes[2, 3] == 0x80            # zero row; -0.0 keeps its sign
+    # decoding reproduces every element within half a code step (relative 2^-4) or the subnormal step
+    back = O.decode_e4m3(codes) * scale[:, None]
+    step = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -9 * scale[:, None])
+    assert np.all(np.abs(back - x) <= step)
+
+
 def test_bf16_matches_torch():
     x = torch.randn(4096, dtype=torch.float32) * 100
     b = x.to(torch.bfloat16)
