@@ -267,6 +267,40 @@ def _roofline_decode(wl, per_stage, steps, peaks):
             "avg_launch_ms": tot / cnt, "launches": cnt}
 
 
+def _time_append(wl, r: Runner, steps: int, warmup: int):
+    """The decode loop's cache write: one new token per sequence (bf16 key of
+    width 128 encoded to e4m3 + scale, and its 576-wide bf16 latent row),
+    written at each sequence's last position.  Timed with CUDA events after
+    the decode steps (it rewrites those rows)."""
+    dev = wl.q.device
+    n = wl.num_seqs
+    k_new = inputs.randn((n, 128), 1, "append_k", dev).to(torch.bfloat16)
+    kv_new = inputs.randn((n, 576), 1, "append_kv", dev).to(torch.bfloat16)
+    seq = torch.arange(n, dtype=torch.int32, device=dev)
+    pos = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev) - 1
+    cache = r.prob.cache.desc()
+
+    def one():
+        api.dsa_cache_append(cache, seq, pos, k_new, wl.k_idx, wl.k_scale, kv_new, wl.kv)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    st = api.dsa_check_device_error()
+    if st != api.DSA_OK:
+        raise RuntimeError(f"device error during cache append: {api.status_string(st)}")
+    ms = e0.elapsed_time(e1) / steps
+    byts = n * ((128 * 2 + 576 * 2) + (128 + 4 + 576 * 2))   # read new rows, write cache rows
+    return {"tokens": n, "ms": ms, "bytes": byts, "achieved_gbs": byts / (ms / 1e3) / 1e9,
+            "note": "latency-bound: one 128-thread block per 4 tokens"}
+
+
 def _e2e(wl, steps: int):
     """Same metric through the public API with host buffers.  Every step
     copies the step's inputs from pinned host memory, runs dsa_forward chunk
@@ -426,6 +460,7 @@ def main():
                   "stages": {k: {"launches": v[0], "ms_per_step": v[1] / max(args.steps, 10)}
                              for k, v in dstage.items()},
                   "roofline": _roofline_decode(wd, dstage, max(args.steps, 10), peaks), "clocks": dclk}
+        decode["cache_append"] = _time_append(wd, rd, max(args.steps, 10), args.warmup)
         del rd, wd
         torch.cuda.empty_cache()
 

@@ -218,13 +218,44 @@ DSA_API const char* dsa_last_error_detail(void);
 /* Static, NUL-terminated description of a status code (never NULL). */
 DSA_API const char* dsa_status_string(dsa_status status);
 
+/*
+ * dsa_cache_append -- write num_tok new tokens into the caches the forward
+ * reads (the step that precedes the indexer in every decode iteration).
+ * The FP8 keys are the operands of the summary card's "cheap FP8 relevance
+ * scores" (DeepSeek-V3.2 summary card, "How DSA Works"); the pages print no
+ * encoding, so this library fixes one: per key row, scale = amax(|row|) /
+ * 448 (1 for an all-zero row) and codes = e4m3(row / scale), round to
+ * nearest with ties to even, saturated to +-448, the scale and the division
+ * in fp32.
+ *
+ *   cache     physical-row map shared by both caches (as for dsa_forward)
+ *   tok_seq, tok_pos  [num_tok] int32: sequence and logical position of each
+ *             new token; its physical row is written
+ *   k_dtype   DSA_BF16 or DSA_F32: element type of k_new
+ *   k_new     [num_tok, dim] new indexer keys, rows 16-byte aligned; dim must
+ *             be 128 (else DSA_ERR_UNSUPPORTED)
+ *   k_cache   [num_rows, 128] uint8 e4m3 key cache (16-byte aligned)
+ *   k_scale   [num_rows] fp32 per-row scales
+ *   kv_new    [num_tok, d_qk] bf16 new latent rows, or NULL (then kv_cache
+ *             must be NULL too and only the keys are written)
+ *   kv_cache  [num_rows, d_qk] bf16 latent cache; d_qk * 2 a multiple of 16
+ *
+ * Rows of tokens whose position lies outside the descriptor are skipped and
+ * DSA_ERR_BOUNDS is recorded for dsa_check_device_error().  Two tokens that
+ * map to the same row race.  num_tok == 0 enqueues nothing.
+ */
+DSA_API dsa_status dsa_cache_append(const dsa_cache_desc* cache, int32_t num_tok, const int32_t* tok_seq,
+                                    const int32_t* tok_pos, dsa_dtype k_dtype, const void* k_new, int32_t dim,
+                                    uint8_t* k_cache, float* k_scale, const void* kv_new, int32_t d_qk,
+                                    void* kv_cache, dsa_stream_t stream);
+
 /* ---- Measurement aids (host-side state; not thread-safe) ----------------
  * While a profile is open, every kernel the library launches is bracketed by
  * a pair of CUDA events recorded on its launch stream, and tagged with its
  * stage.  dsa_profile_read() waits for the recorded events and returns each
  * launch's stage and device duration.  Events are created by the library (no
  * device memory); at most `capacity` launches are recorded. */
-typedef enum { DSA_STAGE_INDEXER = 1, DSA_STAGE_TOPK = 2, DSA_STAGE_ATTN = 3 } dsa_stage;
+typedef enum { DSA_STAGE_INDEXER = 1, DSA_STAGE_TOPK = 2, DSA_STAGE_ATTN = 3, DSA_STAGE_APPEND = 4 } dsa_stage;
 DSA_API dsa_status dsa_profile_start(int32_t capacity);
 /* Closes the profile; returns the number of launches recorded. */
 DSA_API int32_t dsa_profile_stop(void);

@@ -67,6 +67,10 @@ _SIGS = {
     "dsa_forward_noalloc": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(IndexerInputs), ctypes.c_int32,
                                            _P(AttnInputs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                            ctypes.c_void_p]),
+    "dsa_cache_append": (ctypes.c_int, [_P(CacheDesc), ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.c_void_p]),
     "dsa_check_device_error": (ctypes.c_int, [ctypes.c_void_p]),
     "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dsa_last_error_detail": (ctypes.c_char_p, []),
@@ -76,8 +80,8 @@ _SIGS = {
     "dsa_profile_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     "dsa_launch_count": (ctypes.c_int64, []),
 }
-DSA_STAGE_INDEXER, DSA_STAGE_TOPK, DSA_STAGE_ATTN = 1, 2, 3
-STAGE_NAMES = {1: "indexer", 2: "topk", 3: "attention"}
+DSA_STAGE_INDEXER, DSA_STAGE_TOPK, DSA_STAGE_ATTN, DSA_STAGE_APPEND = 1, 2, 3, 4
+STAGE_NAMES = {1: "indexer", 2: "topk", 3: "attention", 4: "cache_append"}
 
 _lib = None
 
@@ -188,6 +192,25 @@ def dsa_forward(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, k: int, a
 
 
 NOALLOC_MAX_KV = 2097152
+
+
+def dsa_cache_append(cache: CacheDesc, tok_seq: torch.Tensor, tok_pos: torch.Tensor, k_new: torch.Tensor,
+                     k_cache: torch.Tensor, k_scale: torch.Tensor, kv_new: Optional[torch.Tensor] = None,
+                     kv_cache: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Writes new tokens into the caches: key rows (bf16 or fp32, width 128)
+    encoded as e4m3 codes with a per-row scale, and optionally latent rows."""
+    if k_new.dtype == torch.bfloat16:
+        kdt = DSA_BF16
+    elif k_new.dtype == torch.float32:
+        kdt = DSA_F32
+    else:
+        raise TypeError("k_new must be bfloat16 or float32")
+    d_qk = kv_new.shape[-1] if kv_new is not None else 0
+    _check(lib().dsa_cache_append(ctypes.byref(cache), int(tok_seq.numel()), _ptr(tok_seq), _ptr(tok_pos), kdt,
+                                  _ptr(k_new), int(k_new.shape[-1]), _ptr(k_cache), _ptr(k_scale),
+                                  None if kv_new is None else _ptr(kv_new), d_qk,
+                                  None if kv_cache is None else _ptr(kv_cache), _stream(stream)),
+           "dsa_cache_append")
 
 
 def dsa_forward_noalloc(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, k: int, at: AttnInputs,

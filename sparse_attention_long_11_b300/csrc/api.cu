@@ -248,6 +248,31 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const
   return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
 }
 
+dsa_status dsa_cache_append(const dsa_cache_desc* cd, int32_t num_tok, const int32_t* tok_seq, const int32_t* tok_pos,
+                            dsa_dtype k_dtype, const void* k_new, int32_t dim, uint8_t* k_cache, float* k_scale,
+                            const void* kv_new, int32_t d_qk, void* kv_cache, dsa_stream_t stream) {
+  if (num_tok < 0) return DSA_ERR_INVALID_ARG;
+  if (num_tok == 0) return DSA_OK;
+  DSA_TRY(check_cache(cd, 1));
+  if (k_dtype != DSA_BF16 && k_dtype != DSA_F32) return DSA_ERR_UNSUPPORTED;
+  if (dim != 128) return DSA_ERR_UNSUPPORTED;
+  if (!tok_seq || !tok_pos || !aligned(tok_seq, 4) || !aligned(tok_pos, 4)) return DSA_ERR_INVALID_ARG;
+  if (!k_new || !k_cache || !k_scale || !aligned(k_new, 16) || !aligned(k_cache, 16) || !aligned(k_scale, 4))
+    return DSA_ERR_INVALID_ARG;
+  if ((kv_new == nullptr) != (kv_cache == nullptr)) return DSA_ERR_INVALID_ARG;
+  if (kv_new) {
+    if (!aligned(kv_new, 16) || !aligned(kv_cache, 16)) return DSA_ERR_INVALID_ARG;
+    if (d_qk < 8 || d_qk > 4096 || (d_qk * 2) % 16) return DSA_ERR_UNSUPPORTED;
+  }
+  int* err = device_error_ptr();
+  if (!err) return DSA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(launch(DSA_STAGE_APPEND, st, [&] {
+    return launch_cache_append(to_map(cd), num_tok, tok_seq, tok_pos, k_dtype == DSA_BF16, k_new, k_cache, k_scale,
+                               kv_new, kv_cache, kv_new ? d_qk * 2 : 0, err, st);
+  }));
+}
+
 const char* dsa_last_error_detail(void) { return g_last_detail; }
 
 dsa_status dsa_check_device_error(dsa_stream_t stream) {

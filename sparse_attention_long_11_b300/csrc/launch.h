@@ -48,4 +48,11 @@ inline cudaError_t launch_attn(const QueryBatch& qb, const CacheMap& cm, const d
   return launch_attn_simt(qb, cm, at, idx, k, out, lse, err, stream);
 }
 
+// Appends new tokens to the caches: each key row (128 bf16 or fp32 values)
+// encoded as e4m3 codes with scale amax/448, and (when kv_new is non-null)
+// the latent row copied.  One warp per token.
+cudaError_t launch_cache_append(const CacheMap& cm, int num_tok, const int32_t* tok_seq, const int32_t* tok_pos,
+                                bool k_is_bf16, const void* k_new, uint8_t* k_cache, float* k_scale,
+                                const void* kv_new, void* kv_cache, int kv_row_bytes, int* err, cudaStream_t stream);
+
 }  // namespace dsa

@@ -66,7 +66,9 @@ def quantize_fp8_rows(x: torch.Tensor) -> Tuple[torch.Tensor, torch.Tensor]:
     preparation: the indexer consumes the bytes and scales as given.
     """
     amax = x.abs().amax(dim=-1)
-    scale = torch.where(amax > 0, amax / FP8_MAX, torch.ones_like(amax))
+    # tensor / tensor: an IEEE fp32 division (dividing by a Python number
+    # multiplies by its reciprocal on the GPU, which can differ in the last bit)
+    scale = torch.where(amax > 0, amax / torch.full_like(amax, FP8_MAX), torch.ones_like(amax))
     y = (x / scale.unsqueeze(-1)).clamp_(-FP8_MAX, FP8_MAX)
     codes = y.to(torch.float8_e4m3fn).view(torch.uint8)
     return codes.contiguous(), scale.contiguous()

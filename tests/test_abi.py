@@ -92,6 +92,23 @@ def test_host_validation_rejects_before_launch():
                              0x10000, 0x10000, None) == api.DSA_ERR_UNSUPPORTED
 
 
+def test_cache_append_validation_rejects_before_launch():
+    L = api.lib()
+    cd = api.CacheDesc(1, 4096, 4096, None, 0, 0)
+    A = 0x10000
+    f = lambda n=4, kdt=api.DSA_BF16, kn=A, dim=128, kc=A, ks=A, kvn=A, dqk=576, kvc=A, c=cd: L.dsa_cache_append(
+        ctypes.byref(c), n, A, A, kdt, kn, dim, kc, ks, kvn, dqk, kvc, None)
+    assert f(n=0) == api.DSA_OK                                   # nothing to append: no launch
+    assert f(n=-1) == api.DSA_ERR_INVALID_ARG
+    assert f(dim=64) == api.DSA_ERR_UNSUPPORTED
+    assert f(kdt=api.DSA_FP8_E4M3) == api.DSA_ERR_UNSUPPORTED
+    assert f(kn=A + 8) == api.DSA_ERR_INVALID_ARG                 # key rows must be 16-byte aligned
+    assert f(kc=None) == api.DSA_ERR_INVALID_ARG
+    assert f(kvc=None) == api.DSA_ERR_INVALID_ARG                 # latent rows without a latent cache
+    assert f(dqk=100) == api.DSA_ERR_UNSUPPORTED                  # 200-byte rows: not a 16-byte multiple
+    assert f(c=api.CacheDesc(1, 4096, 0, A, 64, 0)) == api.DSA_ERR_INVALID_ARG   # empty block table
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(api, "_lib", None)
     monkeypatch.setattr(api, "LIB_PATH", str(tmp_path / "libdsa.so"))
