@@ -143,7 +143,7 @@ DSA_API dsa_status dsa_index_scores(const dsa_query_desc* qd, const dsa_cache_de
  * s = 0..q_pos[i] (scores at larger s are ignored), written to
  * idx[i * k .. i * k + k) in ascending s, padded with -1 when q_pos[i] + 1 < k.
  * Exact: the selected set is unique (score desc, then s asc; -0 == +0;
- * scores must not be NaN).  1 <= k <= 2048; ld_scores >= max_kv.
+ * scores must not be NaN).  1 <= k <= 8192; ld_scores >= max_kv.
  * Uses no workspace. */
 DSA_API dsa_status dsa_topk(const dsa_query_desc* qd, const float* scores, int64_t ld_scores, int32_t k,
                     int32_t* idx, dsa_stream_t stream);
@@ -153,7 +153,7 @@ DSA_API dsa_status dsa_topk(const dsa_query_desc* qd, const float* scores, int64
  * position must be <= q_pos[i]).  out [num_q, heads, d_v] (bf16 for
  * DSA_BF16, fp32 for DSA_F32), lse [num_q, heads] fp32 natural-log
  * log-sum-exp of the logits (-INFINITY and a zero output row if nothing is
- * selected).  1 <= k <= 2048. */
+ * selected).  1 <= k <= 8192. */
 DSA_API dsa_status dsa_sparse_attn(const dsa_query_desc* qd, const dsa_cache_desc* cd,
                            const dsa_attn_inputs* at, const int32_t* idx, int32_t k,
                            void* out, float* lse, dsa_stream_t stream);

@@ -21,7 +21,7 @@ __device__ int g_device_error;   // sticky error word (see flag_error)
 // fused forward, so the staged rows stay resident in the 126 MB L2 between
 // the indexer writing them and the top-k reading them.
 constexpr size_t kStageBytes = size_t(64) << 20;
-constexpr int kMaxTopk = 2048;
+constexpr int kMaxTopk = 8192;
 constexpr int kMaxKv = 1 << 22;   // keeps every grid dimension in range
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

@@ -53,7 +53,7 @@ def test_workspace_size_validation():
     ws = L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix()), 2048, ctypes.byref(_at()))
     assert ws >= 16 * 4096 * 4 and ws % 256 == 0
     # k out of range, unsupported shapes, bad dtypes -> 0
-    assert L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix()), 4096, ctypes.byref(_at())) == 0
+    assert L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix()), 8193, ctypes.byref(_at())) == 0
     assert L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix(heads=32)), 2048, ctypes.byref(_at())) == 0
     assert L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix()), 2048, ctypes.byref(_at(d_v=256))) == 0
     # staged scores are bounded (64 MiB) however many queries there are
@@ -69,7 +69,7 @@ def test_host_validation_rejects_before_launch():
     args = lambda q=qd, c=cd, ix=_ix(), k=2048, at=_at(), idx=0x10000, ws=0x10000, wsb=1 << 30: (
         ctypes.byref(q), ctypes.byref(c), ctypes.byref(ix), k, ctypes.byref(at), idx, 0x10000, 0x10000, ws, wsb, None)
     assert f(*args(k=0)) == api.DSA_ERR_INVALID_ARG
-    assert f(*args(k=2049)) == api.DSA_ERR_INVALID_ARG
+    assert f(*args(k=8193)) == api.DSA_ERR_INVALID_ARG
     assert f(*args(idx=None)) == api.DSA_ERR_INVALID_ARG
     assert f(*args(ix=_ix(scales=False))) == api.DSA_ERR_INVALID_ARG           # fp8 without scales
     assert f(*args(ix=_ix(addr=0x10004))) == api.DSA_ERR_INVALID_ARG           # misaligned operand

@@ -52,6 +52,15 @@ def test_forward_fp8_bf16_small():
     _check_rows(wl, idx, out, lse, _sample(wl.num_q, 40, [2046, 2047, 2048, 2049]), ATTN_ATOL_BF16)
 
 
+@pytest.mark.parametrize("k", [1024, 4096, 8192])
+def test_forward_other_k(k):
+    """The top-k sweep beyond the 2048 of the pages: rows below and above k."""
+    wl = inputs.make_prefill(seed=3, device=DEV, L=9000, topk=k)
+    idx, out, lse = run_forward(api.Problem(wl))
+    assert api.dsa_check_device_error() == api.DSA_OK
+    _check_rows(wl, idx, out, lse, _sample(wl.num_q, 12, [k - 2, k - 1, k, wl.num_q - 1]), ATTN_ATOL_BF16)
+
+
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
 def test_forward_full_size(cfg):
     """Full workload sizes, launched as the benchmark launches them."""

@@ -119,6 +119,23 @@ def test_topk_exact_when_evenly_spaced_positions_hold_the_largest_scores(nq):
         assert np.array_equal(got[i], O.topk_select(s_np[i], k)), f"row {i}"
 
 
+@pytest.mark.parametrize("k", [4096, 8192])
+@pytest.mark.parametrize("nq", [6, 400])
+def test_topk_exact_large_k(k, nq):
+    """k beyond 2048, for the wide-block (few rows) and narrow-block paths."""
+    n = 20000
+    sc = inputs.make_scores(nq, n, seed=k + nq, device=DEV, kind="ties")
+    pos = torch.linspace(0, n - 1, nq).round().to(torch.int32)
+    batch = api.Batch(torch.zeros(nq, dtype=torch.int32, device=DEV), pos.to(DEV), n)
+    idx = torch.empty((nq, k), dtype=torch.int32, device=DEV)
+    api.dsa_topk(batch.desc(), sc, k, idx)
+    assert api.dsa_check_device_error() == api.DSA_OK
+    got, s_np = idx.cpu().numpy(), sc.cpu().numpy()
+    for i in range(0, nq, max(1, nq // 12)):
+        p = int(pos[i])
+        assert np.array_equal(got[i], O.topk_select(s_np[i, :p + 1], k)), f"row {i} pos {p}"
+
+
 def test_topk_ignores_scores_beyond_position():
     n, k = 4096, 64
     sc = inputs.make_scores(2, n, seed=9, device=DEV)
