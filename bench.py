@@ -22,6 +22,7 @@ on a bounded sample of the same workload and prints the same line with
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -417,6 +418,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-k-sweep", action="store_true")
+    ap.add_argument("--no-128k", action="store_true")
     args = ap.parse_args()
     ws, rank, local = _dist()
     if args.impl == "reference":
@@ -445,8 +448,37 @@ def main():
         cpu = {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{done} queries at evenly spaced positions of the L=32768 prefill, "
                          f"full oracle path (indexer, top-k, attention) in {dt:.1f} s"}
+    k_sweep = None
+    if not args.no_k_sweep:
+        # the same prefill and inputs with other top-k sizes (not part of the headline value)
+        k_sweep = {}
+        for kk in (1024, 4096, 8192):
+            rk = Runner(dataclasses.replace(wl, topk=kk))
+            kms, kst, _, _ = _time_steps(rk, 2, args.warmup, ws, local)
+            kms = _max_over_ranks(kms, ws)
+            k_sweep[str(kk)] = {"value": wl.num_q * ws / (kms / 1e3), "unit": "tokens/s", "ms_per_step": kms,
+                                "stages": {n: round(v[1] / 2, 3) for n, v in kst.items()}}
+            del rk
+            torch.cuda.empty_cache()
     del wl
     torch.cuda.empty_cache()
+
+    # ---------------- 128K prefill (not part of the headline value): where the indexer leads
+    long128k = None
+    if not args.no_128k:
+        wx = inputs.make_prefill(seed=0, device=dev, L=131072, chunk=4096, name="long128k")
+        rx = Runner(wx)
+        xms, xst, _, _ = _time_steps(rx, 2, args.warmup, ws, local)
+        xms = _max_over_ranks(xms, ws)
+        n_idx, n_attn = _pairs(wx)
+        ims, ams = xst["indexer"][1] / 2, xst["attention"][1] / 2
+        long128k = {"workload": "single-sequence causal prefill L=131072 in 32 calls of 4096 queries, k=2048",
+                    "value": wx.num_q * ws / (xms / 1e3), "unit": "tokens/s", "ms_per_step": xms,
+                    "stages": {n: round(v[1] / 2, 3) for n, v in xst.items()},
+                    "indexer_tflops": n_idx * FLOP_PER_IDX_PAIR / (ims / 1e3) / 1e12,
+                    "attention_tflops": n_attn * FLOP_PER_ATTN_PAIR / (ams / 1e3) / 1e12}
+        del rx, wx
+        torch.cuda.empty_cache()
 
     # ---------------- decode batch (second half of the metric)
     decode = None
@@ -475,7 +507,8 @@ def main():
                 "roofline": roof, "stages": stages, "gpu_launches": launches, "clocks": clocks,
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-                "cpu_baseline": cpu, "decode": decode}
+                "cpu_baseline": cpu, "decode": decode, "k_sweep": k_sweep,
+                "prefill_128k": long128k}
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist

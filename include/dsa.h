@@ -159,8 +159,9 @@ DSA_API dsa_status dsa_sparse_attn(const dsa_query_desc* qd, const dsa_cache_des
                            void* out, float* lse, dsa_stream_t stream);
 
 /* Bytes of workspace dsa_forward needs for this batch (0 if the arguments are
- * invalid).  Depends only on the host-side fields (num_q, max_kv, k, dtypes,
- * shapes). */
+ * invalid): the score rows of all num_q queries, capped at 1 GiB but never
+ * less than one row.  Depends only on the host-side fields (num_q, max_kv, k,
+ * dtypes, shapes). */
 DSA_API size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
                                   const dsa_attn_inputs* at);
 
@@ -169,7 +170,10 @@ DSA_API size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_in
  * positions, as dsa_topk would write them), out and lse (as dsa_sparse_attn).
  * workspace: >= dsa_forward_workspace_size() bytes, 256-byte aligned, owned by
  * the caller and not read before it is written (no zeroing needed); it must
- * not be used by other work while this call's kernels run. */
+ * not be used by other work while this call's kernels run.  It holds the
+ * staged indexer scores: the queries run in equal stages of as many score
+ * rows (max_kv rounded up to a multiple of 4, times 4 bytes, each) as it holds, so a
+ * larger workspace means fewer, fuller stages and the same results. */
 DSA_API dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd,
                        const dsa_indexer_inputs* ix, int32_t k, const dsa_attn_inputs* at,
                        int32_t* idx, void* out, float* lse,

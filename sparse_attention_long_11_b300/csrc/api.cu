@@ -20,7 +20,7 @@ __device__ int g_device_error;   // sticky error word (see flag_error)
 // Scores of at most this many bytes are staged per indexer/top-k round of the
 // fused forward, so the staged rows stay resident in the 126 MB L2 between
 // the indexer writing them and the top-k reading them.
-constexpr size_t kStageBytes = size_t(64) << 20;
+constexpr size_t kStageBytes = size_t(1) << 30;   // recommended staged-score budget (fewer, fuller stages)
 constexpr int kMaxTopk = 8192;
 constexpr int kMaxKv = 1 << 22;   // keeps every grid dimension in range
 
@@ -153,6 +153,36 @@ cudaError_t launch(int stage, cudaStream_t st, F&& f) {
   return e;
 }
 
+// The fused forward over validated arguments: the queries in stages of at
+// most max_rows score rows (as many as the scratch holds), each stage's
+// indexer scores written to `scores` and reduced to its top-k rows, then one
+// attention launch over the whole batch.  The stages are made equal in size,
+// so the last one is not a sliver.
+dsa_status run_staged(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix, int32_t k,
+                      const dsa_attn_inputs* at, int32_t* idx, void* out, float* lse, float* scores,
+                      int64_t max_rows, int* err, cudaStream_t st) {
+  const CacheMap cm = to_map(cd);
+  const int64_t ld = score_ld(qd->max_kv);
+  max_rows = std::max<int64_t>(1, std::min<int64_t>(max_rows, qd->num_q));
+  const int64_t stages = (qd->num_q + max_rows - 1) / max_rows;
+  const int64_t rows = (qd->num_q + stages - 1) / stages;
+  const size_t qi_row = (size_t)ix->heads * ix->dim * idx_elem_size(ix);
+  for (int64_t r0 = 0; r0 < qd->num_q; r0 += rows) {
+    const int n = (int)std::min<int64_t>(rows, qd->num_q - r0);
+    QueryBatch qb{qd->q_seq + r0, qd->q_pos + r0, n, qd->max_kv};
+    dsa_indexer_inputs sub = *ix;
+    sub.q = static_cast<const uint8_t*>(ix->q) + r0 * qi_row;
+    sub.w = ix->w + r0 * ix->heads;
+    if (ix->q_scale) sub.q_scale = ix->q_scale + r0 * ix->heads;
+    cudaError_t e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer(qb, cm, sub, scores, ld, err, st); });
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    e = launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(qb, scores, ld, k, idx + r0 * k, err, st); });
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  return cuda_status(
+      launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
+}
+
 }  // namespace
 }  // namespace dsa
 
@@ -228,24 +258,8 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const
   if (!err) return DSA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  const CacheMap cm = to_map(cd);
-  const int64_t ld = score_ld(qd->max_kv);
-  const int64_t rows = stage_rows(qd->num_q, qd->max_kv);
-  float* scores = static_cast<float*>(workspace);
-  const size_t qi_row = (size_t)ix->heads * ix->dim * idx_elem_size(ix);
-  for (int64_t r0 = 0; r0 < qd->num_q; r0 += rows) {
-    const int n = (int)std::min<int64_t>(rows, qd->num_q - r0);
-    QueryBatch qb{qd->q_seq + r0, qd->q_pos + r0, n, qd->max_kv};
-    dsa_indexer_inputs sub = *ix;
-    sub.q = static_cast<const uint8_t*>(ix->q) + r0 * qi_row;
-    sub.w = ix->w + r0 * ix->heads;
-    if (ix->q_scale) sub.q_scale = ix->q_scale + r0 * ix->heads;
-    cudaError_t e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer(qb, cm, sub, scores, ld, err, st); });
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
-    e = launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(qb, scores, ld, k, idx + r0 * k, err, st); });
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
-  }
-  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
+  const int64_t rows = (int64_t)(workspace_bytes / (score_ld(qd->max_kv) * sizeof(float)));
+  return run_staged(qd, cd, ix, k, at, idx, out, lse, static_cast<float*>(workspace), rows, err, st);
 }
 
 dsa_status dsa_cache_append(const dsa_cache_desc* cd, int32_t num_tok, const int32_t* tok_seq, const int32_t* tok_pos,
@@ -357,24 +371,8 @@ dsa_status dsa_forward_noalloc(const dsa_query_desc* qd, const dsa_cache_desc* c
   if (!err) return DSA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  const CacheMap cm = to_map(cd);
-  const int64_t ld = score_ld(qd->max_kv);
-  const int64_t rows = std::max<int64_t>(
-      1, std::min<int64_t>(qd->num_q, (int64_t)(DSA_NOALLOC_SCRATCH_BYTES / (ld * sizeof(float)))));
-  const size_t qi_row = (size_t)ix->heads * ix->dim * idx_elem_size(ix);
-  for (int64_t r0 = 0; r0 < qd->num_q; r0 += rows) {
-    const int n = (int)std::min<int64_t>(rows, qd->num_q - r0);
-    QueryBatch qb{qd->q_seq + r0, qd->q_pos + r0, n, qd->max_kv};
-    dsa_indexer_inputs sub = *ix;
-    sub.q = static_cast<const uint8_t*>(ix->q) + r0 * qi_row;
-    sub.w = ix->w + r0 * ix->heads;
-    if (ix->q_scale) sub.q_scale = ix->q_scale + r0 * ix->heads;
-    cudaError_t e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer(qb, cm, sub, scores, ld, err, st); });
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
-    e = launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(qb, scores, ld, k, idx + r0 * k, err, st); });
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
-  }
-  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
+  const int64_t rows = (int64_t)(DSA_NOALLOC_SCRATCH_BYTES / (score_ld(qd->max_kv) * sizeof(float)));
+  return run_staged(qd, cd, ix, k, at, idx, out, lse, scores, rows, err, st);
 }
 
 dsa_status dsa_profile_start(int32_t capacity) {

@@ -22,9 +22,15 @@
 // When the guess misses (fewer than k collected, or a list overflows) the
 // block falls back to the same radix rounds over the whole row, followed by
 // an ordered compaction of the whole row.  Rows are read with 16-byte loads
-// straight from global memory: inside the fused forward they were just
-// written by the indexer and sit in L2.  Blocks of 256 threads let several
-// rows share an SM; batches with few rows use 1024-thread blocks instead.
+// straight from global memory (inside the fused forward the indexer has just
+// written them).  Blocks of 256 threads let several rows share an SM; batches
+// with few rows, or lists too large for several blocks an SM, use
+// 1024-thread blocks instead.  The list is sized at launch from k and the
+// longest row, and a row whose expected candidates would nearly fill it goes
+// straight to the exact rounds.
+#include <algorithm>
+#include <cmath>
+
 #include "launch.h"
 
 namespace dsa {
@@ -126,11 +132,13 @@ struct RowKeys {
 
 constexpr int kSamples = 1024;
 
-// Per-warp capacity of the candidate list (the list is 32 or 64 KiB of
-// dynamic shared memory: keys and positions).
-template <int NT> struct Region;   // per-warp list capacity; NW * kPerWarp >= kCandCap
+// Smallest per-warp capacity of the candidate list (keys and positions in
+// dynamic shared memory, 8 bytes a slot); the launch raises it for large k or
+// long rows.  NW * kPerWarp >= kCandCap, which the fallback needs.
+template <int NT> struct Region;
 template <> struct Region<256> { static constexpr int kPerWarp = 512; };   // 44 KiB a block: five blocks per SM
 template <> struct Region<1024> { static constexpr int kPerWarp = 256; };
+constexpr int kMaxListBytes = 200 << 10;   // dynamic shared memory cap for the list
 
 template <int NT>
 struct TopkShared {
@@ -353,10 +361,9 @@ __device__ __forceinline__ uint32_t select_in_list(int total, Get get, uint32_t 
 template <int NT>
 __global__ void __launch_bounds__(NT)
 topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, int32_t* __restrict__ idx,
-            int* err) {
+            int R, int* err) {
   constexpr int NW = NT / 32;
-  constexpr int R = Region<NT>::kPerWarp;
-  extern __shared__ __align__(16) uint32_t dsm[];   // [NW * R] candidate keys, then [NW * R] positions
+  extern __shared__ __align__(16) uint32_t dsm[];   // [NW * R] candidate keys, then [NW * R] positions (R per warp)
   uint32_t* ckey = dsm;
   uint32_t* cpos = dsm + NW * R;
   __shared__ uint32_t hist[kBins];
@@ -382,7 +389,15 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, 
   const RowKeys rk{row, n, (reinterpret_cast<uintptr_t>(row) & 15) == 0};
 
   // ---- 1. a threshold guess from evenly spaced samples: the r-th largest
-  // sample, r a safe margin above the expected rank of the k-th largest key
+  // sample, r a safe margin above the expected rank of the k-th largest key.
+  // When the r n / 1024 keys expected above it would nearly fill the list,
+  // the guess would overflow it: take the exact rounds over the row at once.
+  const float f = (float)kSamples * (float)k / (float)n;
+  const int r = min(kSamples, (int)ceilf(f + 3.f * sqrtf(f) + 8.f));
+  if (8 * (int64_t)r * n > 7 * (int64_t)kSamples * NW * R) {   // block-uniform
+    radix_path<NT>(rk, k, out, err, hist, dsm, warp_tot, S);
+    return;
+  }
   for (int s = tid; s < kSamples; s += NT) samp[s] = score_key(__ldg(row + (int)(((int64_t)s * n) / kSamples)));
   if (tid == 0) {
     S.overflow = 0;
@@ -390,8 +405,6 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, 
     S.sel_above = 0;
   }
   __syncthreads();
-  const float f = (float)kSamples * (float)k / (float)n;
-  const int r = min(kSamples, (int)ceilf(f + 3.f * sqrtf(f) + 8.f));
   uint32_t unused;
   const uint32_t G = select_in_list<NT>(kSamples, [&](int s, uint32_t& u) { u = samp[s]; return true; }, (uint32_t)r,
                                         hist, warp_tot, S, &unused, 2);
@@ -399,31 +412,39 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, 
   // ---- 2. one pass over the row: every key >= G with its position, into
   // the warp's region of the list, in position order (warp w scans the
   // contiguous segment [w*seg, (w+1)*seg); seg a multiple of 128, four
-  // candidates per lane and step)
+  // candidates per lane and step, four steps' loads in flight)
   const int seg = ((n + NW - 1) / NW + 127) & ~127;
   const int beg = warp * seg, end = min(n, beg + seg);
   uint32_t cnt = 0;
-  for (int j0 = beg; j0 < end; j0 += 128) {   // warp-uniform bound
-    const int j = j0 + 4 * lane;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (j < end) v = rk.load4(j);
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-    uint32_t m = 0;
+#pragma unroll 1
+  for (int j0 = beg; j0 < end; j0 += 512) {   // warp-uniform bound
+    uint4 v[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (j + e < end && u[e] >= G) m |= 1u << e;
-    uint32_t tot;
-    uint32_t slot = cnt + warp_excl_scan(__popc(m), &tot);
+    for (int t = 0; t < 4; ++t) {
+      const int j = j0 + 128 * t + 4 * lane;
+      v[t] = j < end ? rk.load4(j) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (m & (1u << e)) {
-        if (slot < (uint32_t)R) {
-          ckey[warp * R + slot] = u[e];
-          cpos[warp * R + slot] = (uint32_t)(j + e);
+    for (int t = 0; t < 4; ++t) {
+      const int j = j0 + 128 * t + 4 * lane;
+      const uint32_t u[4] = {v[t].x, v[t].y, v[t].z, v[t].w};
+      uint32_t m = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (j + e < end && u[e] >= G) m |= 1u << e;
+      uint32_t tot;
+      uint32_t slot = cnt + warp_excl_scan(__popc(m), &tot);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (m & (1u << e)) {
+          if (slot < (uint32_t)R) {
+            ckey[warp * R + slot] = u[e];
+            cpos[warp * R + slot] = (uint32_t)(j + e);
+          }
+          ++slot;
         }
-        ++slot;
-      }
-    cnt += tot;
+      cnt += tot;
+    }
   }
   if (lane == 0) {
     S.w_cnt[warp] = cnt;
@@ -441,10 +462,13 @@ topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, 
   // ---- 3. the exact k-th largest key among the candidates (all keys >= G,
   // at least k of them, so the row's top k are among them)
   uint32_t need;
+  // c / R as a multiply-high: exact, since c < 2^16 and the reciprocal's error
+  // stays far below 1/R
+  const uint32_t inv_r = (uint32_t)(0xffffffffull / (uint32_t)R) + 1u;
   const uint32_t T = select_in_list<NT>(
       NW * R,
       [&](int c, uint32_t& u) {
-        const int w = c / R;
+        const int w = (int)__umulhi((uint32_t)c, inv_r);
         if ((uint32_t)(c - w * R) >= S.w_cnt[w]) return false;
         u = ckey[c];
         return true;
@@ -514,25 +538,46 @@ int sm_count_topk() {
   return cache[dev];
 }
 
+// Per-warp list capacity for rows of up to max_kv keys: 4/3 of the keys
+// expected above the sampled guess in the longest row, spread over the warps,
+// rounded up to 32; at least the default and at most kMaxListBytes in all.
+int list_per_warp(int nt, int k, int max_kv) {
+  const int nw = nt / 32;
+  const double n = (double)std::max(max_kv, 1);
+  const double f = (double)kSamples * k / n;
+  const double r = std::min((double)kSamples, std::ceil(f + 3.0 * std::sqrt(f) + 8.0));
+  const double expect = std::min(n, r * n / kSamples);
+  int per = (int)std::ceil(expect * 4.0 / 3.0 / nw);
+  per = (per + 31) & ~31;
+  const int lo = nt == kManyRowsThreads ? Region<kManyRowsThreads>::kPerWarp : Region<kFewRowsThreads>::kPerWarp;
+  const int hi = kMaxListBytes / (8 * nw);
+  return std::max(lo, std::min(per, hi));
+}
+
+template <int NT>
+cudaError_t launch_topk_nt(const QueryBatch& qb, const float* scores, int64_t ld, int k, int32_t* idx, int per,
+                           int* err, cudaStream_t stream) {
+  const int smem = 2 * (NT / 32) * per * (int)sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  topk_kernel<NT><<<qb.num_q, NT, smem, stream>>>(qb, scores, ld, k, idx, per, err);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
+// Many rows: 256-thread blocks, several per SM, while the list stays within
+// 100 KiB; otherwise (few rows, or a list that would leave one narrow block
+// per SM) 1024-thread blocks.
 cudaError_t launch_topk(const QueryBatch& qb, const float* scores, int64_t ld, int k, int32_t* idx,
                         int* err, cudaStream_t stream) {
-  // many rows: small blocks, several per SM; few rows: wide blocks
   if (qb.num_q >= 2 * sm_count_topk()) {
-    constexpr int NT = kManyRowsThreads;
-    const int smem = 2 * (NT / 32) * Region<NT>::kPerWarp * (int)sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    topk_kernel<NT><<<qb.num_q, NT, smem, stream>>>(qb, scores, ld, k, idx, err);
-  } else {
-    constexpr int NT = kFewRowsThreads;
-    const int smem = 2 * (NT / 32) * Region<NT>::kPerWarp * (int)sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    topk_kernel<NT><<<qb.num_q, NT, smem, stream>>>(qb, scores, ld, k, idx, err);
+    const int per = list_per_warp(kManyRowsThreads, k, qb.max_kv);
+    if (8 * (kManyRowsThreads / 32) * per <= (100 << 10))
+      return launch_topk_nt<kManyRowsThreads>(qb, scores, ld, k, idx, per, err, stream);
   }
-  return cudaGetLastError();
+  return launch_topk_nt<kFewRowsThreads>(qb, scores, ld, k, idx, list_per_warp(kFewRowsThreads, k, qb.max_kv), err,
+                                         stream);
 }
 
 }  // namespace dsa

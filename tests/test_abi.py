@@ -56,9 +56,12 @@ def test_workspace_size_validation():
     assert L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix()), 8193, ctypes.byref(_at())) == 0
     assert L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix(heads=32)), 2048, ctypes.byref(_at())) == 0
     assert L.dsa_forward_workspace_size(ctypes.byref(qd), ctypes.byref(_ix()), 2048, ctypes.byref(_at(d_v=256))) == 0
-    # staged scores are bounded (64 MiB) however many queries there are
+    # staged scores are bounded (1 GiB) however many queries there are, and hold at least one row
     big = api.QueryDesc(1 << 20, 0x10000, 0x10000, 131072)
-    assert L.dsa_forward_workspace_size(ctypes.byref(big), ctypes.byref(_ix()), 2048, ctypes.byref(_at())) <= 64 << 20
+    assert 131072 * 4 <= L.dsa_forward_workspace_size(ctypes.byref(big), ctypes.byref(_ix()), 2048,
+                                                       ctypes.byref(_at())) <= 1 << 30
+    huge = api.QueryDesc(4, 0x10000, 0x10000, 1 << 22)
+    assert L.dsa_forward_workspace_size(ctypes.byref(huge), ctypes.byref(_ix()), 2048, ctypes.byref(_at())) == 4 << 24
 
 
 def test_host_validation_rejects_before_launch():

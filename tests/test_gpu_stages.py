@@ -136,6 +136,23 @@ def test_topk_exact_large_k(k, nq):
         assert np.array_equal(got[i], O.topk_select(s_np[i, :p + 1], k)), f"row {i} pos {p}"
 
 
+@pytest.mark.parametrize("k", [2048, 4096])
+def test_topk_exact_long_rows(k):
+    """Rows up to 131072 keys (a 128K context): the candidate list is sized
+    for the longest row, so the sampled path holds the expected candidates."""
+    n, nq = 131072, 400
+    sc = inputs.make_scores(nq, n, seed=k + 7, device=DEV)
+    pos = torch.linspace(k, n - 1, nq).round().to(torch.int32)
+    batch = api.Batch(torch.zeros(nq, dtype=torch.int32, device=DEV), pos.to(DEV), n)
+    idx = torch.empty((nq, k), dtype=torch.int32, device=DEV)
+    api.dsa_topk(batch.desc(), sc, k, idx)
+    assert api.dsa_check_device_error() == api.DSA_OK
+    got, s_np = idx.cpu().numpy(), sc.cpu().numpy()
+    for i in list(range(0, nq, nq // 10)) + [nq - 1]:
+        p = int(pos[i])
+        assert np.array_equal(got[i], O.topk_select(s_np[i, :p + 1], k)), f"row {i} pos {p}"
+
+
 def test_topk_ignores_scores_beyond_position():
     n, k = 4096, 64
     sc = inputs.make_scores(2, n, seed=9, device=DEV)
