@@ -65,7 +65,7 @@ typedef enum {
   DSA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   DSA_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (reported by dsa_check_device_error) */
   DSA_ERR_BOUNDS = 5,      /* device-side range check failed (reported by dsa_check_device_error) */
-  DSA_ERR_WORKSPACE = 6    /* workspace NULL, misaligned (256 B) or smaller than required */
+  DSA_ERR_WORKSPACE = 6    /* workspace NULL, misaligned (256 B) or smaller than one staged row */
 } dsa_status;
 
 typedef enum { DSA_F32 = 0, DSA_BF16 = 1, DSA_FP8_E4M3 = 2 } dsa_dtype;
@@ -158,9 +158,9 @@ DSA_API dsa_status dsa_sparse_attn(const dsa_query_desc* qd, const dsa_cache_des
                            const dsa_attn_inputs* at, const int32_t* idx, int32_t k,
                            void* out, float* lse, dsa_stream_t stream);
 
-/* Bytes of workspace dsa_forward needs for this batch (0 if the arguments are
- * invalid): the score rows of all num_q queries, capped at 1 GiB but never
- * less than one row.  Depends only on the host-side fields (num_q, max_kv, k,
+/* Recommended bytes of workspace for dsa_forward on this batch (0 if the
+ * arguments are invalid): the score rows of all num_q queries, capped at
+ * 1 GiB but never less than one row.  Depends only on the host-side fields (num_q, max_kv, k,
  * dtypes, shapes). */
 DSA_API size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
                                   const dsa_attn_inputs* at);
@@ -168,12 +168,13 @@ DSA_API size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_in
 /* The whole hot path: indexer -> top-k -> sparse attention for a batch of
  * prefill chunks and/or decode tokens.  Writes idx [num_q, k] (the selected
  * positions, as dsa_topk would write them), out and lse (as dsa_sparse_attn).
- * workspace: >= dsa_forward_workspace_size() bytes, 256-byte aligned, owned by
- * the caller and not read before it is written (no zeroing needed); it must
- * not be used by other work while this call's kernels run.  It holds the
- * staged indexer scores: the queries run in equal stages of as many score
- * rows (max_kv rounded up to a multiple of 4, times 4 bytes, each) as it holds, so a
- * larger workspace means fewer, fuller stages and the same results. */
+ * workspace: 256-byte aligned, owned by the caller and not read before it is
+ * written (no zeroing needed); it must not be used by other work while this
+ * call's kernels run.  It holds the staged indexer scores: the queries run in
+ * equal stages of as many score rows (max_kv rounded up to a multiple of 4,
+ * times 4 bytes, each) as it holds.  One row is the least it may hold;
+ * dsa_forward_workspace_size() gives the recommended size.  Any size gives the
+ * same results; fewer, fuller stages run faster. */
 DSA_API dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd,
                        const dsa_indexer_inputs* ix, int32_t k, const dsa_attn_inputs* at,
                        int32_t* idx, void* out, float* lse,

@@ -252,8 +252,8 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const
   DSA_TRY(check_indexer(ix));
   DSA_TRY(check_attn(at));
   if (!idx || !out || !lse || !aligned(idx, 4) || !aligned(out, 16) || !aligned(lse, 4)) return DSA_ERR_INVALID_ARG;
-  const size_t need = dsa_forward_workspace_size(qd, ix, k, at);
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return DSA_ERR_WORKSPACE;
+  const size_t row_bytes = (size_t)score_ld(qd->max_kv) * sizeof(float);   // the least: one staged row
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < row_bytes) return DSA_ERR_WORKSPACE;
   int* err = device_error_ptr();
   if (!err) return DSA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

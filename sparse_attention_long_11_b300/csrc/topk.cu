@@ -23,9 +23,9 @@
 // block falls back to the same radix rounds over the whole row, followed by
 // an ordered compaction of the whole row.  Rows are read with 16-byte loads
 // straight from global memory (inside the fused forward the indexer has just
-// written them).  Blocks of 256 threads let several rows share an SM; batches
-// with few rows, or lists too large for several blocks an SM, use
-// 1024-thread blocks instead.  The list is sized at launch from k and the
+// written them).  Blocks of 512 threads let four rows share an SM; batches
+// with few rows, rows longer than 65536 keys, or lists too large for several
+// blocks an SM use 1024-thread blocks instead.  The list is sized at launch from k and the
 // longest row, and a row whose expected candidates would nearly fill it goes
 // straight to the exact rounds.
 #include <algorithm>
@@ -38,7 +38,8 @@ namespace {
 
 constexpr int kBins = 2048;
 constexpr int kCandCap = 4096;   // threshold-bin keys gathered for the finer rounds (the candidate-list buffer)
-constexpr int kManyRowsThreads = 256, kFewRowsThreads = 1024;
+constexpr int kManyRowsThreads = 512, kFewRowsThreads = 1024;
+constexpr int kLongRow = 65536;   // rows beyond this many keys scan faster with 1024-thread blocks
 
 template <int NT>
 __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t* warp_tot) {
@@ -136,7 +137,7 @@ constexpr int kSamples = 1024;
 // dynamic shared memory, 8 bytes a slot); the launch raises it for large k or
 // long rows.  NW * kPerWarp >= kCandCap, which the fallback needs.
 template <int NT> struct Region;
-template <> struct Region<256> { static constexpr int kPerWarp = 512; };   // 44 KiB a block: five blocks per SM
+template <> struct Region<512> { static constexpr int kPerWarp = 256; };    // 32 KiB a block: four blocks per SM
 template <> struct Region<1024> { static constexpr int kPerWarp = 256; };
 constexpr int kMaxListBytes = 200 << 10;   // dynamic shared memory cap for the list
 
@@ -359,7 +360,7 @@ __device__ __forceinline__ uint32_t select_in_list(int total, Get get, uint32_t 
 }
 
 template <int NT>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, NT == kManyRowsThreads ? 2048 / NT : 1)
 topk_kernel(QueryBatch qb, const float* __restrict__ scores, int64_t ld, int k, int32_t* __restrict__ idx,
             int R, int* err) {
   constexpr int NW = NT / 32;
@@ -566,12 +567,13 @@ cudaError_t launch_topk_nt(const QueryBatch& qb, const float* scores, int64_t ld
 
 }  // namespace
 
-// Many rows: 256-thread blocks, several per SM, while the list stays within
-// 100 KiB; otherwise (few rows, or a list that would leave one narrow block
-// per SM) 1024-thread blocks.
+// Many rows of at most kLongRow keys: 512-thread blocks, four per SM, while
+// the list stays within 100 KiB; otherwise (few rows, long rows, or a list
+// that would leave one narrow block per SM) 1024-thread blocks, whose 32
+// warps keep more loads in flight for each row.
 cudaError_t launch_topk(const QueryBatch& qb, const float* scores, int64_t ld, int k, int32_t* idx,
                         int* err, cudaStream_t stream) {
-  if (qb.num_q >= 2 * sm_count_topk()) {
+  if (qb.num_q >= 2 * sm_count_topk() && qb.max_kv <= kLongRow) {
     const int per = list_per_warp(kManyRowsThreads, k, qb.max_kv);
     if (8 * (kManyRowsThreads / 32) * per <= (100 << 10))
       return launch_topk_nt<kManyRowsThreads>(qb, scores, ld, k, idx, per, err, stream);

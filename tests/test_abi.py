@@ -81,6 +81,7 @@ def test_host_validation_rejects_before_launch():
     assert f(*args(ws=None)) == api.DSA_ERR_WORKSPACE
     assert f(*args(ws=0x10010)) == api.DSA_ERR_WORKSPACE                      # not 256-byte aligned
     assert f(*args(wsb=1024)) == api.DSA_ERR_WORKSPACE
+    assert f(*args(wsb=4096 * 4 - 4)) == api.DSA_ERR_WORKSPACE                # less than one staged score row
     assert f(*args(q=api.QueryDesc(16, 0x10000, 0x10000, 0))) == api.DSA_ERR_INVALID_ARG
     assert f(*args(c=api.CacheDesc(2, 4096, 100, None, 0, 0))) == api.DSA_ERR_INVALID_ARG   # overlapping seqs
     assert f(*args(c=api.CacheDesc(1, 4096, 0, 0x10000, 64, 2))) == api.DSA_ERR_INVALID_ARG  # table too short

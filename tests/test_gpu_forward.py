@@ -61,6 +61,20 @@ def test_forward_other_k(k):
     _check_rows(wl, idx, out, lse, _sample(wl.num_q, 12, [k - 2, k - 1, k, wl.num_q - 1]), ATTN_ATOL_BF16)
 
 
+def test_forward_128k_context():
+    """A 131072-token prefill context (the long-context end of the sweep):
+    the last 4096 queries, one bench-sized call, sampled rows vs the oracle."""
+    torch.cuda.empty_cache()
+    L = 131072
+    wl = inputs.make_prefill(seed=6, device=DEV, L=L, q_rows=(L - 4096, L))
+    idx, out, lse = run_forward(api.Problem(wl))
+    assert api.dsa_check_device_error() == api.DSA_OK
+    _check_rows(wl, idx, out, lse, [0, 1500, 4095], ATTN_ATOL_BF16)
+    assert bool((idx >= 0).all()) and bool(torch.isfinite(out.float()).all())
+    del wl, idx, out, lse
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
 def test_forward_full_size(cfg):
     """Full workload sizes, launched as the benchmark launches them."""
@@ -113,6 +127,27 @@ def test_chunked_equals_whole_and_decode_equals_prefill_row():
         one = run_forward(api.Problem(wl), chunks=[(r, r + 1)])
         for x, y in zip(whole, one):
             assert torch.equal(x[r], y[r])
+
+
+def test_workspace_size_does_not_change_results():
+    """Stages of 1, 100 (not a divisor of the batch) and all rows give the same bits."""
+    wl = inputs.make_prefill(seed=8, device=DEV, L=2600)
+    prob = api.Problem(wl)
+    qd, ix, at = prob.rows(0, wl.num_q)
+    ld = (2600 + 3) // 4 * 4
+    res = []
+    for rows in (None, 100, 1):
+        nb = api.dsa_forward_workspace_size(qd, ix, wl.topk, at) if rows is None else rows * ld * 4
+        ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+        idx = torch.empty((wl.num_q, wl.topk), dtype=torch.int32, device=DEV)
+        out = torch.empty((wl.num_q, wl.H, wl.d_v), dtype=prob.out_dtype(), device=DEV)
+        lse = torch.empty((wl.num_q, wl.H), dtype=torch.float32, device=DEV)
+        api.dsa_forward(qd, prob.cache.desc(), ix, wl.topk, at, idx, out, lse, ws)
+        assert api.dsa_check_device_error() == api.DSA_OK
+        res.append((idx, out, lse))
+    for other in res[1:]:
+        for x, y in zip(res[0], other):
+            assert torch.equal(x, y)
 
 
 def test_fused_selection_equals_staged_stages():
