@@ -36,6 +36,13 @@ key-cache encoding (quantize_e4m3_rows): the FP8 keys of the summary card's
 "cheap FP8 relevance scores" are written once per token as e4m3 codes with a
 per-row scale amax/448, and the codes that write produces are decided by its
 float32 scale and division, which the oracle therefore takes in float32.
+
+FP8 latent KV cache (an optional storage format of the attention cache; the
+pages name no KV format, so this library reuses the key-cache encoding for
+it): each 576-wide latent row is stored as e4m3 codes with one fp32 scale,
+and the attention reads row s as bf16(scale_s * code_s), the product taken in
+float32 and rounded once to bfloat16 (dequantize_kv_e4m3).  The attention
+itself is then the bf16 one above, on those values.
 """
 from __future__ import annotations
 
@@ -104,6 +111,25 @@ def quantize_e4m3_rows(x) -> tuple:
     scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
     y = (x / scale[:, None]).astype(np.float32)
     return encode_e4m3(y), scale
+
+
+def round_bf16(x) -> np.ndarray:
+    """float32 values -> the nearest bfloat16 value (ties to the even bit
+    pattern), as float64.  bf16 keeps the top 16 bits of a binary32, so the
+    rounding adds half a unit of the dropped 16 bits, plus one when the kept
+    part is odd, and truncates.  Inputs are finite."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) & np.uint64(0xFFFF0000)
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def dequantize_kv_e4m3(codes, scale) -> np.ndarray:
+    """FP8 latent rows -> the bf16 values the attention reads:
+    bf16(float32(scale[r]) * float32(e4m3 value of codes[r, d])).
+    codes [n, d] uint8, scale [n] float32; returns float64 [n, d]."""
+    v = decode_e4m3(codes).astype(np.float32)                    # exact: e4m3 values fit float32
+    prod = (np.asarray(scale, dtype=np.float32)[:, None] * v).astype(np.float32)
+    return round_bf16(prod)
 
 
 def decode_bf16(bits) -> np.ndarray:

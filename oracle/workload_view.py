@@ -26,9 +26,17 @@ def _decode_idx(t: torch.Tensor, dtype: str) -> np.ndarray:
 
 
 def _decode_attn(t: torch.Tensor, dtype: str) -> np.ndarray:
-    if dtype == "bf16":
+    if dtype in ("bf16", "fp8kv"):          # queries are bf16 in both
         return O.decode_bf16(_np_bits16(t))
     return t.detach().to("cpu").numpy().astype(np.float64)
+
+
+def _decode_kv(wl, rows: torch.Tensor) -> np.ndarray:
+    if wl.attn_dtype == "fp8kv":
+        codes = wl.kv[rows].detach().to("cpu").contiguous().view(torch.uint8).numpy()
+        scale = wl.kv_scale[rows].detach().to("cpu").numpy().astype(np.float32)
+        return O.dequantize_kv_e4m3(codes, scale)
+    return _decode_attn(wl.kv[rows], wl.attn_dtype)
 
 
 class OracleView:
@@ -51,7 +59,7 @@ class OracleView:
         wl = self.wl
         k_vals = _decode_idx(wl.k_idx[rows], wl.idx_dtype)
         k_scale = None if wl.k_scale is None else wl.k_scale[rows].to("cpu").numpy().astype(np.float64)
-        kv = _decode_attn(wl.kv[rows], wl.attn_dtype)
+        kv = _decode_kv(wl, rows)
         self._seq_cache = {seq: (n, (k_vals, k_scale, kv))}  # keep one sequence resident
         return k_vals, k_scale, kv
 

@@ -89,6 +89,49 @@ def test_bf16_matches_torch():
     assert np.array_equal(O.decode_bf16(bits), b.to(torch.float64).numpy())
 
 
+def test_bf16_rounding_ties_and_torch():
+    # hand cases: exact, below/above the halfway point, ties to the even pattern, sign
+    one = np.float32(1.0)
+    ulp = 2.0 ** -7                                             # bf16 spacing just above 1
+    cases = {1.0: 1.0, 1.0 + 2 ** -9: 1.0, 1.0 + 2 ** -8 + 2 ** -20: 1.0 + ulp,
+             1.0 + 2 ** -8: 1.0,                                # tie, 1.0 is even -> stays
+             1.0 + 3 * 2 ** -8: 1.0 + 2 * ulp,                 # tie between 1+ulp (odd) and 1+2ulp (even)
+             -(1.0 + 3 * 2 ** -8): -(1.0 + 2 * ulp), 0.0: 0.0}
+    for x, want in cases.items():
+        assert O.round_bf16(np.float32(x)) == want, x
+    assert O.round_bf16(one) == 1.0
+    # torch's float32 -> bfloat16 cast on random values and constructed ties
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(20000, generator=g, dtype=torch.float32) * 50
+    ties = (x.view(torch.int32) & ~0xFFFF) | 0x8000
+    for t in (x, ties.view(torch.float32)):
+        assert np.array_equal(O.round_bf16(t.numpy()), t.to(torch.bfloat16).to(torch.float64).numpy())
+
+
+def test_fp8_kv_dequantisation():
+    codes = np.arange(256, dtype=np.uint8).reshape(4, 64)
+    finite = ~np.isnan(O.decode_e4m3(codes))
+    # scale 1 and powers of two: the product is exact and every e4m3 value is a bf16 value
+    for sc in (1.0, 2.0 ** -5, 2.0 ** 7):
+        got = O.dequantize_kv_e4m3(codes, np.full(4, sc, dtype=np.float32))
+        assert np.array_equal(got[finite], O.decode_e4m3(codes)[finite] * sc)
+    # signed zero and the subnormal step survive
+    got = O.dequantize_kv_e4m3(np.array([[0x00, 0x80, 0x01, 0x7E]], dtype=np.uint8), np.array([3.0], np.float32))
+    assert got[0, 0] == 0.0 and np.signbit(got[0, 1]) and got[0, 2] == 3.0 * 2.0 ** -9 and got[0, 3] == 1344.0
+    # arbitrary scales: torch's float8 decode, a float32 multiply and its bfloat16 cast, bit for bit
+    g = torch.Generator().manual_seed(5)
+    c = torch.randint(0, 256, (300, 576), generator=g, dtype=torch.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x11                                # no NaN codes
+    sc = torch.rand(300, generator=g, dtype=torch.float32) * 0.01 + 1e-4
+    want = (c.view(torch.float8_e4m3fn).to(torch.float32) * sc[:, None]).to(torch.bfloat16).to(torch.float64)
+    assert np.array_equal(O.dequantize_kv_e4m3(c.numpy(), sc.numpy()), want.numpy())
+    # a quantised row comes back within the e4m3 step and the bf16 rounding of the row
+    x = np.random.default_rng(0).standard_normal((8, 576)).astype(np.float32)
+    q, s8 = O.quantize_e4m3_rows(x)
+    back = O.dequantize_kv_e4m3(q, s8)
+    assert np.all(np.abs(back - x) <= np.abs(x) * (2.0 ** -4 + 2.0 ** -8) + 2.0 ** -9 * s8[:, None])
+
+
 # --------------------------------------------------------------------------- indexer
 
 def test_indexer_hand_cases():
