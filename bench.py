@@ -43,6 +43,7 @@ FLOP_PER_ATTN_PAIR = 2 * 128 * (576 + 512)        # QK^T + PV per selected (quer
 FLOP_PER_IDX_PAIR = 2 * 64 * 128                  # per causal (query, key) indexer pair
 BYTES_PER_IDX_KEY = 128 + 4                       # FP8 key row + its scale
 BYTES_PER_ATTN_KEY = 576 * 2                      # gathered bf16 latent row
+BYTES_PER_ATTN_KEY_FP8 = 576 + 4                  # gathered FP8 latent row and its scale
 
 
 def _traffic(entry: str, kernel: str):
@@ -420,6 +421,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-k-sweep", action="store_true")
     ap.add_argument("--no-128k", action="store_true")
+    ap.add_argument("--no-fp8-kv", action="store_true")
     args = ap.parse_args()
     ws, rank, local = _dist()
     if args.impl == "reference":
@@ -448,6 +450,16 @@ def main():
         cpu = {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{done} queries at evenly spaced positions of the L=32768 prefill, "
                          f"full oracle path (indexer, top-k, attention) in {dt:.1f} s"}
+    prefill_fp8_kv = None
+    if not args.no_fp8_kv:
+        # the same prefill over an FP8 latent cache (not part of the headline value)
+        r8 = Runner(inputs.with_fp8_kv(wl))
+        ms8, st8, _, _ = _time_steps(r8, 2, args.warmup, ws, local)
+        ms8 = _max_over_ranks(ms8, ws)
+        prefill_fp8_kv = {"value": wl.num_q * ws / (ms8 / 1e3), "unit": "tokens/s", "ms_per_step": ms8,
+                          "stages": {n: round(v[1] / 2, 3) for n, v in st8.items()}}
+        del r8
+        torch.cuda.empty_cache()
     k_sweep = None
     if not args.no_k_sweep:
         # the same prefill and inputs with other top-k sizes (not part of the headline value)
@@ -493,7 +505,20 @@ def main():
                              for k, v in dstage.items()},
                   "roofline": _roofline_decode(wd, dstage, max(args.steps, 10), peaks), "clocks": dclk}
         decode["cache_append"] = _time_append(wd, rd, max(args.steps, 10), args.warmup)
-        del rd, wd
+        del rd
+        if not args.no_fp8_kv:
+            # the same batch over an FP8 latent cache (e4m3 codes + one fp32 scale per row)
+            w8 = inputs.with_fp8_kv(wd)
+            r8 = Runner(w8)
+            ms8, st8, _, _ = _time_steps(r8, max(args.steps, 10), args.warmup, ws, local)
+            v8, ms8 = aggregate(w8.num_q, ms8, ws)
+            _, n_attn = _pairs(w8)
+            a_ms = st8["attention"][1] / max(args.steps, 10)
+            decode["fp8_kv"] = {"value": v8, "unit": "tokens/s", "ms_per_step": ms8,
+                                "stages": {n: round(v[1] / max(args.steps, 10), 4) for n, v in st8.items()},
+                                "attention_gather_gbs": n_attn * BYTES_PER_ATTN_KEY_FP8 / (a_ms / 1e3) / 1e9}
+            del r8, w8
+        del wd
         torch.cuda.empty_cache()
 
     if rank == 0:
@@ -508,7 +533,7 @@ def main():
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "cpu_baseline": cpu, "decode": decode, "k_sweep": k_sweep,
-                "prefill_128k": long128k}
+                "prefill_128k": long128k, "prefill_fp8_kv": prefill_fp8_kv}
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist

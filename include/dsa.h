@@ -116,11 +116,20 @@ typedef struct {
 
 /* Attention operands: MQA over one shared latent row per token; the value of
  * a row is its first d_v entries.
- *   DSA_BF16: heads = 128, d_qk = 576, d_v = 512 (the DeepSeek-V3.2 latent
- *             shape), output bf16;
- *   DSA_F32:  heads in {8, 16, ..., 128} (multiple of 8), d_qk <= 576 and a
- *             multiple of 4, d_v <= d_qk and a multiple of 4, output fp32.
- * q and kv must be 16-byte aligned. */
+ *   DSA_BF16:     heads = 128, d_qk = 576, d_v = 512 (the DeepSeek-V3.2
+ *                 latent shape), q and kv bf16, output bf16;
+ *   DSA_FP8_E4M3: the same shape with the latent cache stored as FP8: kv
+ *                 holds OCP e4m3 codes [num_rows, 576] and kv_scale one fp32
+ *                 scale per row; row s is read as the bf16 values
+ *                 bf16(kv_scale[s] * code), the product in fp32 rounded once
+ *                 to nearest even.  q bf16, output bf16.  (The pages name no
+ *                 KV-cache format; this one reuses the indexer keys'
+ *                 per-row encoding and halves the bytes a gathered row costs.)
+ *   DSA_F32:      heads in {8, 16, ..., 128} (multiple of 8), d_qk <= 576 and
+ *                 a multiple of 4, d_v <= d_qk and a multiple of 4, output
+ *                 fp32.
+ * q and kv must be 16-byte aligned; kv_scale 4-byte aligned for
+ * DSA_FP8_E4M3 and NULL otherwise. */
 typedef struct {
   dsa_dtype dtype;
   int32_t heads;          /* H */
@@ -129,6 +138,7 @@ typedef struct {
   const void* q;          /* [num_q, heads, d_qk] */
   const void* kv;         /* [num_rows, d_qk] latent KV cache */
   float softmax_scale;    /* finite; logits are scale * <q, kv> */
+  const float* kv_scale;  /* DSA_FP8_E4M3: [num_rows] per-row scales; else NULL */
 } dsa_attn_inputs;
 
 /* Stage 1 alone (debug / parity API): materialises the score rows.

@@ -48,7 +48,7 @@ class IndexerInputs(ctypes.Structure):
 class AttnInputs(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("heads", ctypes.c_int32), ("d_qk", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("q", ctypes.c_void_p), ("kv", ctypes.c_void_p),
-                ("softmax_scale", ctypes.c_float)]
+                ("softmax_scale", ctypes.c_float), ("kv_scale", ctypes.c_void_p)]
 
 
 _P = ctypes.POINTER
@@ -156,8 +156,10 @@ def indexer_inputs(dtype: int, q, q_scale, w, k, k_scale) -> IndexerInputs:
     return IndexerInputs(dtype, q.shape[-2], q.shape[-1], _ptr(q), _ptr(q_scale), _ptr(w), _ptr(k), _ptr(k_scale))
 
 
-def attn_inputs(dtype: int, q, kv, d_v: int, softmax_scale: float) -> AttnInputs:
-    return AttnInputs(dtype, q.shape[-2], q.shape[-1], d_v, _ptr(q), _ptr(kv), softmax_scale)
+def attn_inputs(dtype: int, q, kv, d_v: int, softmax_scale: float, kv_scale=None) -> AttnInputs:
+    """DSA_FP8_E4M3: bf16 q, uint8 e4m3 kv codes and their fp32 kv_scale rows."""
+    return AttnInputs(dtype, q.shape[-2], q.shape[-1], d_v, _ptr(q), _ptr(kv), softmax_scale,
+                      None if kv_scale is None else _ptr(kv_scale))
 
 
 # --------------------------------------------------------------------------- entry points
@@ -263,9 +265,9 @@ class Problem:
         self.batch = Batch(wl.q_seq, wl.q_pos, wl.max_kv)
         self.cache = Cache(wl.num_seqs, wl.num_rows, wl.seq_stride, wl.block_table, wl.block_size)
         idt = DSA_FP8_E4M3 if wl.idx_dtype == "fp8" else DSA_F32
-        adt = DSA_BF16 if wl.attn_dtype == "bf16" else DSA_F32
+        adt = {"bf16": DSA_BF16, "fp8kv": DSA_FP8_E4M3}.get(wl.attn_dtype, DSA_F32)
         self.ix = indexer_inputs(idt, wl.q_idx, wl.q_scale, wl.w, wl.k_idx, wl.k_scale)
-        self.at = attn_inputs(adt, wl.q, wl.kv, wl.d_v, wl.softmax_scale)
+        self.at = attn_inputs(adt, wl.q, wl.kv, wl.d_v, wl.softmax_scale, wl.kv_scale)
         self.idx_dtype, self.attn_dtype = idt, adt
 
     def rows(self, r0: int, r1: int):
@@ -273,8 +275,8 @@ class Problem:
         wl = self.wl
         ix = indexer_inputs(self.idx_dtype, wl.q_idx[r0:r1], None if wl.q_scale is None else wl.q_scale[r0:r1],
                             wl.w[r0:r1], wl.k_idx, wl.k_scale)
-        at = attn_inputs(self.attn_dtype, wl.q[r0:r1], wl.kv, wl.d_v, wl.softmax_scale)
+        at = attn_inputs(self.attn_dtype, wl.q[r0:r1], wl.kv, wl.d_v, wl.softmax_scale, wl.kv_scale)
         return self.batch.desc(r0, r1), ix, at
 
     def out_dtype(self):
-        return torch.bfloat16 if self.attn_dtype == DSA_BF16 else torch.float32
+        return torch.float32 if self.attn_dtype == DSA_F32 else torch.bfloat16

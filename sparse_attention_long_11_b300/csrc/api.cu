@@ -75,7 +75,9 @@ dsa_status check_attn(const dsa_attn_inputs* at) {
   if (!at || !at->q || !at->kv) return DSA_ERR_INVALID_ARG;
   if (!aligned(at->q, 16) || !aligned(at->kv, 16)) return DSA_ERR_INVALID_ARG;
   if (!std::isfinite(at->softmax_scale)) return DSA_ERR_INVALID_ARG;
-  if (at->dtype == DSA_BF16) {
+  if ((at->dtype == DSA_FP8_E4M3) != (at->kv_scale != nullptr)) return DSA_ERR_INVALID_ARG;
+  if (at->kv_scale && !aligned(at->kv_scale, 4)) return DSA_ERR_INVALID_ARG;
+  if (at->dtype == DSA_BF16 || at->dtype == DSA_FP8_E4M3) {
     if (at->heads != 128 || at->d_qk != 576 || at->d_v != 512) return DSA_ERR_UNSUPPORTED;
   } else if (at->dtype == DSA_F32) {
     if (at->heads < 8 || at->heads > 128 || at->heads % 8) return DSA_ERR_UNSUPPORTED;

@@ -144,9 +144,33 @@ __device__ __forceinline__ QueryInfo query_info(const QueryBatch& qb, const int3
   return r;
 }
 
+// Eight e4m3 codes (memory order) -> the eight bf16 values
+// bf16(s * code): each code widened exactly (e4m3 -> f16 -> f32), the
+// product taken in fp32, then rounded once to nearest even.
+__device__ __forceinline__ uint4 e4m3x8_scaled_bf16(uint2 c, float s) {
+  uint32_t h[4];
+  asm("{\n .reg .b16 l0, h0, l1, h1;\n mov.b32 {l0, h0}, %4;\n mov.b32 {l1, h1}, %5;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, l0;\n cvt.rn.f16x2.e4m3x2 %1, h0;\n"
+      " cvt.rn.f16x2.e4m3x2 %2, l1;\n cvt.rn.f16x2.e4m3x2 %3, h1;\n}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(c.x), "r"(c.y));
+  const uint64_t ss = f2(s, s);
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 v = f16x2_to_f32x2(h[j]);             // (lower code, upper code)
+    const float2 p = f2_split(mul2(f2(v.x, v.y), ss));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(o[j]) : "f"(p.y), "f"(p.x));   // upper half = second code
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// kFp8Kv: the latent cache holds e4m3 codes and per-row scales (kv_scale);
+// the gather dequantises each row into the same bf16 shared-memory tiles.
+template <bool kFp8Kv>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat16* __restrict__ q,
-               const __nv_bfloat16* __restrict__ kv, QueryBatch qb, CacheMap cm, const int32_t* __restrict__ idx, int k, int prefix_valid,
+               const void* __restrict__ kv_raw, const float* __restrict__ kv_scale, QueryBatch qb, CacheMap cm, const int32_t* __restrict__ idx, int k, int prefix_valid,
                float scale_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -479,12 +503,69 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         if (e < k) s_e = __ldg(irow + e);
         ATTN_TRACE(2, g, 0 + 3 * wg, lane == 0);
         const int st = g % kStages;
+        if constexpr (kFp8Kv) {
+          // FP8 rows go through registers (8 codes = 8 bytes per lane and row
+          // in, 16 bytes of bf16 out, into the same swizzled slots the bf16
+          // path fills), so their loads may start before the stage is free:
+          // the first two batches of 8 rows are in flight during the wait,
+          // and after it each batch is converted while the next one loads.
+          int row = -1;
+          if (s_e >= 0 && s_e <= qi.pos) row = (int)cache_row(cm, seq, s_e, err);
+          else if (s_e != -1) flag_error(err, DSA_ERR_BOUNDS);
+          const uint8_t* kv8 = static_cast<const uint8_t*>(kv_raw);
+          const float srow = row >= 0 ? __ldg(kv_scale + row) : 0.f;
+          const uint8_t* lat8 = kv8 + crank * 256 + lane * 8;
+          const uint8_t* rope8 = kv8 + 512 + 32 * crank + (lane & 3) * 8;
+          auto load8 = [&](int b0, uint2 (&c)[8]) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int r = __shfl_sync(0xffffffffu, row, b0 + j);
+              c[j] = r >= 0 ? __ldg(reinterpret_cast<const uint2*>(lat8 + (int64_t)r * kDqk)) : make_uint2(0, 0);
+            }
+          };
+          uint8_t* sbp = sm + kOffKV + st * kKVStageBytes;
+          auto store8 = [&](int b0, const uint2 (&c)[8]) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float sj = __shfl_sync(0xffffffffu, srow, b0 + j);
+              *reinterpret_cast<uint4*>(sbp + (lane >> 3) * kKVSlotBytes + sw128_offset(32 * wg + b0 + j, lane & 7)) =
+                  e4m3x8_scaled_bf16(c[j], sj);
+            }
+          };
+          uint2 ca[8], cb[8], cr[4];
+          load8(0, ca);
+          load8(8, cb);
+          if (!(ok = mbar_wait(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
+          ATTN_TRACE(2, g, 1 + 3 * wg, lane == 0);
+          store8(0, ca);
+          load8(16, ca);
+          store8(8, cb);
+          load8(24, cb);
+          store8(16, ca);
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {   // rope: 8 rows x 4 lanes of 8 codes per step
+            const int r = __shfl_sync(0xffffffffu, row, it * 8 + (lane >> 2));
+            cr[it] = r >= 0 ? __ldg(reinterpret_cast<const uint2*>(rope8 + (int64_t)r * kDqk)) : make_uint2(0, 0);
+          }
+          store8(24, cb);
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const float sj = __shfl_sync(0xffffffffu, srow, it * 8 + (lane >> 2));
+            *reinterpret_cast<uint4*>(sbp + 4 * kKVSlotBytes + sw64_offset(32 * wg + it * 8 + (lane >> 2), lane & 3)) =
+                e4m3x8_scaled_bf16(cr[it], sj);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&B.kv_full[st]);
+          ATTN_TRACE(2, g, 2 + 3 * wg, lane == 0);
+          continue;
+        }
         if (!(ok = mbar_wait(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
         ATTN_TRACE(2, g, 1 + 3 * wg, lane == 0);
         int row = -1;                                         // physical rows fit in 31 bits
         if (s_e >= 0 && s_e <= qi.pos) row = (int)cache_row(cm, seq, s_e, err);
         else if (s_e != -1) flag_error(err, DSA_ERR_BOUNDS);
         const uint32_t sb = sKV + st * kKVStageBytes;
+        const __nv_bfloat16* kv = static_cast<const __nv_bfloat16*>(kv_raw);
         const __nv_bfloat16* lat = kv + crank * 256 + lane * 8;
         // one 32-bit broadcast per row; batches of 16 rows let the shuffles pipeline
 #pragma unroll
@@ -639,14 +720,15 @@ cudaError_t launch_attn_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_a
   if (!make_tmap_bf16(&q_rope, at.q, qrows, kDqk, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   const int ncl = std::min(qb.num_q, sm_count() / 2);
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+  const bool fp8 = at.dtype == DSA_FP8_E4M3;
+  auto kern = fp8 ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
   const float scale_log2 = (float)((double)at.softmax_scale * 1.4426950408889634);
-  attn_tc_kernel<<<2 * ncl, kThreads, kSmemAlloc, stream>>>(q_rope, static_cast<const __nv_bfloat16*>(at.q),
-                                                             static_cast<const __nv_bfloat16*>(at.kv),
-                                                             qb, cm, idx, k,
-                                                             prefix_valid ? 1 : 0, scale_log2,
-                                                             static_cast<__nv_bfloat16*>(out), lse, err);
+  kern<<<2 * ncl, kThreads, kSmemAlloc, stream>>>(q_rope, static_cast<const __nv_bfloat16*>(at.q), at.kv,
+                                                  fp8 ? at.kv_scale : nullptr, qb, cm, idx, k,
+                                                  prefix_valid ? 1 : 0, scale_log2,
+                                                  static_cast<__nv_bfloat16*>(out), lse, err);
   return cudaGetLastError();
 }
 

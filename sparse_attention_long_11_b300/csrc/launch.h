@@ -32,19 +32,20 @@ inline cudaError_t launch_indexer(const QueryBatch& qb, const CacheMap& cm, cons
   return launch_indexer_simt(qb, cm, ix, scores, ld, err, stream);
 }
 
-// Sparse attention on tcgen05 tensor cores: bf16, 128 heads, d_qk 576, d_v 512.
+// Sparse attention on tcgen05 tensor cores: 128 heads, d_qk 576, d_v 512, bf16
+// queries, a bf16 or FP8 (e4m3 + per-row scale) latent cache.
 // prefix_valid: every idx row is ascending with its valid entries first
 // (as the top-k stage writes them), so no row needs scanning.
 cudaError_t launch_attn_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_attn_inputs& at,
                            const int32_t* idx, int k, bool prefix_valid, void* out, float* lse, int* err,
                            cudaStream_t stream);
 
-// Stage dispatch: the tensor-core kernel for the bf16 latent shape, the
-// CUDA-core kernel for fp32 operands.
+// Stage dispatch: the tensor-core kernel for the latent shape (bf16 or FP8
+// cache), the CUDA-core kernel for fp32 operands.
 inline cudaError_t launch_attn(const QueryBatch& qb, const CacheMap& cm, const dsa_attn_inputs& at,
                                const int32_t* idx, int k, void* out, float* lse, int* err, cudaStream_t stream,
                                bool prefix_valid = false) {
-  if (at.dtype == DSA_BF16) return launch_attn_tc(qb, cm, at, idx, k, prefix_valid, out, lse, err, stream);
+  if (at.dtype == DSA_BF16 || at.dtype == DSA_FP8_E4M3) return launch_attn_tc(qb, cm, at, idx, k, prefix_valid, out, lse, err, stream);
   return launch_attn_simt(qb, cm, at, idx, k, out, lse, err, stream);
 }
 

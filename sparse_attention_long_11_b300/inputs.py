@@ -95,12 +95,12 @@ class Workload:
     k_scale: Optional[torch.Tensor]  # [rows] f32 (fp8 only)
     topk: int
     # attention
-    attn_dtype: str           # "f32" or "bf16"
+    attn_dtype: str           # "f32", "bf16", or "fp8kv" (bf16 queries, FP8 latent cache)
     H: int
     d_qk: int
     d_v: int
     q: torch.Tensor           # [num_q, H, d_qk]
-    kv: torch.Tensor          # [rows, d_qk]
+    kv: torch.Tensor          # [rows, d_qk] (uint8 e4m3 codes for "fp8kv")
     softmax_scale: float
     # batch layout
     q_seq: torch.Tensor       # [num_q] int32
@@ -110,6 +110,7 @@ class Workload:
     block_table: Optional[torch.Tensor]  # [num_seqs, max_blocks] int32 (paged) or None
     block_size: int
     chunks: List[Tuple[int, int]]  # query-row ranges processed as one call each
+    kv_scale: Optional[torch.Tensor] = None  # [rows] f32 ("fp8kv" only)
 
     @property
     def num_q(self) -> int:
@@ -170,6 +171,19 @@ def _bf16_normal(shape, seed, name, device, chunk_rows=1 << 14):
         r1 = min(shape[0], r0 + chunk_rows)
         flat[r0:r1] = randn((r1 - r0, flat.shape[1]), seed, f"{name}[{r0}]", device).to(torch.bfloat16)
     return out
+
+
+def with_fp8_kv(wl: Workload, chunk_rows: int = 1 << 16) -> Workload:
+    """The same workload with its latent KV cache stored as FP8: every bf16
+    row encoded like the indexer keys (e4m3 codes, one fp32 scale amax/448),
+    in row chunks to bound the fp32 transient.  Input preparation only."""
+    n = wl.kv.shape[0]
+    codes = torch.empty(wl.kv.shape, dtype=torch.uint8, device=wl.kv.device)
+    scale = torch.empty((n,), dtype=torch.float32, device=wl.kv.device)
+    for r0 in range(0, n, chunk_rows):
+        r1 = min(n, r0 + chunk_rows)
+        codes[r0:r1], scale[r0:r1] = quantize_fp8_rows(wl.kv[r0:r1].float())
+    return dataclasses.replace(wl, attn_dtype="fp8kv", kv=codes, kv_scale=scale)
 
 
 def make_tiny(seed=0, device="cpu", L=256, topk=32) -> Workload:

@@ -43,8 +43,8 @@ def _ix(dtype=api.DSA_FP8_E4M3, heads=64, dim=128, scales=True, addr=0x10000):
     return api.IndexerInputs(dtype, heads, dim, addr, s, addr, addr, s)
 
 
-def _at(dtype=api.DSA_BF16, heads=128, d_qk=576, d_v=512, addr=0x10000):
-    return api.AttnInputs(dtype, heads, d_qk, d_v, addr, addr, 0.04)
+def _at(dtype=api.DSA_BF16, heads=128, d_qk=576, d_v=512, addr=0x10000, kv_scale=None):
+    return api.AttnInputs(dtype, heads, d_qk, d_v, addr, addr, 0.04, kv_scale)
 
 
 def test_workspace_size_validation():
@@ -78,6 +78,11 @@ def test_host_validation_rejects_before_launch():
     assert f(*args(ix=_ix(addr=0x10004))) == api.DSA_ERR_INVALID_ARG           # misaligned operand
     assert f(*args(ix=_ix(dtype=api.DSA_BF16))) == api.DSA_ERR_UNSUPPORTED
     assert f(*args(at=_at(heads=64))) == api.DSA_ERR_UNSUPPORTED
+    # FP8 latent cache: the per-row scales are required, 4-byte aligned, and only with that dtype
+    assert f(*args(at=_at(dtype=api.DSA_FP8_E4M3))) == api.DSA_ERR_INVALID_ARG
+    assert f(*args(at=_at(dtype=api.DSA_FP8_E4M3, kv_scale=0x10002))) == api.DSA_ERR_INVALID_ARG
+    assert f(*args(at=_at(kv_scale=0x10000))) == api.DSA_ERR_INVALID_ARG
+    assert f(*args(at=_at(dtype=api.DSA_FP8_E4M3, kv_scale=0x10000, d_v=256))) == api.DSA_ERR_UNSUPPORTED
     assert f(*args(ws=None)) == api.DSA_ERR_WORKSPACE
     assert f(*args(ws=0x10010)) == api.DSA_ERR_WORKSPACE                      # not 256-byte aligned
     assert f(*args(wsb=1024)) == api.DSA_ERR_WORKSPACE

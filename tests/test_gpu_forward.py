@@ -61,6 +61,24 @@ def test_forward_other_k(k):
     _check_rows(wl, idx, out, lse, _sample(wl.num_q, 12, [k - 2, k - 1, k, wl.num_q - 1]), ATTN_ATOL_BF16)
 
 
+@pytest.mark.parametrize("kind", ["decode", "prefill"])
+def test_forward_fp8_kv_cache(kind):
+    """The FP8 latent cache through the fused forward: the decode batch at full
+    size (64 x 65536) and a 4096-token prefill, sampled rows vs the oracle."""
+    torch.cuda.empty_cache()
+    if kind == "decode":
+        wl = inputs.with_fp8_kv(inputs.make_decode(seed=2, device=DEV))
+        rows = _sample(wl.num_q, 8, [wl.num_q - 1])
+    else:
+        wl = inputs.with_fp8_kv(inputs.make_prefill(seed=2, device=DEV, L=4096))
+        rows = _sample(wl.num_q, 10, [2047, 2048, 4095])
+    idx, out, lse = run_forward(api.Problem(wl))
+    assert api.dsa_check_device_error() == api.DSA_OK
+    _check_rows(wl, idx, out, lse, rows, ATTN_ATOL_BF16)
+    del wl, idx, out, lse
+    torch.cuda.empty_cache()
+
+
 def test_forward_128k_context():
     """A 131072-token prefill context (the long-context end of the sweep):
     the last 4096 queries, one bench-sized call, sampled rows vs the oracle."""

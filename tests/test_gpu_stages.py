@@ -2,6 +2,8 @@
 oracle, on identical seeded inputs.  Needs a B300 and the built library."""
 import math
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -177,7 +179,7 @@ def _attn(prob, idx_cpu, k):
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
-@pytest.mark.parametrize("case", ["tiny", "bf16_k2048", "bf16_k100", "paged"])
+@pytest.mark.parametrize("case", ["tiny", "bf16_k2048", "bf16_k100", "paged", "fp8kv_k2048", "fp8kv_paged"])
 def test_sparse_attn_matches_oracle(case):
     if case == "tiny":
         wl, k, atol = inputs.make_tiny(seed=4, device=DEV), 32, ATTN_ATOL_F32
@@ -185,9 +187,13 @@ def test_sparse_attn_matches_oracle(case):
         wl, k, atol = inputs.make_prefill(seed=5, device=DEV, L=2600), 2048, ATTN_ATOL_BF16
     elif case == "bf16_k100":
         wl, k, atol = inputs.make_prefill(seed=6, device=DEV, L=700, topk=100), 100, ATTN_ATOL_BF16
+    elif case == "fp8kv_k2048":
+        wl, k, atol = inputs.with_fp8_kv(inputs.make_prefill(seed=12, device=DEV, L=2600)), 2048, ATTN_ATOL_BF16
     else:
         wl = inputs.make_mixed(seed=7, device=DEV, batch=2, lo=2100, hi=2500, prefill=60, decode=3, block=64)
         k, atol = 2048, ATTN_ATOL_BF16
+        if case == "fp8kv_paged":
+            wl = inputs.with_fp8_kv(wl)
     prob = api.Problem(wl)
     sel = inputs.random_index_sets(wl.q_pos, k, seed=11)
     o, lse = _attn(prob, sel, k)
@@ -198,6 +204,20 @@ def test_sparse_attn_matches_oracle(case):
         err = np.abs(o[i] - ro).max()
         assert err <= atol, f"query {i}: max |O - O_ref| = {err}"
         assert np.abs(lse[i] - rl).max() <= 1e-3 * max(1.0, np.abs(rl).max()), i
+
+
+def test_fp8_kv_attention_equals_bf16_attention_on_the_dequantised_cache():
+    """The FP8 gather writes the same bf16 tiles as the bf16 path would for
+    the cache bf16(scale * code): outputs and LSE agree bit for bit.  The
+    dequantised cache here is torch's float8 decode, a float32 multiply and
+    its bfloat16 cast."""
+    w8 = inputs.with_fp8_kv(inputs.make_prefill(seed=13, device=DEV, L=2200))
+    deq = (w8.kv.view(torch.float8_e4m3fn).float() * w8.kv_scale[:, None]).to(torch.bfloat16)
+    wb = dataclasses.replace(w8, attn_dtype="bf16", kv=deq, kv_scale=None)
+    sel = inputs.random_index_sets(w8.q_pos, 2048, seed=2)
+    o8, l8 = _attn(api.Problem(w8), sel, 2048)
+    ob, lb = _attn(api.Problem(wb), sel, 2048)
+    assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
 
 
 def test_sparse_attn_skips_padding_and_any_order():
