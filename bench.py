@@ -271,9 +271,10 @@ def _roofline_decode(wl, per_stage, steps, peaks):
 
 def _time_append(wl, r: Runner, steps: int, warmup: int):
     """The decode loop's cache write: one new token per sequence (bf16 key of
-    width 128 encoded to e4m3 + scale, and its 576-wide bf16 latent row),
-    written at each sequence's last position.  Timed with CUDA events after
-    the decode steps (it rewrites those rows)."""
+    width 128 encoded to e4m3 + scale, and its 576-wide bf16 latent row,
+    copied, or encoded to e4m3 + scale for an FP8 latent cache), written at
+    each sequence's last position.  Timed with CUDA events after the decode
+    steps (it rewrites those rows)."""
     dev = wl.q.device
     n = wl.num_seqs
     k_new = inputs.randn((n, 128), 1, "append_k", dev).to(torch.bfloat16)
@@ -283,24 +284,30 @@ def _time_append(wl, r: Runner, steps: int, warmup: int):
     cache = r.prob.cache.desc()
 
     def one():
-        api.dsa_cache_append(cache, seq, pos, k_new, wl.k_idx, wl.k_scale, kv_new, wl.kv)
+        api.dsa_cache_append(cache, seq, pos, k_new, wl.k_idx, wl.k_scale, kv_new, wl.kv, kv_scale=wl.kv_scale)
 
     for _ in range(warmup):
         one()
     torch.cuda.synchronize()
+    api.dsa_profile_start(steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(steps):
         one()
     e1.record()
     torch.cuda.synchronize()
+    api.dsa_profile_stop()
+    recs = api.dsa_profile_read(steps)
     st = api.dsa_check_device_error()
     if st != api.DSA_OK:
         raise RuntimeError(f"device error during cache append: {api.status_string(st)}")
-    ms = e0.elapsed_time(e1) / steps
-    byts = n * ((128 * 2 + 576 * 2) + (128 + 4 + 576 * 2))   # read new rows, write cache rows
-    return {"tokens": n, "ms": ms, "bytes": byts, "achieved_gbs": byts / (ms / 1e3) / 1e9,
-            "note": "latency-bound: one 128-thread block per 4 tokens"}
+    loop_ms = e0.elapsed_time(e1) / steps          # includes the host call between launches
+    ms = sum(t for _, t in recs) / max(1, len(recs))   # the kernel alone, from the launch events
+    kv_row = 576 + 4 if wl.kv_scale is not None else 576 * 2
+    byts = n * ((128 * 2 + 576 * 2) + (128 + 4 + kv_row))   # read new rows, write cache rows
+    return {"tokens": n, "ms": ms, "loop_ms_per_call": loop_ms, "bytes": byts,
+            "achieved_gbs": byts / (ms / 1e3) / 1e9,
+            "note": "latency-bound: one 128-thread block per 4 tokens; ms from the launch's own events"}
 
 
 def _e2e(wl, steps: int):
@@ -517,6 +524,7 @@ def main():
             decode["fp8_kv"] = {"value": v8, "unit": "tokens/s", "ms_per_step": ms8,
                                 "stages": {n: round(v[1] / max(args.steps, 10), 4) for n, v in st8.items()},
                                 "attention_gather_gbs": n_attn * BYTES_PER_ATTN_KEY_FP8 / (a_ms / 1e3) / 1e9}
+            decode["fp8_kv"]["cache_append"] = _time_append(w8, r8, max(args.steps, 10), args.warmup)
             del r8, w8
         del wd
         torch.cuda.empty_cache()

@@ -252,8 +252,12 @@ DSA_API const char* dsa_status_string(dsa_status status);
  *   k_cache   [num_rows, 128] uint8 e4m3 key cache (16-byte aligned)
  *   k_scale   [num_rows] fp32 per-row scales
  *   kv_new    [num_tok, d_qk] bf16 new latent rows, or NULL (then kv_cache
- *             must be NULL too and only the keys are written)
- *   kv_cache  [num_rows, d_qk] bf16 latent cache; d_qk * 2 a multiple of 16
+ *             and kv_scale must be NULL too and only the keys are written)
+ *   kv_cache  [num_rows, d_qk] latent cache: bf16 (rows copied; d_qk * 2 a
+ *             multiple of 16) when kv_scale is NULL, else the FP8 latent
+ *             cache of dsa_attn_inputs' DSA_FP8_E4M3: uint8 e4m3 codes, each
+ *             row encoded like the keys (d_qk a multiple of 16, <= 4096)
+ *   kv_scale  [num_rows] fp32 per-row scales of the FP8 latent cache, or NULL
  *
  * Rows of tokens whose position lies outside the descriptor are skipped and
  * DSA_ERR_BOUNDS is recorded for dsa_check_device_error().  Two tokens that
@@ -262,7 +266,7 @@ DSA_API const char* dsa_status_string(dsa_status status);
 DSA_API dsa_status dsa_cache_append(const dsa_cache_desc* cache, int32_t num_tok, const int32_t* tok_seq,
                                     const int32_t* tok_pos, dsa_dtype k_dtype, const void* k_new, int32_t dim,
                                     uint8_t* k_cache, float* k_scale, const void* kv_new, int32_t d_qk,
-                                    void* kv_cache, dsa_stream_t stream);
+                                    void* kv_cache, float* kv_scale, dsa_stream_t stream);
 
 /* ---- Measurement aids (host-side state; not thread-safe) ----------------
  * While a profile is open, every kernel the library launches is bracketed by

@@ -70,7 +70,7 @@ _SIGS = {
     "dsa_cache_append": (ctypes.c_int, [_P(CacheDesc), ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
-                                        ctypes.c_void_p]),
+                                        ctypes.c_void_p, ctypes.c_void_p]),
     "dsa_check_device_error": (ctypes.c_int, [ctypes.c_void_p]),
     "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dsa_last_error_detail": (ctypes.c_char_p, []),
@@ -198,9 +198,12 @@ NOALLOC_MAX_KV = 2097152
 
 def dsa_cache_append(cache: CacheDesc, tok_seq: torch.Tensor, tok_pos: torch.Tensor, k_new: torch.Tensor,
                      k_cache: torch.Tensor, k_scale: torch.Tensor, kv_new: Optional[torch.Tensor] = None,
-                     kv_cache: Optional[torch.Tensor] = None, stream=None) -> None:
+                     kv_cache: Optional[torch.Tensor] = None, stream=None,
+                     kv_scale: Optional[torch.Tensor] = None) -> None:
     """Writes new tokens into the caches: key rows (bf16 or fp32, width 128)
-    encoded as e4m3 codes with a per-row scale, and optionally latent rows."""
+    encoded as e4m3 codes with a per-row scale, and optionally latent rows
+    (copied into a bf16 cache, or encoded the same way into an FP8 cache
+    when kv_scale is given)."""
     if k_new.dtype == torch.bfloat16:
         kdt = DSA_BF16
     elif k_new.dtype == torch.float32:
@@ -211,7 +214,8 @@ def dsa_cache_append(cache: CacheDesc, tok_seq: torch.Tensor, tok_pos: torch.Ten
     _check(lib().dsa_cache_append(ctypes.byref(cache), int(tok_seq.numel()), _ptr(tok_seq), _ptr(tok_pos), kdt,
                                   _ptr(k_new), int(k_new.shape[-1]), _ptr(k_cache), _ptr(k_scale),
                                   None if kv_new is None else _ptr(kv_new), d_qk,
-                                  None if kv_cache is None else _ptr(kv_cache), _stream(stream)),
+                                  None if kv_cache is None else _ptr(kv_cache),
+                                  None if kv_scale is None else _ptr(kv_scale), _stream(stream)),
            "dsa_cache_append")
 
 

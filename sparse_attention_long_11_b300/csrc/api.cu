@@ -266,7 +266,7 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const
 
 dsa_status dsa_cache_append(const dsa_cache_desc* cd, int32_t num_tok, const int32_t* tok_seq, const int32_t* tok_pos,
                             dsa_dtype k_dtype, const void* k_new, int32_t dim, uint8_t* k_cache, float* k_scale,
-                            const void* kv_new, int32_t d_qk, void* kv_cache, dsa_stream_t stream) {
+                            const void* kv_new, int32_t d_qk, void* kv_cache, float* kv_scale, dsa_stream_t stream) {
   if (num_tok < 0) return DSA_ERR_INVALID_ARG;
   if (num_tok == 0) return DSA_OK;
   DSA_TRY(check_cache(cd, 1));
@@ -276,16 +276,19 @@ dsa_status dsa_cache_append(const dsa_cache_desc* cd, int32_t num_tok, const int
   if (!k_new || !k_cache || !k_scale || !aligned(k_new, 16) || !aligned(k_cache, 16) || !aligned(k_scale, 4))
     return DSA_ERR_INVALID_ARG;
   if ((kv_new == nullptr) != (kv_cache == nullptr)) return DSA_ERR_INVALID_ARG;
+  if (kv_scale && !kv_new) return DSA_ERR_INVALID_ARG;
   if (kv_new) {
     if (!aligned(kv_new, 16) || !aligned(kv_cache, 16)) return DSA_ERR_INVALID_ARG;
+    if (kv_scale && !aligned(kv_scale, 4)) return DSA_ERR_INVALID_ARG;
     if (d_qk < 8 || d_qk > 4096 || (d_qk * 2) % 16) return DSA_ERR_UNSUPPORTED;
+    if (kv_scale && d_qk % 16) return DSA_ERR_UNSUPPORTED;   // FP8 rows of whole 16-byte chunks
   }
   int* err = device_error_ptr();
   if (!err) return DSA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return cuda_status(launch(DSA_STAGE_APPEND, st, [&] {
     return launch_cache_append(to_map(cd), num_tok, tok_seq, tok_pos, k_dtype == DSA_BF16, k_new, k_cache, k_scale,
-                               kv_new, kv_cache, kv_new ? d_qk * 2 : 0, err, st);
+                               kv_new, kv_cache, kv_scale, kv_new ? d_qk : 0, err, st);
   }));
 }
 

@@ -51,9 +51,11 @@ inline cudaError_t launch_attn(const QueryBatch& qb, const CacheMap& cm, const d
 
 // Appends new tokens to the caches: each key row (128 bf16 or fp32 values)
 // encoded as e4m3 codes with scale amax/448, and (when kv_new is non-null)
-// the latent row copied.  One warp per token.
+// the latent row of d_qk bf16 values copied, or, with kv_scale, encoded the
+// same way into an FP8 latent cache.  One warp per token.
 cudaError_t launch_cache_append(const CacheMap& cm, int num_tok, const int32_t* tok_seq, const int32_t* tok_pos,
                                 bool k_is_bf16, const void* k_new, uint8_t* k_cache, float* k_scale,
-                                const void* kv_new, void* kv_cache, int kv_row_bytes, int* err, cudaStream_t stream);
+                                const void* kv_new, void* kv_cache, float* kv_scale, int d_qk, int* err,
+                                cudaStream_t stream);
 
 }  // namespace dsa

@@ -105,8 +105,8 @@ def test_cache_append_validation_rejects_before_launch():
     L = api.lib()
     cd = api.CacheDesc(1, 4096, 4096, None, 0, 0)
     A = 0x10000
-    f = lambda n=4, kdt=api.DSA_BF16, kn=A, dim=128, kc=A, ks=A, kvn=A, dqk=576, kvc=A, c=cd: L.dsa_cache_append(
-        ctypes.byref(c), n, A, A, kdt, kn, dim, kc, ks, kvn, dqk, kvc, None)
+    f = lambda n=4, kdt=api.DSA_BF16, kn=A, dim=128, kc=A, ks=A, kvn=A, dqk=576, kvc=A, kvs=None, c=cd: \
+        L.dsa_cache_append(ctypes.byref(c), n, A, A, kdt, kn, dim, kc, ks, kvn, dqk, kvc, kvs, None)
     assert f(n=0) == api.DSA_OK                                   # nothing to append: no launch
     assert f(n=-1) == api.DSA_ERR_INVALID_ARG
     assert f(dim=64) == api.DSA_ERR_UNSUPPORTED
@@ -116,6 +116,10 @@ def test_cache_append_validation_rejects_before_launch():
     assert f(kvc=None) == api.DSA_ERR_INVALID_ARG                 # latent rows without a latent cache
     assert f(dqk=100) == api.DSA_ERR_UNSUPPORTED                  # 200-byte rows: not a 16-byte multiple
     assert f(c=api.CacheDesc(1, 4096, 0, A, 64, 0)) == api.DSA_ERR_INVALID_ARG   # empty block table
+    # FP8 latent cache: scales only with latent rows, 4-byte aligned, rows of whole 16-byte chunks
+    assert f(kvn=None, kvc=None, kvs=A) == api.DSA_ERR_INVALID_ARG
+    assert f(kvs=A + 2) == api.DSA_ERR_INVALID_ARG
+    assert f(kvs=A, dqk=72) == api.DSA_ERR_UNSUPPORTED
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

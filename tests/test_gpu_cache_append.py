@@ -83,6 +83,38 @@ def test_cache_append_flags_and_skips_out_of_range_tokens():
     assert int((ks != 0).sum()) == 2                               # nothing else was written
 
 
+def test_cache_append_fp8_latent_rows_match_oracle():
+    """Latent rows into an FP8 cache: each row encoded like a key (oracle
+    quantize_e4m3_rows on the bf16 values), codes and scales bit for bit, and
+    the whole cache equal to the generator's FP8 latent cache."""
+    cache, perm, rows, block = _paged_cache(seed=6)
+    wl_rows = rows
+    kv_new = inputs.randn((wl_rows, 576), 14, "append_kv8", DEV).to(torch.bfloat16)
+    kv_new[3] = 0.0                                                # all-zero row: scale 1
+    kv_new[5, 100] = 5e3                                           # an outlier row
+    # every logical position of the three sequences, so the whole cache is written
+    seq = torch.arange(3, dtype=torch.int32).repeat_interleave(5 * block)
+    pos = torch.arange(5 * block, dtype=torch.int32).repeat(3)
+    k_new = inputs.randn((wl_rows, 128), 15, "append_k8", DEV)
+    k_cache = torch.empty((rows, 128), dtype=torch.uint8, device=DEV)
+    k_scale = torch.empty((rows,), dtype=torch.float32, device=DEV)
+    kv_cache = torch.full((rows, 576), 0x5A, dtype=torch.uint8, device=DEV)
+    kv_scale = torch.full((rows,), -7.0, dtype=torch.float32, device=DEV)
+    api.dsa_cache_append(cache.desc(), seq.to(DEV), pos.to(DEV), k_new, k_cache, k_scale, kv_new, kv_cache,
+                         kv_scale=kv_scale)
+    assert api.dsa_check_device_error() == api.DSA_OK
+    phys = (perm[seq.long(), (pos // block).long()].to(torch.int64) * block + (pos % block)).numpy()
+    codes, scale = O.quantize_e4m3_rows(kv_new.float().cpu().numpy())
+    kvc, kvs = kv_cache.cpu().numpy(), kv_scale.cpu().numpy()
+    assert np.array_equal(kvc[phys], codes)
+    assert np.array_equal(kvs[phys].view(np.uint32), scale.view(np.uint32))
+    assert scale[3] == 1.0 and np.all(codes[3] == 0)
+    # the generator's encoding of the same rows (in physical order)
+    order = torch.from_numpy(np.argsort(phys))
+    c8, s8 = inputs.quantize_fp8_rows(kv_new[order.to(DEV)].float())
+    assert torch.equal(kv_cache, c8) and torch.equal(kv_scale, s8)
+
+
 def test_cache_append_rebuilds_the_generated_fp8_key_cache():
     """Appending the raw keys of a workload reproduces the FP8 key cache the
     generator built for it (same encoding, so the forward's inputs and a
