@@ -29,7 +29,9 @@ fp32 vectors and no scales), keys s <= t (causal, inclusive);
 top-k = the min(k, t+1) largest I[t,s], ties to the lower s, returned in
 ascending s and padded with -1; attention
     O[t,h,:] = sum_{s in sel} softmax_s(tau * <q[t,h,:], kv[s,:]>) * kv[s,:d_v]
-plus LSE[t,h] = log sum_s exp(tau * <q, kv_s>) (natural log).
+plus LSE[t,h] = log sum_s exp(tau * <q, kv_s>) (natural log).  For training,
+the indexer's alignment loss KL(p || softmax(I)) over a query's candidate
+set and its gradients (indexer_kl_backward).
 
 Everything is computed in float64 from exactly decoded inputs, except the
 key-cache encoding (quantize_e4m3_rows): the FP8 keys of the summary card's
@@ -244,3 +246,87 @@ def dsa_query(q_idx_vals, q_scale, w, k_vals, k_scale, pos, topk, q_attn, kv_val
     sel = idx[idx >= 0]
     o, lse = sparse_attention(q_attn, kv_vals[sel], scale, d_v)
     return sc, idx, o, lse
+
+
+# ---------------------------------------------------------------------------
+# Indexer training: the alignment (KL) loss and its gradients
+# ---------------------------------------------------------------------------
+
+
+def indexer_kl_loss(q, w, k_sel, p) -> float:
+    """KL(p || softmax(I)) for ONE query over its candidate set, straight from
+    the definitions (used to pin the gradients by finite differences).
+    q [H, d] and k_sel [n, d] dequantised values, w [H], p [n] (sums to 1)."""
+    x = np.asarray(q, dtype=np.float64) @ np.asarray(k_sel, dtype=np.float64).T     # [H, n]
+    I = np.asarray(w, dtype=np.float64) @ np.maximum(x, 0.0)                       # [n]
+    log_pi = I - I.max() - np.log(np.exp(I - I.max()).sum())
+    p = np.asarray(p, dtype=np.float64)
+    nz = p > 0
+    return float((p[nz] * (np.log(p[nz]) - log_pi[nz])).sum())
+
+
+def indexer_kl_backward(q_vals, w, k_rows, sel, p, q_scale=None, k_scale=None) -> dict:
+    """Indexer alignment loss of ONE query and its gradients.
+
+    The news article's continued-pre-training section: the indexer is trained
+    with a Kullback-Leibler loss to match the main attention's distribution --
+    over all keys in the dense warm-up, over the selected set only in the
+    sparse phase, where the indexer's gradients come from that loss alone.
+    With the candidate set S (the valid entries of sel), a target
+    distribution p over S, the dequantised operands q_j = sq_j * q_vals[j]
+    and k_s = sk_s * k_rows[s], and x_js = <q_j, k_s>:
+        I_s  = sum_j w_j ReLU(x_js)
+        pi   = softmax over S of I
+        loss = sum_{s in S} p_s (log p_s - log pi_s)            (0 log 0 = 0)
+        g_s  = d loss / d I_s = pi_s - p_s
+        dw_j = sum_s g_s ReLU(x_js)
+        dq_j = sum_s g_s w_j [x_js > 0] k_s
+        dk_s = g_s sum_j w_j [x_js > 0] q_j
+    (ReLU'(0) = 0).  The gradients are with respect to the dequantised q, w
+    and k.
+
+    q_vals [H, d], w [H], k_rows [n, d] (logical rows 0..n-1 of the
+    sequence), sel [k] positions with -1 padding, p [k] aligned with sel
+    (ignored where sel = -1); q_scale [H] and k_scale [n] or None.  Returns a
+    dict with loss, g [k], dw [H], dq [H, d], dk [k, d] (row r belongs to
+    sel[r]; zero at padding) and mag_dw, mag_dq, mag_dk: the same sums taken
+    over absolute values with |g_s| widened by 1e-4 (pi_s + p_s), the scale of
+    the rounding a float32 evaluation of g can carry."""
+    q = np.asarray(q_vals, dtype=np.float64)
+    if q_scale is not None:
+        q = q * np.asarray(q_scale, dtype=np.float64)[:, None]
+    w = np.asarray(w, dtype=np.float64)
+    sel = np.asarray(sel)
+    valid = sel >= 0
+    k_all = np.asarray(k_rows, dtype=np.float64)
+    ks = k_all[sel[valid]]
+    if k_scale is not None:
+        ks = ks * np.asarray(k_scale, dtype=np.float64)[sel[valid]][:, None]
+    pv = np.asarray(p, dtype=np.float64)[valid]
+    H, d = q.shape
+    kk = sel.shape[0]
+    out = {"g": np.zeros(kk), "dk": np.zeros((kk, d)), "mag_dk": np.zeros((kk, d))}
+    if ks.shape[0] == 0:
+        out.update(loss=0.0, dw=np.zeros(H), dq=np.zeros((H, d)), mag_dw=np.zeros(H), mag_dq=np.zeros((H, d)))
+        return out
+    x = q @ ks.T                                  # [H, n]
+    r = np.maximum(x, 0.0)
+    m = (x > 0).astype(np.float64)
+    I = w @ r
+    e = np.exp(I - I.max())
+    pi = e / e.sum()
+    log_pi = I - I.max() - np.log(e.sum())
+    nz = pv > 0
+    loss = float((pv[nz] * (np.log(pv[nz]) - log_pi[nz])).sum())
+    g = pi - pv
+    ga = np.abs(g) + 1e-4 * (pi + pv)
+    wm = w[:, None] * m                           # [H, n]
+    out["loss"] = loss
+    out["g"][valid] = g
+    out["dw"] = r @ g
+    out["mag_dw"] = r @ ga
+    out["dq"] = (wm * g[None, :]) @ ks
+    out["mag_dq"] = (np.abs(wm) * ga[None, :]) @ np.abs(ks)
+    out["dk"][valid] = g[:, None] * (wm.T @ q)
+    out["mag_dk"][valid] = ga[:, None] * (np.abs(wm).T @ np.abs(q))
+    return out

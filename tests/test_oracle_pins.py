@@ -328,3 +328,92 @@ def test_paged_view_reads_logical_rows():
     rows = torch.cat([wl.logical_rows(b, c) for b, c in enumerate(wl.seq_lens)])
     assert rows.unique().numel() == rows.numel()            # no two logical rows share storage
     assert int(rows.max()) < wl.num_rows
+
+
+# --------------------------------------------------------------------------- indexer training (KL alignment)
+
+def _kl_case(seed, H=6, d=16, n=40, kk=24, fp8=False):
+    rng = np.random.default_rng(seed)
+    if fp8:
+        q, qs = O.quantize_e4m3_rows(rng.standard_normal((H, d)).astype(np.float32))
+        kr, ks = O.quantize_e4m3_rows(rng.standard_normal((n, d)).astype(np.float32))
+        q, kr = O.decode_e4m3(q), O.decode_e4m3(kr)
+    else:
+        q, qs, kr, ks = rng.standard_normal((H, d)), None, rng.standard_normal((n, d)), None
+    w = rng.standard_normal(H)
+    sel = np.sort(rng.choice(n, kk - 3, replace=False))
+    sel = np.concatenate([sel, [-1, -1, -1]])
+    p = rng.random(kk) ** 3
+    p[sel < 0] = 0
+    p /= p.sum()
+    return q, qs, w, kr, ks, sel, p
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_indexer_kl_backward_matches_autograd(fp8):
+    q, qs, w, kr, ks, sel, p = _kl_case(1 + fp8, fp8=fp8)
+    r = O.indexer_kl_backward(q, w, kr, sel, p, qs, ks)
+    qd = q * (qs[:, None] if qs is not None else 1.0)
+    kd = kr * (ks[:, None] if ks is not None else 1.0)
+    qt = torch.tensor(qd, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    kt = torch.tensor(kd, requires_grad=True)
+    v = sel >= 0
+    x = qt @ kt[torch.tensor(sel[v])].T
+    lp = torch.log_softmax(wt @ torch.relu(x), 0)
+    pt = torch.tensor(p[v])
+    loss = (pt * (torch.log(pt) - lp)).sum()
+    loss.backward()
+    assert abs(loss.item() - r["loss"]) < 1e-12
+    np.testing.assert_allclose(r["dw"], wt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(r["dq"], qt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    dk = np.zeros_like(kd)
+    for row, s in enumerate(sel):
+        if s >= 0:
+            dk[s] += r["dk"][row]
+    np.testing.assert_allclose(dk, kt.grad.numpy(), rtol=1e-10, atol=1e-13)
+    assert np.all(r["dk"][~v] == 0) and np.all(r["g"][~v] == 0)
+
+
+def test_indexer_kl_loss_and_finite_differences():
+    q, _, w, kr, _, sel, p = _kl_case(3)
+    v = sel >= 0
+    r = O.indexer_kl_backward(q, w, kr, sel, p)
+    assert abs(O.indexer_kl_loss(q, w, kr[sel[v]], p[v]) - r["loss"]) < 1e-12
+    h = 1e-6
+    for j in range(len(w)):
+        wp, wm = w.copy(), w.copy()
+        wp[j] += h
+        wm[j] -= h
+        fd = (O.indexer_kl_loss(q, wp, kr[sel[v]], p[v]) - O.indexer_kl_loss(q, wm, kr[sel[v]], p[v])) / (2 * h)
+        assert abs(fd - r["dw"][j]) < 1e-6 * max(1.0, abs(fd))
+    for (j, c) in [(0, 3), (2, 7), (5, 15)]:
+        qp, qm = q.copy(), q.copy()
+        qp[j, c] += h
+        qm[j, c] -= h
+        fd = (O.indexer_kl_loss(qp, w, kr[sel[v]], p[v]) - O.indexer_kl_loss(qm, w, kr[sel[v]], p[v])) / (2 * h)
+        assert abs(fd - r["dq"][j, c]) < 1e-6 * max(1.0, abs(fd))
+
+
+def test_indexer_kl_special_cases():
+    q, _, w, kr, _, sel, p = _kl_case(4)
+    v = sel >= 0
+    # p = softmax(I): zero loss and zero gradients
+    I = w @ np.maximum(q @ kr[sel[v]].T, 0)
+    pi = np.zeros(len(sel))
+    pi[v] = np.exp(I - I.max()) / np.exp(I - I.max()).sum()
+    r = O.indexer_kl_backward(q, w, kr, sel, pi)
+    assert abs(r["loss"]) < 1e-12 and np.abs(r["dw"]).max() < 1e-12 and np.abs(r["dq"]).max() < 1e-12
+    # one candidate: pi = p = 1
+    one = np.array([5, -1, -1])
+    r = O.indexer_kl_backward(q, w, kr, one, np.array([1.0, 0, 0]))
+    assert r["loss"] == 0 and np.all(r["dw"] == 0) and np.all(r["dq"] == 0) and np.all(r["dk"] == 0)
+    # w = 0: pi uniform, no gradient reaches q or k, dw_j = sum (1/n - p_s) ReLU(x_js)
+    r = O.indexer_kl_backward(q, np.zeros_like(w), kr, sel, p)
+    n = int(v.sum())
+    assert np.all(r["dq"] == 0) and np.all(r["dk"] == 0)
+    np.testing.assert_allclose(r["dw"], np.maximum(q @ kr[sel[v]].T, 0) @ (1.0 / n - p[v]), rtol=1e-12)
+    # KL >= 0
+    for s in range(5):
+        qq, _, ww, kk_, _, ss, pp = _kl_case(10 + s)
+        assert O.indexer_kl_backward(qq, ww, kk_, ss, pp)["loss"] >= 0
