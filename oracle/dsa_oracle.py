@@ -292,16 +292,15 @@ def indexer_kl_backward(q_vals, w, k_rows, sel, p, q_scale=None, k_scale=None) -
     sel[r]; zero at padding) and mag_dw, mag_dq, mag_dk: the same sums taken
     over absolute values with |g_s| widened by 1e-4 (pi_s + p_s), the scale of
     the rounding a float32 evaluation of g can carry."""
-    q = np.asarray(q_vals, dtype=np.float64)
-    if q_scale is not None:
-        q = q * np.asarray(q_scale, dtype=np.float64)[:, None]
+    q8 = np.asarray(q_vals, dtype=np.float64)
+    sq = np.ones(q8.shape[0]) if q_scale is None else np.asarray(q_scale, dtype=np.float64)
+    q = q8 * sq[:, None]
     w = np.asarray(w, dtype=np.float64)
     sel = np.asarray(sel)
     valid = sel >= 0
-    k_all = np.asarray(k_rows, dtype=np.float64)
-    ks = k_all[sel[valid]]
-    if k_scale is not None:
-        ks = ks * np.asarray(k_scale, dtype=np.float64)[sel[valid]][:, None]
+    k8 = np.asarray(k_rows, dtype=np.float64)[sel[valid]]
+    sk = np.ones(k8.shape[0]) if k_scale is None else np.asarray(k_scale, dtype=np.float64)[sel[valid]]
+    ks = k8 * sk[:, None]
     pv = np.asarray(p, dtype=np.float64)[valid]
     H, d = q.shape
     kk = sel.shape[0]
@@ -309,9 +308,14 @@ def indexer_kl_backward(q_vals, w, k_rows, sel, p, q_scale=None, k_scale=None) -
     if ks.shape[0] == 0:
         out.update(loss=0.0, dw=np.zeros(H), dq=np.zeros((H, d)), mag_dw=np.zeros(H), mag_dq=np.zeros((H, d)))
         return out
-    x = q @ ks.T                                  # [H, n]
+    # the dot of the (decoded) operands first, then the scales, as in
+    # ReLU(sq * sk * <q8, k8>): for e4m3 codes that dot is exact in float64,
+    # so the sign deciding [x > 0] is exact (a dot of the scaled operands
+    # would round, and can turn an exact 0 into +-1e-16)
+    raw = q8 @ k8.T                               # [H, n]
+    x = raw * sq[:, None] * sk[None, :]
     r = np.maximum(x, 0.0)
-    m = (x > 0).astype(np.float64)
+    m = (raw > 0).astype(np.float64)
     I = w @ r
     e = np.exp(I - I.max())
     pi = e / e.sum()

@@ -413,6 +413,11 @@ def test_indexer_kl_special_cases():
     n = int(v.sum())
     assert np.all(r["dq"] == 0) and np.all(r["dk"] == 0)
     np.testing.assert_allclose(r["dw"], np.maximum(q @ kr[sel[v]].T, 0) @ (1.0 / n - p[v]), rtol=1e-12)
+    # an exactly-zero code dot is not a positive one, whatever the scales (ReLU'(0) = 0)
+    qz, kz = np.array([[1.0, 1.0, 0.0]]), np.array([[1.0, -1.0, 0.5], [1.0, 1.0, 0.0]])
+    r = O.indexer_kl_backward(qz, np.array([1.0]), kz, np.array([0, 1]), np.array([0.5, 0.5]),
+                              np.array([0.37]), np.array([0.11, 0.13]))
+    assert np.all(r["dk"][0] == 0) and np.all(r["dk"][1] != 0)
     # KL >= 0
     for s in range(5):
         qq, _, ww, kk_, _, ss, pp = _kl_case(10 + s)
