@@ -417,7 +417,7 @@ def test_indexer_kl_special_cases():
     qz, kz = np.array([[1.0, 1.0, 0.0]]), np.array([[1.0, -1.0, 0.5], [1.0, 1.0, 0.0]])
     r = O.indexer_kl_backward(qz, np.array([1.0]), kz, np.array([0, 1]), np.array([0.5, 0.5]),
                               np.array([0.37]), np.array([0.11, 0.13]))
-    assert np.all(r["dk"][0] == 0) and np.all(r["dk"][1] != 0)
+    assert np.all(r["dk"][0] == 0) and np.any(r["dk"][1] != 0)
     # KL >= 0
     for s in range(5):
         qq, _, ww, kk_, _, ss, pp = _kl_case(10 + s)
