@@ -310,6 +310,53 @@ def _time_append(wl, r: Runner, steps: int, warmup: int):
             "note": "latency-bound: one 128-thread block per 4 tokens; ms from the launch's own events"}
 
 
+FP32_FMA_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12   # CUDA-core fp32: SMs x FMA lanes x 2 x max SM clock
+
+
+def _time_kl_backward(r: Runner, steps: int, warmup: int):
+    """The indexer's training step (alignment loss + gradients) over the last
+    4096-query call of the prefill, on the entries the forward selected and
+    seeded synthetic targets.  One launch per step, timed with CUDA events."""
+    wl = r.wl
+    a, b = wl.chunks[-1]
+    qd, ix, _ = r.prob.rows(a, b)
+    idx = r.idx[a:b]
+    k = wl.topk
+    p = inputs.kl_targets(idx, seed=1)
+    n = b - a
+    loss = torch.empty(n, dtype=torch.float32, device=idx.device)
+    g = torch.empty((n, k), dtype=torch.float32, device=idx.device)
+    dw = torch.empty((n, wl.H_I), dtype=torch.float32, device=idx.device)
+    dq = torch.empty((n, wl.H_I, wl.d_I), dtype=torch.float32, device=idx.device)
+    dk = torch.zeros((wl.num_rows, wl.d_I), dtype=torch.float32, device=idx.device)
+    cache = r.prob.cache.desc()
+
+    def one():
+        api.dsa_indexer_kl_backward(qd, cache, ix, idx, k, p, loss, dw, dq, dk, g)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    st = api.dsa_check_device_error()
+    if st != api.DSA_OK:
+        raise RuntimeError(f"device error during the indexer backward: {api.status_string(st)}")
+    ms = e0.elapsed_time(e1) / steps
+    pairs = int((idx >= 0).sum().item())
+    flop = pairs * 3 * 2 * wl.H_I * wl.d_I          # head dots, dq, dk: one 64 x 128 contraction each
+    tf = flop / (ms / 1e3) / 1e12
+    return {"workload": f"queries {a}..{b - 1} of the L={wl.max_kv} prefill, k={k}, synthetic targets",
+            "value": n / (ms / 1e3), "unit": "tokens/s", "ms": ms, "pairs": pairs,
+            "roofline": {"bound": "alu", "achieved": tf, "peak": FP32_FMA_PEAK_TFLOPS, "unit": "TFLOP/s",
+                         "frac": tf / FP32_FMA_PEAK_TFLOPS,
+                         "peak_src": "derived: 148 SMs x 128 fp32 FMA lanes x 2 FLOP x 2032 MHz"}}
+
+
 def _e2e(wl, steps: int):
     """Same metric through the public API with host buffers.  Every step
     copies the step's inputs from pinned host memory, runs dsa_forward chunk
@@ -429,6 +476,7 @@ def main():
     ap.add_argument("--no-k-sweep", action="store_true")
     ap.add_argument("--no-128k", action="store_true")
     ap.add_argument("--no-fp8-kv", action="store_true")
+    ap.add_argument("--no-kl-backward", action="store_true")
     args = ap.parse_args()
     ws, rank, local = _dist()
     if args.impl == "reference":
@@ -446,6 +494,8 @@ def main():
     value, ms = aggregate(wl.num_q, ms, ws)
     roof = _roofline_prefill(wl, per_stage, args.steps, peaks)
     stages = {k: {"launches": v[0], "ms_per_step": v[1] / args.steps} for k, v in per_stage.items()}
+    # the indexer's training step on the selections of the last call (after the timed region)
+    kl_bwd = None if args.no_kl_backward else _time_kl_backward(r, 3, 2)
     del r
     torch.cuda.empty_cache()
     e2e_val, h2d, d2h, e2e_ms = _e2e(wl, args.e2e_steps)
@@ -541,7 +591,7 @@ def main():
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "cpu_baseline": cpu, "decode": decode, "k_sweep": k_sweep,
-                "prefill_128k": long128k, "prefill_fp8_kv": prefill_fp8_kv}
+                "prefill_128k": long128k, "prefill_fp8_kv": prefill_fp8_kv, "indexer_kl_backward": kl_bwd}
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist

@@ -268,13 +268,59 @@ DSA_API dsa_status dsa_cache_append(const dsa_cache_desc* cache, int32_t num_tok
                                     uint8_t* k_cache, float* k_scale, const void* kv_new, int32_t d_qk,
                                     void* kv_cache, float* kv_scale, dsa_stream_t stream);
 
+/*
+ * dsa_indexer_kl_backward -- the indexer's training step: its alignment loss
+ * and the gradients of that loss.  News article on DeepSeek-V3.2,
+ * continued-pre-training section: the indexer is trained with a
+ * Kullback-Leibler loss to match the main attention's distribution -- over
+ * all keys in the dense warm-up, over the selected entries only in the
+ * sparse phase, where that loss is the indexer's only gradient.  The target
+ * distribution is an input here (the pages give no formula for it).
+ *
+ * For query t, its candidate entries are the valid entries e of idx[t]
+ * (0 <= idx[t][e] <= q_pos[t]; -1 = padding, ignored), and p[t][e] is the
+ * target probability of entry e (summing to 1 over the valid entries).  With
+ * the dequantised operands q_j = q_scale[t][j] * q[t][j] and
+ * k_s = k_scale[s] * k[s] (scales 1 for DSA_F32) and x_js = <q_j, k_s>:
+ *   I_e  = sum_j w[t][j] ReLU(x_j,idx[t][e]),   pi = softmax over the entries of I
+ *   loss[t]           = sum_e p_e (log p_e - log pi_e)     (0 log 0 = 0)
+ *   grad_scores[t][e] = pi_e - p_e (0 at padding)           (optional: may be NULL)
+ *   dw[t][j]          = sum_e g_e ReLU(x_je)
+ *   dq[t][j][:]       = w[t][j] sum_e g_e [x_je > 0] k_{idx[t][e]}
+ *   dk[s][:]         += sum over (t, e) with idx[t][e] = s of g_e sum_j w[t][j] [x_je > 0] q_j
+ * ReLU'(0) = 0, and every [x > 0] decision is exact (a dot near zero is
+ * recomputed in fp64).  The dense warm-up is the same call with every
+ * position 0..q_pos[t] as an entry (k >= max_kv).
+ *
+ *   ix        indexer operands as for the forward (FP8 with heads = 64,
+ *             dim = 128, or fp32 with heads <= 64, dim in {32, 64, 128})
+ *   idx, p    [num_q, k] int32 and fp32; 1 <= k <= 8192
+ *   loss      [num_q] fp32; dw [num_q, heads] fp32; dq [num_q, heads, dim]
+ *             fp32 (16-byte aligned)
+ *   dk        [num_rows, dim] fp32 (16-byte aligned), ADDED to: zero it first
+ *             for a fresh gradient.  Additions are atomic, so the bits of dk
+ *             depend on their order; loss, dw and dq do not.
+ *
+ * CUDA cores (one block per query); asynchronous on `stream`.
+ */
+DSA_API dsa_status dsa_indexer_kl_backward(const dsa_query_desc* qd, const dsa_cache_desc* cd,
+                                           const dsa_indexer_inputs* ix, const int32_t* idx, int32_t k,
+                                           const float* p, float* loss, float* grad_scores, float* dw, float* dq,
+                                           float* dk, dsa_stream_t stream);
+
 /* ---- Measurement aids (host-side state; not thread-safe) ----------------
  * While a profile is open, every kernel the library launches is bracketed by
  * a pair of CUDA events recorded on its launch stream, and tagged with its
  * stage.  dsa_profile_read() waits for the recorded events and returns each
  * launch's stage and device duration.  Events are created by the library (no
  * device memory); at most `capacity` launches are recorded. */
-typedef enum { DSA_STAGE_INDEXER = 1, DSA_STAGE_TOPK = 2, DSA_STAGE_ATTN = 3, DSA_STAGE_APPEND = 4 } dsa_stage;
+typedef enum {
+  DSA_STAGE_INDEXER = 1,
+  DSA_STAGE_TOPK = 2,
+  DSA_STAGE_ATTN = 3,
+  DSA_STAGE_APPEND = 4,
+  DSA_STAGE_INDEXER_BWD = 5
+} dsa_stage;
 DSA_API dsa_status dsa_profile_start(int32_t capacity);
 /* Closes the profile; returns the number of launches recorded. */
 DSA_API int32_t dsa_profile_stop(void);

@@ -71,6 +71,9 @@ _SIGS = {
                                         ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p]),
+    "dsa_indexer_kl_backward": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(IndexerInputs), ctypes.c_void_p,
+                                               ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "dsa_check_device_error": (ctypes.c_int, [ctypes.c_void_p]),
     "dsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "dsa_last_error_detail": (ctypes.c_char_p, []),
@@ -80,8 +83,8 @@ _SIGS = {
     "dsa_profile_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p]),
     "dsa_launch_count": (ctypes.c_int64, []),
 }
-DSA_STAGE_INDEXER, DSA_STAGE_TOPK, DSA_STAGE_ATTN, DSA_STAGE_APPEND = 1, 2, 3, 4
-STAGE_NAMES = {1: "indexer", 2: "topk", 3: "attention", 4: "cache_append"}
+DSA_STAGE_INDEXER, DSA_STAGE_TOPK, DSA_STAGE_ATTN, DSA_STAGE_APPEND, DSA_STAGE_INDEXER_BWD = 1, 2, 3, 4, 5
+STAGE_NAMES = {1: "indexer", 2: "topk", 3: "attention", 4: "cache_append", 5: "indexer_bwd"}
 
 _lib = None
 
@@ -217,6 +220,17 @@ def dsa_cache_append(cache: CacheDesc, tok_seq: torch.Tensor, tok_pos: torch.Ten
                                   None if kv_cache is None else _ptr(kv_cache),
                                   None if kv_scale is None else _ptr(kv_scale), _stream(stream)),
            "dsa_cache_append")
+
+
+def dsa_indexer_kl_backward(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, idx: torch.Tensor, k: int,
+                            p: torch.Tensor, loss: torch.Tensor, dw: torch.Tensor, dq: torch.Tensor,
+                            dk: torch.Tensor, grad_scores: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Indexer alignment loss KL(p || softmax(I)) over each query's candidate
+    entries (idx, -1 padded) and its gradients; dk is accumulated into."""
+    _check(lib().dsa_indexer_kl_backward(ctypes.byref(batch), ctypes.byref(cache), ctypes.byref(ix), _ptr(idx), k,
+                                         _ptr(p), _ptr(loss), None if grad_scores is None else _ptr(grad_scores),
+                                         _ptr(dw), _ptr(dq), _ptr(dk), _stream(stream)),
+           "dsa_indexer_kl_backward")
 
 
 def dsa_forward_noalloc(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, k: int, at: AttnInputs,

@@ -145,8 +145,12 @@ cudaError_t launch(int stage, cudaStream_t st, F&& f) {
     cudaEventRecord(g_prof[g_prof_n].a, st);
   }
   cudaError_t e = f();
-  note_cuda_error(e, stage == DSA_STAGE_INDEXER ? "indexer launch" : stage == DSA_STAGE_TOPK ? "top-k launch"
-                                                                                           : "attention launch");
+  note_cuda_error(e, stage == DSA_STAGE_INDEXER        ? "indexer launch"
+                     : stage == DSA_STAGE_TOPK         ? "top-k launch"
+                     : stage == DSA_STAGE_ATTN         ? "attention launch"
+                     : stage == DSA_STAGE_APPEND       ? "cache append launch"
+                     : stage == DSA_STAGE_INDEXER_BWD ? "indexer backward launch"
+                                                       : "launch");
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (rec) {
     cudaEventRecord(g_prof[g_prof_n].b, st);
@@ -262,6 +266,27 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const
 
   const int64_t rows = (int64_t)(workspace_bytes / (score_ld(qd->max_kv) * sizeof(float)));
   return run_staged(qd, cd, ix, k, at, idx, out, lse, static_cast<float*>(workspace), rows, err, st);
+}
+
+dsa_status dsa_indexer_kl_backward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix,
+                                   const int32_t* idx, int32_t k, const float* p, float* loss, float* grad_scores,
+                                   float* dw, float* dq, float* dk, dsa_stream_t stream) {
+  DSA_TRY(check_query(qd));
+  if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+  if (qd->num_q == 0) return DSA_OK;
+  DSA_TRY(check_cache(cd, qd->max_kv));
+  DSA_TRY(check_indexer(ix));
+  if (ix->heads > 64 || (ix->dim != 32 && ix->dim != 64 && ix->dim != 128)) return DSA_ERR_UNSUPPORTED;
+  if (!idx || !p || !loss || !dw || !dq || !dk) return DSA_ERR_INVALID_ARG;
+  if (!aligned(idx, 4) || !aligned(p, 4) || !aligned(loss, 4) || !aligned(dw, 4) || !aligned(dq, 16) ||
+      !aligned(dk, 16) || (grad_scores && !aligned(grad_scores, 4)))
+    return DSA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return DSA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(launch(DSA_STAGE_INDEXER_BWD, st, [&] {
+    return launch_indexer_kl_bwd(to_batch(qd), to_map(cd), *ix, idx, k, p, loss, grad_scores, dw, dq, dk, err, st);
+  }));
 }
 
 dsa_status dsa_cache_append(const dsa_cache_desc* cd, int32_t num_tok, const int32_t* tok_seq, const int32_t* tok_pos,

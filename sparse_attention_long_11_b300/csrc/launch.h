@@ -49,6 +49,12 @@ inline cudaError_t launch_attn(const QueryBatch& qb, const CacheMap& cm, const d
   return launch_attn_simt(qb, cm, at, idx, k, out, lse, err, stream);
 }
 
+// Indexer alignment loss KL(p || softmax(I)) over each query's candidate
+// entries and its gradients for w, q and k (dk accumulated).  CUDA cores.
+cudaError_t launch_indexer_kl_bwd(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
+                                  const int32_t* idx, int k, const float* p, float* loss, float* grad_scores,
+                                  float* dw, float* dq, float* dk, int* err, cudaStream_t stream);
+
 // Appends new tokens to the caches: each key row (128 bf16 or fp32 values)
 // encoded as e4m3 codes with scale amax/448, and (when kv_new is non-null)
 // the latent row of d_qk bf16 values copied, or, with kv_scale, encoded the

@@ -315,6 +315,18 @@ def make_scores(num_q: int, n: int, seed: int, device="cpu", kind: str = "normal
     return x
 
 
+def kl_targets(idx: torch.Tensor, seed: int) -> torch.Tensor:
+    """Seeded synthetic target distributions for the indexer's alignment loss:
+    one row per query over its idx entries, u^3 (u uniform) normalised over
+    the valid entries (idx >= 0), 0 at padding; about 1 entry in 16 is set to
+    exactly 0 so zero targets occur.  fp32, on idx's device."""
+    u = rand(tuple(idx.shape), seed, "kl_target", idx.device) ** 3
+    u = torch.where(rand(tuple(idx.shape), seed, "kl_zero", idx.device) < 1.0 / 16, torch.zeros_like(u), u)
+    u = torch.where(idx >= 0, u, torch.zeros_like(u))
+    tot = u.sum(dim=1, keepdim=True)
+    return torch.where(tot > 0, u / torch.where(tot > 0, tot, torch.ones_like(tot)), u).contiguous()
+
+
 def random_index_sets(q_pos: torch.Tensor, k: int, seed: int) -> torch.Tensor:
     """For each query position p, a seeded random subset of min(k, p+1)
     positions in [0, p], ascending, padded with -1 to width k (CPU int32)."""

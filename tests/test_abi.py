@@ -122,6 +122,21 @@ def test_cache_append_validation_rejects_before_launch():
     assert f(kvs=A, dqk=72) == api.DSA_ERR_UNSUPPORTED
 
 
+def test_indexer_kl_backward_validation_rejects_before_launch():
+    L = api.lib()
+    cd = api.CacheDesc(1, 4096, 4096, None, 0, 0)
+    qd = api.QueryDesc(16, 0x10000, 0x10000, 4096)
+    A = 0x10000
+    f = lambda q=qd, ix=_ix(), idx=A, k=2048, p=A, loss=A, g=None, dw=A, dq=A, dk=A: L.dsa_indexer_kl_backward(
+        ctypes.byref(q), ctypes.byref(cd), ctypes.byref(ix), idx, k, p, loss, g, dw, dq, dk, None)
+    assert f(q=api.QueryDesc(0, None, None, 0)) == api.DSA_OK          # empty batch: no launch
+    assert f(k=0) == api.DSA_ERR_INVALID_ARG and f(k=8193) == api.DSA_ERR_INVALID_ARG
+    assert f(idx=None) == api.DSA_ERR_INVALID_ARG and f(dk=None) == api.DSA_ERR_INVALID_ARG
+    assert f(dq=A + 4) == api.DSA_ERR_INVALID_ARG                      # dq and dk take float4 stores/atomics
+    assert f(dk=A + 8) == api.DSA_ERR_INVALID_ARG
+    assert f(ix=_ix(dtype=api.DSA_F32, scales=False, heads=80)) == api.DSA_ERR_UNSUPPORTED
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(api, "_lib", None)
     monkeypatch.setattr(api, "LIB_PATH", str(tmp_path / "libdsa.so"))
