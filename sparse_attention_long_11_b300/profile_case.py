@@ -3,7 +3,10 @@
     python -m sparse_attention_long_11_b300.profile_case --workload prefill --reps 2
 
 Workloads: tiny, prefill (L=4096), long (L=32768, 8 chunks), decode
-(64 x 65536), mixed (8 paged sequences).  Exits non-zero on a device error.
+(64 x 65536), mixed (8 paged sequences).  With --kl-backward it runs, after
+the forward repetitions, the indexer's training step (dsa_indexer_kl_backward)
+on the selected entries with seeded synthetic targets, --reps times.
+Exits non-zero on a device error.
 """
 import argparse
 import sys
@@ -20,6 +23,8 @@ def main() -> int:
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--q-rows", default=None,
                     help="a:b -- keep only query positions [a, b) of the prefill workloads (all keys stay cached)")
+    ap.add_argument("--kl-backward", action="store_true",
+                    help="then run the indexer backward on the forward's selections, --reps times")
     ap.add_argument("--decode-batch", type=int, default=64,
                     help="sequences of the decode workload (65536 cached rows each)")
     a = ap.parse_args()
@@ -42,6 +47,14 @@ def main() -> int:
     for _ in range(a.reps):
         for r0, r1, qd, ix, at in calls:
             api.dsa_forward(qd, cache, ix, wl.topk, at, idx[r0:r1], out[r0:r1], lse[r0:r1], ws)
+    if a.kl_backward:
+        p = inputs.kl_targets(idx, seed=1)
+        loss = torch.empty(wl.num_q, dtype=torch.float32, device="cuda")
+        dw = torch.empty((wl.num_q, wl.H_I), dtype=torch.float32, device="cuda")
+        dq = torch.empty((wl.num_q, wl.H_I, wl.d_I), dtype=torch.float32, device="cuda")
+        dk = torch.zeros((wl.num_rows, wl.d_I), dtype=torch.float32, device="cuda")
+        for _ in range(a.reps):
+            api.dsa_indexer_kl_backward(prob.batch.desc(), cache, prob.ix, idx, wl.topk, p, loss, dw, dq, dk)
     st = api.dsa_check_device_error()
     print(f"{a.workload}: {wl.num_q} queries x {a.reps} reps, launches={api.dsa_launch_count()}, "
           f"status={api.status_string(st)}")
