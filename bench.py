@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import dataclasses
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -192,12 +193,19 @@ def _pairs(wl):
     return int((pos + 1).sum()), int(torch.clamp(pos + 1, max=wl.topk).sum())
 
 
-def _time_steps(r: Runner, steps: int, warmup: int, ws: int, gpu: int):
+def _time_steps(r: Runner, steps: int, warmup: int, ws: int, gpu: int, profile: bool = True):
+    """Times `steps` steps after `warmup` untimed ones, with CUDA events on the
+    launching stream and nvidia-smi clocks sampled during the timed region.
+    With `profile`, every launch is also bracketed by library events (per-stage
+    device time); the loop time is then measured with that bookkeeping in it.
+    Returns (ms per step, {stage: [launches, total ms]}, launches, clocks)."""
     for _ in range(warmup):
         r.step()
     torch.cuda.synchronize()
-    cap = 8192
-    api.dsa_profile_start(cap)
+    cap = 0
+    if profile:
+        cap = max(8192, steps * len(r.calls) * 8)
+        api.dsa_profile_start(cap)
     n0 = api.dsa_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu) as clk:
@@ -210,17 +218,17 @@ def _time_steps(r: Runner, steps: int, warmup: int, ws: int, gpu: int):
         torch.cuda.synchronize()
         _barrier(ws)
     launches = api.dsa_launch_count() - n0
-    api.dsa_profile_stop()
-    recs = api.dsa_profile_read(cap)
+    per_stage = {}
+    if profile:
+        api.dsa_profile_stop()
+        for s_, t in api.dsa_profile_read(cap):
+            d = per_stage.setdefault(api.STAGE_NAMES[s_], [0, 0.0])
+            d[0] += 1
+            d[1] += t
     st = api.dsa_check_device_error()
     if st != api.DSA_OK:
         raise RuntimeError(f"device error during bench: {api.status_string(st)}")
     ms = e0.elapsed_time(e1) / steps
-    per_stage = {}
-    for s, t in recs:
-        d = per_stage.setdefault(api.STAGE_NAMES[s], [0, 0.0])
-        d[0] += 1
-        d[1] += t
     return ms, per_stage, launches, clk.summary()
 
 
@@ -234,16 +242,20 @@ def _roofline_prefill(wl, per_stage, steps, peaks):
                         "topk": n_idx * steps / cnt}[dom]
     if dom == "attention":
         achieved = per_launch_units * FLOP_PER_ATTN_PAIR / avg_s / 1e12
-        return {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sus"],
-                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sus"],
+        return {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
+                "frac_of_sustained": achieved / peaks["bf16_sus"],
                 "traffic": _traffic("prefill_attention", "attn"),
-                "peak_src": f"{peaks['src']} bf16 sustained", "avg_launch_ms": tot / cnt, "launches": cnt}
+                "peak_src": f"{peaks['src']} bf16 burst (kernel timed in a sub-second step); "
+                            f"frac_of_sustained against {peaks['bf16_sus']}",
+                "avg_launch_ms": tot / cnt, "launches": cnt}
     if dom == "indexer":
         # FP8 peak = measured bf16 peak x the nominal fp8/bf16 ratio (2)
-        pk = 2 * peaks["bf16_sus"]
+        pk = 2 * peaks["bf16"]
         achieved = per_launch_units * FLOP_PER_IDX_PAIR / avg_s / 1e12
         return {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": pk, "unit": "TFLOP/s",
-                "frac": achieved / pk, "traffic": None, "peak_src": f"{peaks['src']} bf16 sustained x2 (fp8)",
+                "frac": achieved / pk, "frac_of_sustained": achieved / (2 * peaks["bf16_sus"]), "traffic": None,
+                "peak_src": f"{peaks['src']} bf16 burst x2 (fp8/bf16 nominal ratio)",
                 "avg_launch_ms": tot / cnt, "launches": cnt}
     achieved = per_launch_units * 4 / avg_s / 1e9
     return {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
@@ -267,6 +279,25 @@ def _roofline_decode(wl, per_stage, steps, peaks):
             "frac": achieved / peaks["hbm"], "traffic": _traffic("decode_indexer", dom) if dom == "indexer" else None,
             "peak_src": f"{peaks['src']} hbm burst",
             "avg_launch_ms": tot / cnt, "launches": cnt}
+
+
+def _decode_stage_roofline(wl, per_stage, steps, peaks):
+    """HBM fraction of every decode stage: algorithmic bytes per launch (indexer:
+    the FP8 key rows and scales of every causal pair; top-k: the staged score
+    rows read and the index rows written; attention: the gathered latent rows
+    plus q read and O written) over its average launch time."""
+    n_idx, n_attn = _pairs(wl)
+    byts = {"indexer": n_idx * BYTES_PER_IDX_KEY,
+            "topk": n_idx * 4 + wl.num_q * wl.topk * 4,
+            "attention": n_attn * BYTES_PER_ATTN_KEY + wl.num_q * wl.H * (wl.d_qk + wl.d_v) * 2}
+    out = {}
+    for name, (cnt, tot) in per_stage.items():
+        if name not in byts:
+            continue
+        ms = tot / steps
+        gbs = byts[name] / (ms / 1e3) / 1e9
+        out[name] = {"bytes": byts[name], "ms": ms, "achieved_gbs": gbs, "frac": gbs / peaks["hbm"]}
+    return out
 
 
 def _time_append(wl, r: Runner, steps: int, warmup: int):
@@ -408,22 +439,41 @@ def _e2e(wl, steps: int):
     return wl.num_q / (ms / 1e3), h2d, d2h, ms
 
 
-def _oracle_sample(wl, budget_s: float, max_q: int = 100000):
-    """Runs the CPU oracle on a stratified sample of the workload's queries
-    (evenly spaced positions) until the time budget is spent."""
-    from oracle.workload_view import OracleView
-    view = OracleView(wl)
-    nq = wl.num_q
-    order = np.linspace(0, nq - 1, min(nq, 256)).astype(int)
-    t0 = time.perf_counter()
-    done = 0
-    for i in order[:max_q]:
-        view.run(int(i))
-        done += 1
-        if time.perf_counter() - t0 > budget_s:
-            break
-    dt = time.perf_counter() - t0
-    return done, dt, _blas_threads()
+class OracleSampler:
+    """The CPU oracle (full path: indexer, top-k, attention) over a stratified
+    sample of the workload's queries: 256 evenly spaced query rows, visited in
+    a seeded random order so that any prefix of the visit is an unbiased
+    sample of the positions (early queries are cheaper than late ones).
+    Successive calls continue where the last one stopped."""
+
+    def __init__(self, wl, points: int = 256, seed: int = 0):
+        from oracle.workload_view import OracleView
+        self.view = OracleView(wl)
+        self.pos = wl.q_pos.to("cpu").numpy()
+        pts = np.linspace(0, wl.num_q - 1, min(wl.num_q, points)).astype(int)
+        self.order = pts[np.random.default_rng(seed).permutation(len(pts))]
+        self.next = 0
+        self.visited = []
+
+    def run(self, budget_s: float, max_q: int = 1 << 30):
+        """Runs queries until budget_s is spent (at least one); returns (queries, seconds)."""
+        t0 = time.perf_counter()
+        done = 0
+        while done < max_q:
+            i = int(self.order[self.next % len(self.order)])
+            self.next += 1
+            self.view.run(i)
+            self.visited.append(int(self.pos[i]))
+            done += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        return done, time.perf_counter() - t0
+
+    def describe(self) -> str:
+        v = np.asarray(self.visited)
+        distinct = len(set(self.visited))
+        return (f"{len(v)} query visits ({distinct} distinct of {len(self.order)} evenly spaced rows, seeded random "
+                f"order), positions {v.min()}..{v.max()}, mean {v.mean():.0f}")
 
 
 def _blas_threads() -> int:
@@ -444,15 +494,18 @@ def run_reference(args, ws, rank):
         return
     wl = inputs.make_long(seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
     budget = 4.0
+    warm = OracleSampler(wl, seed=1)
     for _ in range(args.warmup):
-        _oracle_sample(wl, 0.5, max_q=2)
-    done_tot, t_tot, cores = 0, 0.0, 1
+        warm.run(0.5, max_q=1)
+    samp = OracleSampler(wl, seed=0)
+    done_tot, t_tot = 0, 0.0
     for _ in range(args.steps):
-        d, t, cores = _oracle_sample(wl, budget)
+        d, t = samp.run(budget)
         done_tot += d
         t_tot += t
     val = done_tot / t_tot
-    sample = (f"{done_tot} queries over {args.steps} steps, evenly spaced positions of the L=32768 prefill "
+    cores = _blas_threads()
+    sample = (f"{samp.describe()} of the L=32768 prefill over {args.steps} steps "
               f"(~{budget:.0f} s of oracle work per step)")
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_tot / args.steps * 1e3,
@@ -477,6 +530,7 @@ def main():
     ap.add_argument("--no-128k", action="store_true")
     ap.add_argument("--no-fp8-kv", action="store_true")
     ap.add_argument("--no-kl-backward", action="store_true")
+    ap.add_argument("--no-mixed", action="store_true")
     args = ap.parse_args()
     ws, rank, local = _dist()
     if args.impl == "reference":
@@ -503,10 +557,11 @@ def main():
 
     cpu = None
     if rank == 0 and ws == 1:
-        done, dt, cores = _oracle_sample(wl, args.cpu_budget)
-        cpu = {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{done} queries at evenly spaced positions of the L=32768 prefill, "
-                         f"full oracle path (indexer, top-k, attention) in {dt:.1f} s"}
+        samp = OracleSampler(wl, seed=0)
+        done, dt = samp.run(args.cpu_budget, max_q=len(samp.order))
+        cpu = {"value": done / dt, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+               "sample": f"{samp.describe()} of the L=32768 prefill, full oracle path (indexer, top-k, "
+                         f"attention) in {dt:.1f} s"}
     prefill_fp8_kv = None
     if not args.no_fp8_kv:
         # the same prefill over an FP8 latent cache (not part of the headline value)
@@ -554,29 +609,60 @@ def main():
     if not args.no_decode:
         wd = inputs.make_decode(seed=0, device=dev)
         rd = Runner(wd)
-        dms, dstage, dl, dclk = _time_steps(rd, max(args.steps, 10), args.warmup, ws, local)
+        # per-stage device times from a short run with per-launch events
+        nprof = 20
+        _, dstage, _, _ = _time_steps(rd, nprof, args.warmup, ws, local, profile=True)
+        # the decode value: at least one second of back-to-back steps without
+        # per-launch bookkeeping, so that the clock sampler sees the load
+        est, _, _, _ = _time_steps(rd, 20, 1, ws, local, profile=False)
+        nd = max(args.steps, int(math.ceil(1200.0 / max(est, 1e-3))))
+        dms, _, dl, dclk = _time_steps(rd, nd, 1, ws, local, profile=False)
         dval, dms = aggregate(wd.num_q, dms, ws)
         decode = {"workload": "decode B=64, ctx 65536 each, k=2048", "value": dval,
-                  "unit": "tokens/s", "ms_per_step": dms, "gpu_launches": dl,
-                  "stages": {k: {"launches": v[0], "ms_per_step": v[1] / max(args.steps, 10)}
-                             for k, v in dstage.items()},
-                  "roofline": _roofline_decode(wd, dstage, max(args.steps, 10), peaks), "clocks": dclk}
+                  "unit": "tokens/s", "ms_per_step": dms, "steps": nd, "gpu_launches": dl,
+                  "stages": {k: {"launches": v[0], "ms_per_step": v[1] / nprof} for k, v in dstage.items()},
+                  "stage_roofline": _decode_stage_roofline(wd, dstage, nprof, peaks),
+                  "roofline": _roofline_decode(wd, dstage, nprof, peaks), "clocks": dclk}
         decode["cache_append"] = _time_append(wd, rd, max(args.steps, 10), args.warmup)
         del rd
         if not args.no_fp8_kv:
             # the same batch over an FP8 latent cache (e4m3 codes + one fp32 scale per row)
             w8 = inputs.with_fp8_kv(wd)
             r8 = Runner(w8)
-            ms8, st8, _, _ = _time_steps(r8, max(args.steps, 10), args.warmup, ws, local)
+            ms8, st8, _, _ = _time_steps(r8, nprof, args.warmup, ws, local)
             v8, ms8 = aggregate(w8.num_q, ms8, ws)
             _, n_attn = _pairs(w8)
-            a_ms = st8["attention"][1] / max(args.steps, 10)
+            a_ms = st8["attention"][1] / nprof
             decode["fp8_kv"] = {"value": v8, "unit": "tokens/s", "ms_per_step": ms8,
-                                "stages": {n: round(v[1] / max(args.steps, 10), 4) for n, v in st8.items()},
+                                "stages": {n: round(v[1] / nprof, 4) for n, v in st8.items()},
                                 "attention_gather_gbs": n_attn * BYTES_PER_ATTN_KEY_FP8 / (a_ms / 1e3) / 1e9}
             decode["fp8_kv"]["cache_append"] = _time_append(w8, r8, max(args.steps, 10), args.warmup)
             del r8, w8
         del wd
+        torch.cuda.empty_cache()
+
+    # ---------------- mixed paged batch (not part of the headline value)
+    mixed = None
+    if not args.no_mixed:
+        wm = inputs.make_mixed(seed=0, device=dev)
+        rm = Runner(wm)
+        mms, mst, _, mclk = _time_steps(rm, 2, args.warmup, ws, local)
+        mms = _max_over_ranks(mms, ws)
+        n_idx, n_attn = _pairs(wm)
+        ims, ams = mst["indexer"][1] / 2, mst["attention"][1] / 2
+        at_tf = n_attn * FLOP_PER_ATTN_PAIR / (ams / 1e3) / 1e12
+        mixed = {"workload": f"mixed paged batch: 8 sequences of {min(wm.seq_lens)}..{max(wm.seq_lens)} cached "
+                             f"rows (block 64, permuted pool), per sequence 8192 prefill + 32 decode queries, "
+                             f"k=2048, one call",
+                 "value": wm.num_q * ws / (mms / 1e3), "unit": "tokens/s", "ms_per_step": mms,
+                 "queries": wm.num_q, "indexer_pairs": n_idx, "attention_pairs": n_attn,
+                 "stages": {n: round(v[1] / 2, 3) for n, v in mst.items()},
+                 "indexer_tflops": n_idx * FLOP_PER_IDX_PAIR / (ims / 1e3) / 1e12,
+                 "roofline": {"kernel": "attention", "bound": "tensor", "achieved": at_tf, "peak": peaks["bf16"],
+                              "unit": "TFLOP/s", "frac": at_tf / peaks["bf16"],
+                              "peak_src": f"{peaks['src']} bf16 burst"},
+                 "clocks": mclk}
+        del rm, wm
         torch.cuda.empty_cache()
 
     if rank == 0:
@@ -591,7 +677,8 @@ def main():
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "cpu_baseline": cpu, "decode": decode, "k_sweep": k_sweep,
-                "prefill_128k": long128k, "prefill_fp8_kv": prefill_fp8_kv, "indexer_kl_backward": kl_bwd}
+                "prefill_128k": long128k, "prefill_fp8_kv": prefill_fp8_kv, "indexer_kl_backward": kl_bwd,
+                "mixed": mixed}
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist

@@ -149,6 +149,19 @@ DSA_API dsa_status dsa_index_scores(const dsa_query_desc* qd, const dsa_cache_de
                             const dsa_indexer_inputs* ix, float* scores, int64_t ld_scores,
                             dsa_stream_t stream);
 
+/* dsa_index_scores with an explicit bound on the kernel's device-side waits:
+ * every wait of the tensor-core indexer gives up after wait_limit_cycles SM
+ * clocks (dsa_index_scores uses about 2e9, one second).  A test aid for the
+ * timeout path: with a limit of a few hundred clocks the kernel's pipeline
+ * waits expire, the kernel drains its own in-flight copies and MMAs, frees
+ * its tensor memory and returns, and dsa_check_device_error() reports
+ * DSA_ERR_TIMEOUT; the scores are then undefined and the context stays
+ * usable.  Ignored by the CUDA-core indexer (DSA_F32), which has no waits.
+ * wait_limit_cycles >= 1, else DSA_ERR_INVALID_ARG. */
+DSA_API dsa_status dsa_index_scores_wait_limit(const dsa_query_desc* qd, const dsa_cache_desc* cd,
+                                               const dsa_indexer_inputs* ix, float* scores, int64_t ld_scores,
+                                               int64_t wait_limit_cycles, dsa_stream_t stream);
+
 /* Stage 2 alone: per query row i, the top-k of scores[i * ld_scores + s] over
  * s = 0..q_pos[i] (scores at larger s are ignored), written to
  * idx[i * k .. i * k + k) in ascending s, padded with -1 when q_pos[i] + 1 < k.

@@ -55,6 +55,8 @@ _P = ctypes.POINTER
 _SIGS = {
     "dsa_index_scores": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(IndexerInputs), ctypes.c_void_p,
                                         ctypes.c_int64, ctypes.c_void_p]),
+    "dsa_index_scores_wait_limit": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(IndexerInputs), ctypes.c_void_p,
+                                                   ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]),
     "dsa_topk": (ctypes.c_int, [_P(QueryDesc), ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p,
                                 ctypes.c_void_p]),
     "dsa_sparse_attn": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(AttnInputs), ctypes.c_void_p,
@@ -171,6 +173,15 @@ def dsa_index_scores(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, scor
                      stream=None) -> None:
     _check(lib().dsa_index_scores(ctypes.byref(batch), ctypes.byref(cache), ctypes.byref(ix), _ptr(scores),
                                   scores.stride(0), _stream(stream)), "dsa_index_scores")
+
+
+def dsa_index_scores_wait_limit(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, scores: torch.Tensor,
+                                wait_limit_cycles: int, stream=None) -> None:
+    """dsa_index_scores with every device-side wait bounded by wait_limit_cycles
+    SM clocks (a test aid for the timeout path)."""
+    _check(lib().dsa_index_scores_wait_limit(ctypes.byref(batch), ctypes.byref(cache), ctypes.byref(ix),
+                                             _ptr(scores), scores.stride(0), int(wait_limit_cycles),
+                                             _stream(stream)), "dsa_index_scores_wait_limit")
 
 
 def dsa_topk(batch: QueryDesc, scores: torch.Tensor, k: int, idx: torch.Tensor, stream=None) -> None:

@@ -211,6 +211,23 @@ dsa_status dsa_index_scores(const dsa_query_desc* qd, const dsa_cache_desc* cd, 
   }));
 }
 
+dsa_status dsa_index_scores_wait_limit(const dsa_query_desc* qd, const dsa_cache_desc* cd,
+                                      const dsa_indexer_inputs* ix, float* scores, int64_t ld_scores,
+                                      int64_t wait_limit_cycles, dsa_stream_t stream) {
+  if (wait_limit_cycles < 1) return DSA_ERR_INVALID_ARG;
+  DSA_TRY(check_query(qd));
+  if (qd->num_q == 0) return DSA_OK;
+  DSA_TRY(check_cache(cd, qd->max_kv));
+  DSA_TRY(check_indexer(ix));
+  if (!scores || !aligned(scores, 16) || ld_scores < qd->max_kv || ld_scores % 4) return DSA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return DSA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(launch(DSA_STAGE_INDEXER, st, [&] {
+    return launch_indexer(to_batch(qd), to_map(cd), *ix, scores, ld_scores, err, st, (long long)wait_limit_cycles);
+  }));
+}
+
 dsa_status dsa_topk(const dsa_query_desc* qd, const float* scores, int64_t ld_scores, int32_t k, int32_t* idx,
                     dsa_stream_t stream) {
   DSA_TRY(check_query(qd));

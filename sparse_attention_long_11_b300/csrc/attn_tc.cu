@@ -95,7 +95,7 @@ __device__ long long g_attn_trace[4][512][8];
 struct Bars {
   uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], xf[2], xe[2];
   uint64_t s_empty[2], p_full[2], pv_done[2], mdone[2];
-  uint64_t q_full, q_empty, o_empty, qend, fin[2];
+  uint64_t q_full, q_rope, q_empty, o_empty, qend, fin[2];
   float mtile[2][128];          // [group][head] scratch: the tile maximum
   float mpub[2][128];           // [tile parity][head] running maximum after the group's latest tile
   float lsum[2][2][128];        // [query parity][group][head] the groups' sums at the end of a query
@@ -120,14 +120,6 @@ __device__ __forceinline__ int count_tiles(const int32_t* row, int k, int pos, b
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
   return last < 0 ? 0 : last / kNK + 1;
-}
-
-__device__ __forceinline__ bool wait_fin(uint64_t* bar) {   // bounded, ignores the abort flag
-  const uint32_t a = smem_u32(bar);
-  const long long t0 = clock64();
-  while (!mbar_try_wait(a, 0))
-    if (clock64() - t0 > kWaitLimitCycles) return false;
-  return true;
 }
 
 struct QueryInfo {
@@ -191,7 +183,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       mbar_init(&B.xf[s], 1);          // armed by our thread 0; the peer's st.async credit the bytes
       mbar_init(&B.xe[s], 128);        // arrivals of the peer's softmax group of this parity
     }
-    mbar_init(&B.q_full, 129);       // 128 TMEM writers + the rope TMA (with its bytes)
+    mbar_init(&B.q_full, 128);       // the 128 TMEM writers of Q's latent part
+    mbar_init(&B.q_rope, 1);         // the rope TMA (with its bytes)
     mbar_init(&B.q_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&B.p_full[s], 128);
@@ -450,7 +443,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     const bool q_writer = warp < 12;                         // warps 8-11 cover the four TMEM lane quadrants
     const int hq = ((warp & 3) << 5) | lane;                 // TMEM lane (head) this thread writes Q for
     const uint32_t q_lane = (uint32_t)((warp & 3) * 32) << 16;
-    uint32_t g = 0, qv = 0;
+    uint32_t g = 0, qv = 0, n_rope = 0;   // n_rope: rope TMA loads issued (warp 8, lane 0)
     if (warp == 8 && lane == 0) tma_prefetch_desc(&tm_q_rope);
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
       const QueryInfo qi = query_info(qb, idx, k, i, pv);
@@ -460,8 +453,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       // Q of this query: every S MMA of the previous query has completed
       if (q_writer && !mbar_wait(&B.q_empty, (qv & 1) ^ 1, abort)) break;
       if (warp == 8 && lane == 0) {
-        mbar_arrive_expect_tx(&B.q_full, kQRopeBytes);
-        tma_load_2d(sQr, &tm_q_rope, 512 + 32 * crank, i * kH, &B.q_full);
+        mbar_arrive_expect_tx(&B.q_rope, kQRopeBytes);
+        tma_load_2d(sQr, &tm_q_rope, 512 + 32 * crank, i * kH, &B.q_rope);
+        ++n_rope;
         if (i + ncl < qb.num_q) tma_prefetch_2d(&tm_q_rope, 512 + 32 * crank, (i + ncl) * kH);
       }
       if (q_writer) {
@@ -597,6 +591,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       if (!ok) break;
       ++qv;
     }
+    // the last rope TMA issued here has landed before the CTA may exit
+    if (warp == 8 && lane == 0 && n_rope > 0) mbar_wait_own(&B.q_rope, (n_rope - 1) & 1);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ score MMA issue (lane 0)
     // S(g) goes into buffer g % 2 once the softmax group has loaded S(g-2)
@@ -609,7 +605,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       const QueryInfo qi = query_info(qb, idx, k, i, pv);
       const int nt = qi.nt;
       if (nt == 0) continue;
-      if (!mbar_wait(&B.q_full, qv & 1, abort)) break;
+      if (!mbar_wait(&B.q_full, qv & 1, abort) || !mbar_wait(&B.q_rope, qv & 1, abort)) break;
       bool ok = true;
       for (int t = 0; t < nt; ++t, ++g) {
         const uint32_t st = g % kStages, sb = g & 1;
@@ -644,7 +640,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     }
     if (lane == 0) mma_commit(&B.fin[0]);
     __syncwarp();
-    wait_fin(&B.fin[0]);   // every MMA issued by this warp has completed
+    mbar_wait_own(&B.fin[0], 0);   // every MMA issued by this warp has completed
   } else {
     // ------------------------------------------------------------ P.V MMA issue (warp 15, lane 0)
     const uint32_t id_pv = idesc_bf16(128, 256, true);
@@ -679,7 +675,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     }
     if (lane == 0) mma_commit(&B.fin[1]);
     __syncwarp();
-    wait_fin(&B.fin[1]);   // every MMA issued by this warp has completed
+    mbar_wait_own(&B.fin[1], 0);   // every MMA issued by this warp has completed
   }
 
   tc_fence_before();

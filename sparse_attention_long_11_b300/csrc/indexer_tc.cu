@@ -206,19 +206,11 @@ __device__ __forceinline__ float head_partial(const uint32_t (&r)[16], const flo
   return (alo + ahi) + (blo + bhi);
 }
 
-__device__ __forceinline__ bool wait_plain(uint64_t* bar, uint32_t parity) {
-  const uint32_t a = smem_u32(bar);
-  const long long t0 = clock64();
-  while (!mbar_try_wait(a, parity))
-    if (clock64() - t0 > kWaitLimitCycles) return false;
-  return true;
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   QueryBatch qb, CacheMap cm, const float* __restrict__ q_scale, const float* __restrict__ w,
                   const float* __restrict__ k_scale, float* __restrict__ scores, int64_t ld, int ngroups,
-                  int nchunk, int ch, int* err) {
+                  int nchunk, int ch, long long wait_limit, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Shared S;
@@ -257,16 +249,17 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      uint32_t g = 0, j = 0;
+      uint32_t g = 0, j = 0;   // key tiles and query tiles issued
       for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
         const int gi = item % ngroups, c = item / ngroups;
         Group G;
         describe_group(qb, cm, gi, G);
         if (item_tiles(G, c, ch) == 0) continue;
         const int bb = j & 1;
-        if (!mbar_wait(&S.b_empty[bb], ((j >> 1) & 1) ^ 1, abort)) break;
+        if (!mbar_wait(&S.b_empty[bb], ((j >> 1) & 1) ^ 1, abort, wait_limit)) break;
         mbar_arrive_expect_tx(&S.b_full[bb], kBBytes);
         tma_load_2d(sB + bb * kBBytes, &tm_q, 0, gi * kQG * kHI, &S.b_full[bb]);
+        ++j;
         bool ok = true;
         for (int p = 0; p < G.npass && ok; ++p) {
           const int seq = G.pass_seq[p], mp = G.pass_maxpos[p];
@@ -275,7 +268,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           for (int t = t0; t < t1; ++t, ++g) {
             const int st = g % kStagesA;
             IDX_TRACE(0, g, 0, true);
-            if (!(ok = mbar_wait(&S.a_empty[st], ((g / kStagesA) & 1) ^ 1, abort))) break;
+            if (!(ok = mbar_wait(&S.a_empty[st], ((g / kStagesA) & 1) ^ 1, abort, wait_limit))) break;
             IDX_TRACE(0, g, 1, true);
             int64_t rows[2];
             uint32_t bytes = 0;
@@ -302,7 +295,17 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
         }
         if (!ok) break;
-        ++j;
+      }
+      // Before the CTA may exit (after an abort the consumers stop waiting),
+      // every TMA load issued here must have landed: wait for the last phase
+      // armed on each stage and query buffer (each completes by its own bytes).
+      for (uint32_t st = 0; st < (uint32_t)kStagesA && st < g; ++st) {
+        const uint32_t last = st + kStagesA * ((g - 1 - st) / kStagesA);
+        mbar_wait_own(&S.a_full[st], (last / kStagesA) & 1);
+      }
+      for (uint32_t b = 0; b < 2 && b < j; ++b) {
+        const uint32_t last = b + 2 * ((j - 1 - b) / 2);
+        mbar_wait_own(&S.b_full[b], (last >> 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -314,7 +317,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       describe_group(qb, cm, gi, G);
       if (item_tiles(G, c, ch) == 0) continue;
       const int bb = j & 1;
-      if (!mbar_wait(&S.b_full[bb], (j >> 1) & 1, abort)) break;
+      if (!mbar_wait(&S.b_full[bb], (j >> 1) & 1, abort, wait_limit)) break;
       bool ok = true;
       // One accumulator buffer holds one shared-pass tile (4 queries x 64
       // heads) or up to four consecutive per-query tiles (64 columns each),
@@ -329,9 +332,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int t = t0; t < t1; ++t, ++g, ++dq) {
           const int st = g % kStagesA, b = dq & 1;
           IDX_TRACE(1, g, 0, lane == 0);
-          if (!(ok = mbar_wait(&S.a_full[st], (g / kStagesA) & 1, abort))) break;
+          if (!(ok = mbar_wait(&S.a_full[st], (g / kStagesA) & 1, abort, wait_limit))) break;
           IDX_TRACE(1, g, 1, lane == 0);
-          if (!(ok = mbar_wait(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort))) break;
+          if (!(ok = mbar_wait(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort, wait_limit))) break;
           IDX_TRACE(1, g, 2, lane == 0);
           tc_fence_after();
           if (lane == 0) {
@@ -347,14 +350,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       for (int e0 = 0; e0 < ne && ok && !uni; e0 += per_d, ++dq) {
         const int b = dq & 1, nsub = min(per_d, ne - e0);
-        if (!(ok = mbar_wait(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort))) break;
+        if (!(ok = mbar_wait(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort, wait_limit))) break;
         for (int u = 0; u < nsub; ++u, ++g) {
           int p, t;
           entry_at(G, c, ch, e0 + u, p, t);
           const uint32_t boff = bb * kBBytes + (uni ? 0u : (uint32_t)G.pass_q[p] * (kHI * 128));
           const int st = g % kStagesA;
           IDX_TRACE(1, g, 0, lane == 0);
-          if (!(ok = mbar_wait(&S.a_full[st], (g / kStagesA) & 1, abort))) break;
+          if (!(ok = mbar_wait(&S.a_full[st], (g / kStagesA) & 1, abort, wait_limit))) break;
           IDX_TRACE(1, g, 1, lane == 0);
           tc_fence_after();
           if (lane == 0) {
@@ -377,7 +380,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     if (lane == 0) mma_commit(&S.fin);
     __syncwarp();
-    wait_plain(&S.fin, 0);
+    mbar_wait_own(&S.fin, 0);
   } else {
     // ------------------------------------------------------------ epilogue
     const int qd = warp & 3, uq = (warp - 2) >> 2, et = tid - 64;
@@ -396,7 +399,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 r < qb.num_q ? __ldg(w + (int64_t)r * kHI + jj) * __ldg(q_scale + (int64_t)r * kHI + jj) : 0.f;
           }
           mbar_arrive(&S.epi_sync[bb]);
-          if (!mbar_wait(&S.epi_sync[bb], (j >> 1) & 1, abort)) break;
+          if (!mbar_wait(&S.epi_sync[bb], (j >> 1) & 1, abort, wait_limit)) break;
         }
         bool ok = true;
         const bool uni = G.uniform;
@@ -420,7 +423,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               if (key_ok) sk = __ldg(k_scale + row);
             }
             IDX_TRACE(2, dq, 0, et == 0);
-            if (!(ok = mbar_wait(&S.d_full[b], (dq >> 1) & 1, abort))) break;
+            if (!(ok = mbar_wait(&S.d_full[b], (dq >> 1) & 1, abort, wait_limit))) break;
             IDX_TRACE(2, dq, 1, et == 0);
             tc_fence_after();
             float P[4];
@@ -462,7 +465,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (key_ok) sk = __ldg(k_scale + row);
           }
           IDX_TRACE(2, dq, 0, et == 0);
-          if (!(ok = mbar_wait(&S.d_full[b], (dq >> 1) & 1, abort))) break;
+          if (!(ok = mbar_wait(&S.d_full[b], (dq >> 1) & 1, abort, wait_limit))) break;
           IDX_TRACE(2, dq, 1, et == 0);
           tc_fence_after();
           if (mine) {
@@ -549,7 +552,7 @@ bool indexer_tc_supported(const CacheMap& cm, const dsa_indexer_inputs& ix) {
 }
 
 cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix, float* scores,
-                              int64_t ld, int* err, cudaStream_t stream) {
+                              int64_t ld, int* err, cudaStream_t stream, long long wait_limit) {
   CUtensorMap tm_q, tm_k;
   if (!make_tmap_rows128(&tm_q, ix.q, (uint64_t)qb.num_q * kHI, 128, kQG * kHI)) return cudaErrorInvalidValue;
   if (!make_tmap_rows128(&tm_k, ix.k, (uint64_t)cm.num_rows, 128, 64)) return cudaErrorInvalidValue;
@@ -575,7 +578,7 @@ cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const ds
   cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
   indexer_tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tm_q, tm_k, qb, cm, ix.q_scale, ix.w, ix.k_scale, scores,
-                                                             ld, ngroups, nchunk, ch, err);
+                                                             ld, ngroups, nchunk, ch, wait_limit, err);
   return cudaGetLastError();
 }
 

@@ -22,13 +22,17 @@ cudaError_t launch_attn_simt(const QueryBatch& qb, const CacheMap& cm, const dsa
 
 // Lightning indexer on tcgen05 tensor cores: FP8 e4m3, 64 heads x 128, contiguous
 // caches or paged caches whose block size is a multiple of 64.
+// wait_limit: SM clocks after which any of the kernel's waits gives up
+// (DSA_ERR_TIMEOUT); the default is about one second.
 bool indexer_tc_supported(const CacheMap& cm, const dsa_indexer_inputs& ix);
 cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
-                              float* scores, int64_t ld, int* err, cudaStream_t stream);
+                              float* scores, int64_t ld, int* err, cudaStream_t stream,
+                              long long wait_limit = 2000000000LL);
 
 inline cudaError_t launch_indexer(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
-                                  float* scores, int64_t ld, int* err, cudaStream_t stream) {
-  if (indexer_tc_supported(cm, ix)) return launch_indexer_tc(qb, cm, ix, scores, ld, err, stream);
+                                  float* scores, int64_t ld, int* err, cudaStream_t stream,
+                                  long long wait_limit = 2000000000LL) {
+  if (indexer_tc_supported(cm, ix)) return launch_indexer_tc(qb, cm, ix, scores, ld, err, stream, wait_limit);
   return launch_indexer_simt(qb, cm, ix, scores, ld, err, stream);
 }
 

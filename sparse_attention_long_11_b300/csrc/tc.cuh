@@ -77,21 +77,48 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for phase `parity` of `bar` to complete.  Gives up (returns false and
-// raises *abort) after kWaitLimitCycles, or at once if *abort is already set,
-// so that a broken pipeline ends instead of hanging the GPU.
+// raises *abort) after `limit` SM clocks, or at once if *abort is already
+// set, so that a broken pipeline ends instead of hanging the GPU.  A limit
+// below kPollBelowCycles (a test of the timeout path) polls with the
+// non-blocking test_wait, so the limit is counted from the first look and
+// not hidden inside a hardware-suspended try_wait.
+constexpr long long kPollBelowCycles = 1000000LL;
 template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          long long limit = kWaitLimitCycles) {
   const uint32_t a = smem_u32(bar);
+  if (!kCluster && limit < kPollBelowCycles) {   // (cluster-scope waits always use try_wait)
+    const long long t0 = clock64();
+    while (true) {
+      if (mbar_test(bar, parity)) return true;
+      if (*abort) return false;
+      if (clock64() - t0 > limit) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
   if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (kCluster ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
     if (*abort) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort = 1;
       return false;
     }
   }
+}
+
+// Waits for a phase that completes by this thread's own asynchronous work
+// alone (its TMA loads, its MMAs): used before a CTA exits, so it ignores the
+// abort flag.  Bounded by kWaitLimitCycles; false if that expires.
+__device__ __forceinline__ bool mbar_wait_own(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (!mbar_try_wait(a, parity))
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  return true;
 }
 
 // ------------------------------------------------------------------ cp.async

@@ -142,3 +142,13 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(api, "LIB_PATH", str(tmp_path / "libdsa.so"))
     with pytest.raises(RuntimeError, match="missing"):
         api.lib()
+
+
+def test_wait_limit_entry_point_validates_on_the_host():
+    L = api.lib()
+    qd = api.QueryDesc(16, 0x10000, 0x10000, 4096)
+    cd = api.CacheDesc(1, 4096, 4096, None, 0, 0)
+    for limit in (0, -5):
+        st = L.dsa_index_scores_wait_limit(ctypes.byref(qd), ctypes.byref(cd), ctypes.byref(_ix()), _fake(),
+                                           4096, limit, None)
+        assert st == api.DSA_ERR_INVALID_ARG

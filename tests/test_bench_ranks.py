@@ -56,3 +56,16 @@ def test_single_rank_is_plain_throughput():
     import bench
     value, ms = bench.aggregate(64, 0.5, 1)
     assert ms == 0.5 and value == pytest.approx(64 / 0.0005)
+
+
+def test_oracle_sampler_visits_every_stratified_point_in_a_seeded_order():
+    import bench
+    from sparse_attention_long_11_b300 import inputs
+    wl = inputs.make_tiny(seed=0, L=64, topk=16)
+    a, b = bench.OracleSampler(wl, points=16, seed=3), bench.OracleSampler(wl, points=16, seed=3)
+    assert list(a.order) == list(b.order) and sorted(a.order) == sorted(set(a.order))
+    assert list(a.order) != sorted(a.order)                  # not ascending: any prefix mixes early and late rows
+    n1, _ = a.run(1e9, max_q=5)
+    n2, _ = a.run(1e9, max_q=11)                              # continues where the first call stopped
+    assert (n1, n2) == (5, 11)
+    assert sorted(a.visited) == sorted(int(wl.q_pos[i]) for i in a.order)

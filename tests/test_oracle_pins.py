@@ -319,12 +319,52 @@ def test_dsa_rows_before_k_equal_dense():
         assert len(set(idx.tolist())) == 32 and idx.min() >= 0 and idx.max() <= i
 
 
+def _hand_paged_workload():
+    """A paged cache written out by hand: block size 4, three sequences of 6,
+    9 and 3 positions, block table [[4, 1], [0, 5, 2], [3, 0]] (the last 0 is
+    padding past sequence 2's one block).  Row r of every cache tensor holds
+    the value r, so a decoded logical cache shows which physical row it read."""
+    bt = torch.tensor([[4, 1, 0], [0, 5, 2], [3, 0, 0]], dtype=torch.int32)
+    rows = 6 * 4
+    col = torch.arange(rows, dtype=torch.float32)[:, None]
+    q_seq = torch.tensor([0, 1, 2], dtype=torch.int32)
+    q_pos = torch.tensor([5, 8, 2], dtype=torch.int32)
+    return inputs.Workload(
+        name="hand_paged", seed=0, idx_dtype="f32", H_I=1, d_I=4,
+        q_idx=torch.ones((3, 1, 4)), q_scale=None, w=torch.ones((3, 1)),
+        k_idx=col.repeat(1, 4), k_scale=None, topk=4, attn_dtype="f32", H=8, d_qk=4, d_v=4,
+        q=torch.zeros((3, 8, 4)), kv=col.repeat(1, 4) + 0.5, softmax_scale=0.5,
+        q_seq=q_seq, q_pos=q_pos, seq_lens=[6, 9, 3], seq_stride=0,
+        block_table=bt, block_size=4, chunks=[(0, 3)])
+
+
+def test_paged_row_map_walked_by_hand():
+    # row(b, s) = block_table[b][s // 4] * 4 + s % 4, each value typed out
+    wl = _hand_paged_workload()
+    want = {
+        0: [16, 17, 18, 19, 4, 5],                       # blocks 4, 1
+        1: [0, 1, 2, 3, 20, 21, 22, 23, 8],              # blocks 0, 5, 2
+        2: [12, 13, 14],                                 # block 3
+    }
+    for b, rows in want.items():
+        assert wl.logical_rows(b, len(rows)).tolist() == rows, b
+    from oracle.workload_view import OracleView
+    view = OracleView(wl)
+    for b, rows in want.items():
+        k_vals, k_scale, kv = view.seq_cache(b, len(rows))
+        assert k_scale is None
+        assert k_vals[:, 0].tolist() == [float(r) for r in rows], b
+        assert kv[:, 0].tolist() == [r + 0.5 for r in rows], b
+
+
 def test_paged_view_reads_logical_rows():
-    # the mixed workload's block table is a permutation: the oracle view must
-    # see every sequence's rows in logical order
+    # the mixed workload's block table maps its sequences onto disjoint
+    # physical blocks that together are a permutation of the pool
     wl = inputs.make_mixed(seed=0, batch=3, lo=200, hi=300, prefill=40, decode=4, block=16, topk=16)
-    nblk = sum((c + 15) // 16 for c in wl.seq_lens)
-    assert sorted(wl.block_table[wl.block_table >= 0].unique().tolist()) == list(range(nblk)) or True
+    nblk = [(c + 15) // 16 for c in wl.seq_lens]
+    used = torch.cat([wl.block_table[b, :n] for b, n in enumerate(nblk)])
+    assert sorted(used.tolist()) == list(range(sum(nblk)))
+    assert wl.num_rows == sum(nblk) * 16
     rows = torch.cat([wl.logical_rows(b, c) for b, c in enumerate(wl.seq_lens)])
     assert rows.unique().numel() == rows.numel()            # no two logical rows share storage
     assert int(rows.max()) < wl.num_rows
