@@ -188,9 +188,12 @@ class Runner:
 
 
 def _pairs(wl):
-    """Algorithmic work of one step: (indexer causal pairs, selected attention pairs)."""
-    pos = wl.q_pos.to(torch.int64)
-    return int((pos + 1).sum()), int(torch.clamp(pos + 1, max=wl.topk).sum())
+    """Algorithmic work of one step: (indexer pairs, selected attention pairs).
+    A query at position t with t + 1 <= k selects all its t + 1 keys, so only
+    queries with t + 1 > k need indexer scores: the indexer's work is their
+    causal (query, key) pairs; attention has min(t + 1, k) pairs a query."""
+    n = wl.q_pos.to(torch.int64) + 1
+    return int(torch.where(n > wl.topk, n, torch.zeros_like(n)).sum()), int(torch.clamp(n, max=wl.topk).sum())
 
 
 def _time_steps(r: Runner, steps: int, warmup: int, ws: int, gpu: int, profile: bool = True):
@@ -283,12 +286,16 @@ def _roofline_decode(wl, per_stage, steps, peaks):
 
 def _decode_stage_roofline(wl, per_stage, steps, peaks):
     """HBM fraction of every decode stage: algorithmic bytes per launch (indexer:
-    the FP8 key rows and scales of every causal pair; top-k: the staged score
-    rows read and the index rows written; attention: the gathered latent rows
-    plus q read and O written) over its average launch time."""
+    the FP8 key rows and scales of every scored pair; top-k: the k candidate
+    keys a selecting query needs at the least, and the index rows written;
+    attention: the gathered latent rows plus q read and O written) over its
+    average launch time."""
     n_idx, n_attn = _pairs(wl)
+    n_sel = int((wl.q_pos.to(torch.int64) + 1 > wl.topk).sum())   # queries that select from more than k keys
     byts = {"indexer": n_idx * BYTES_PER_IDX_KEY,
-            "topk": n_idx * 4 + wl.num_q * wl.topk * 4,
+            # the streamed selection reads at least k candidates (8-byte keys) of
+            # each selecting query and writes every index row
+            "topk": n_sel * wl.topk * 8 + wl.num_q * wl.topk * 4,
             "attention": n_attn * BYTES_PER_ATTN_KEY + wl.num_q * wl.H * (wl.d_qk + wl.d_v) * 2}
     out = {}
     for name, (cnt, tot) in per_stage.items():

@@ -65,7 +65,7 @@ typedef enum {
   DSA_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
   DSA_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired (reported by dsa_check_device_error) */
   DSA_ERR_BOUNDS = 5,      /* device-side range check failed (reported by dsa_check_device_error) */
-  DSA_ERR_WORKSPACE = 6    /* workspace NULL, misaligned (256 B) or smaller than one staged row */
+  DSA_ERR_WORKSPACE = 6    /* workspace NULL, misaligned (256 B) or smaller than one stage of one row */
 } dsa_status;
 
 typedef enum { DSA_F32 = 0, DSA_BF16 = 1, DSA_FP8_E4M3 = 2 } dsa_dtype;
@@ -182,22 +182,45 @@ DSA_API dsa_status dsa_sparse_attn(const dsa_query_desc* qd, const dsa_cache_des
                            void* out, float* lse, dsa_stream_t stream);
 
 /* Recommended bytes of workspace for dsa_forward on this batch (0 if the
- * arguments are invalid): the score rows of all num_q queries, capped at
- * 1 GiB but never less than one row.  Depends only on the host-side fields (num_q, max_kv, k,
- * dtypes, shapes). */
+ * arguments are invalid): every query row in one stage, capped at 1 GiB.
+ * With the FP8 indexer (the streamed selection below) a row needs its
+ * sampled scores and candidate list, O(k + max_kv / 32) entries, not a score
+ * row; with fp32 indexer operands a row is one staged score row.  Depends
+ * only on the host-side fields (num_q, max_kv, k, dtypes, shapes). */
 DSA_API size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
                                   const dsa_attn_inputs* at);
 
+/* Bytes of workspace with which dsa_forward runs this batch in stages of at
+ * most stage_rows query rows (0 if the arguments are invalid or stage_rows <
+ * 1).  dsa_forward_workspace_size() is this for the recommended stage;
+ * stage_rows = 1 gives the least workspace dsa_forward accepts. */
+DSA_API size_t dsa_forward_stage_workspace_size(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
+                                                const dsa_attn_inputs* at, int64_t stage_rows);
+
 /* The whole hot path: indexer -> top-k -> sparse attention for a batch of
  * prefill chunks and/or decode tokens.  Writes idx [num_q, k] (the selected
- * positions, as dsa_topk would write them), out and lse (as dsa_sparse_attn).
+ * positions, exactly as dsa_topk would write them for dsa_index_scores'
+ * rows), out and lse (as dsa_sparse_attn).
+ *
+ * With FP8 indexer operands (the tensor-core indexer) the score rows are
+ * never written: the indexer first scores every m-th key tile of each query
+ * (at most 32 tiles a row), a per-query threshold is taken from those
+ * samples, the indexer then scores the other tiles and keeps only the keys at
+ * or above the threshold, and an exact selection runs on those candidates.
+ * A row whose threshold misses (too few keys above it, or more than its list
+ * holds: adversarial or heavily tied rows) is recomputed exactly by a
+ * fallback, with the same arithmetic, so every row's selection is exact and
+ * bitwise equal to dsa_topk on dsa_index_scores.  Otherwise (fp32 operands,
+ * or a paged cache whose block size is not a multiple of 64) the score rows
+ * are staged through the workspace.
+ *
  * workspace: 256-byte aligned, owned by the caller and not read before it is
  * written (no zeroing needed); it must not be used by other work while this
- * call's kernels run.  It holds the staged indexer scores: the queries run in
- * equal stages of as many score rows (max_kv rounded up to a multiple of 4,
- * times 4 bytes, each) as it holds.  One row is the least it may hold;
- * dsa_forward_workspace_size() gives the recommended size.  Any size gives the
- * same results; fewer, fuller stages run faster. */
+ * call's kernels run.  The queries run in equal stages of as many rows as it
+ * holds: dsa_forward_stage_workspace_size() gives the bytes for a stage size
+ * (1 row is the least; DSA_ERR_WORKSPACE below it) and
+ * dsa_forward_workspace_size() the recommended size.  Any size gives the same
+ * results; fewer, fuller stages run faster. */
 DSA_API dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd,
                        const dsa_indexer_inputs* ix, int32_t k, const dsa_attn_inputs* at,
                        int32_t* idx, void* out, float* lse,

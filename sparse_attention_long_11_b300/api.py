@@ -63,6 +63,8 @@ _SIGS = {
                                        ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "dsa_forward_workspace_size": (ctypes.c_size_t, [_P(QueryDesc), _P(IndexerInputs), ctypes.c_int32,
                                                      _P(AttnInputs)]),
+    "dsa_forward_stage_workspace_size": (ctypes.c_size_t, [_P(QueryDesc), _P(IndexerInputs), ctypes.c_int32,
+                                                           _P(AttnInputs), ctypes.c_int64]),
     "dsa_forward": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(IndexerInputs), ctypes.c_int32,
                                    _P(AttnInputs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -197,6 +199,12 @@ def dsa_sparse_attn(batch: QueryDesc, cache: CacheDesc, at: AttnInputs, idx: tor
 
 def dsa_forward_workspace_size(batch: QueryDesc, ix: IndexerInputs, k: int, at: AttnInputs) -> int:
     return int(lib().dsa_forward_workspace_size(ctypes.byref(batch), ctypes.byref(ix), k, ctypes.byref(at)))
+
+
+def dsa_forward_stage_workspace_size(batch: QueryDesc, ix: IndexerInputs, k: int, at: AttnInputs,
+                                     stage_rows: int) -> int:
+    return int(lib().dsa_forward_stage_workspace_size(ctypes.byref(batch), ctypes.byref(ix), k, ctypes.byref(at),
+                                                      int(stage_rows)))
 
 
 def dsa_forward(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, k: int, at: AttnInputs,

@@ -189,6 +189,130 @@ dsa_status run_staged(const dsa_query_desc* qd, const dsa_cache_desc* cd, const 
       launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
 }
 
+// ---- The fused forward: the selection streams out of the indexer, so no
+// score row is written (select.cu).  Workspace of one stage of `rows` query
+// rows: sampled scores, thresholds, candidate counts and lists, the fallback
+// queue, and one fallback score row per fallback CTA.
+struct FusedLayout {
+  SelectPlan plan;
+  int64_t ld = 0;          // fallback score row length (floats)
+  int64_t rows = 0;
+  int fb_grid = 0;
+  size_t samp = 0, thr = 0, cnt = 0, fail_rows = 0, ctr = 0, cand = 0, slots = 0, total = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+FusedLayout fused_layout(int64_t rows, int fb_grid, int max_kv, int k) {
+  FusedLayout L;
+  L.plan = plan_select(max_kv, k);
+  L.ld = score_ld(max_kv);
+  L.rows = rows;
+  L.fb_grid = fb_grid;
+  size_t off = 0;
+  L.samp = off;      off += align256((size_t)rows * L.plan.lds * sizeof(float));
+  L.thr = off;       off += align256((size_t)rows * sizeof(uint64_t));
+  L.cnt = off;       off += align256((size_t)rows * sizeof(uint32_t));
+  L.fail_rows = off; off += align256((size_t)rows * sizeof(uint32_t));
+  L.ctr = off;       off += 256;
+  L.cand = off;      off += align256((size_t)rows * L.plan.cap * sizeof(uint64_t));
+  L.slots = off;     off += align256((size_t)fb_grid * L.ld * sizeof(float));
+  L.total = off;
+  return L;
+}
+
+bool fused_supported(const dsa_cache_desc* cd, const dsa_indexer_inputs* ix) {
+  return indexer_tc_supported(to_map(cd), *ix);
+}
+
+// The most rows per stage that `bytes` hold with fb_grid fallback rows (0 if
+// not even one).
+int64_t fused_rows_fitting(size_t bytes, int fb_grid, int max_kv, int k, int64_t num_q) {
+  const FusedLayout one = fused_layout(1, fb_grid, max_kv, k);
+  if (one.total > bytes) return 0;
+  const size_t per = (size_t)one.plan.lds * 4 + 8 + 4 + 4 + (size_t)one.plan.cap * 8;
+  const size_t fixed = align256((size_t)fb_grid * one.ld * 4) + 256 + 6 * 256;
+  int64_t r = bytes > fixed ? (int64_t)((bytes - fixed) / per) : 1;
+  r = std::max<int64_t>(1, std::min<int64_t>(r, num_q));
+  while (r > 1 && fused_layout(r, fb_grid, max_kv, k).total > bytes) --r;
+  return r;
+}
+
+dsa_status run_fused(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix, int32_t k,
+                     const dsa_attn_inputs* at, int32_t* idx, void* out, float* lse, void* workspace, size_t ws_bytes,
+                     int* err, cudaStream_t st) {
+  const CacheMap cm = to_map(cd);
+  int fb = sel_fallback_grid(qd->num_q);
+  int64_t max_rows = fused_rows_fitting(ws_bytes, fb, qd->max_kv, k, qd->num_q);
+  if (max_rows == 0) {   // a small workspace: one fallback row
+    fb = 1;
+    max_rows = fused_rows_fitting(ws_bytes, fb, qd->max_kv, k, qd->num_q);
+    if (max_rows == 0) return DSA_ERR_WORKSPACE;
+  }
+  const int64_t stages = (qd->num_q + max_rows - 1) / max_rows;
+  const int64_t rows = (qd->num_q + stages - 1) / stages;   // equal stages
+  const FusedLayout L = fused_layout(rows, fb, qd->max_kv, k);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  float* samp = reinterpret_cast<float*>(base + L.samp);
+  uint64_t* thr = reinterpret_cast<uint64_t*>(base + L.thr);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(base + L.cnt);
+  uint32_t* fail_rows = reinterpret_cast<uint32_t*>(base + L.fail_rows);
+  uint32_t* ctr = reinterpret_cast<uint32_t*>(base + L.ctr);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(base + L.cand);
+  float* slots = reinterpret_cast<float*>(base + L.slots);
+  const size_t qi_row = (size_t)ix->heads * ix->dim * idx_elem_size(ix);
+  for (int64_t r0 = 0; r0 < qd->num_q; r0 += rows) {
+    const int n = (int)std::min<int64_t>(rows, qd->num_q - r0);
+    QueryBatch qb{qd->q_seq + r0, qd->q_pos + r0, n, qd->max_kv};
+    dsa_indexer_inputs sub = *ix;
+    sub.q = static_cast<const uint8_t*>(ix->q) + r0 * qi_row;
+    sub.w = ix->w + r0 * ix->heads;
+    if (ix->q_scale) sub.q_scale = ix->q_scale + r0 * ix->heads;
+    int32_t* idx_s = idx + r0 * k;
+    IndexerOut so;
+    so.mode = IndexerOut::kSample;
+    so.m = L.plan.m;
+    so.min_pos = k;
+    so.scores = samp;
+    so.ld = L.plan.lds;
+    cudaError_t e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer_tc(qb, cm, sub, so, err, st); });
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    e = launch(DSA_STAGE_TOPK, st, [&] { return launch_sel_threshold(qb, L.plan, samp, k, thr, cnt, ctr, st); });
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    if (L.plan.m > 1) {   // with m = 1 every tile was sampled
+      IndexerOut fo;
+      fo.mode = IndexerOut::kFilter;
+      fo.m = L.plan.m;
+      fo.min_pos = k;
+      fo.thr = thr;
+      fo.cnt = cnt;
+      fo.cand = cand;
+      fo.cap = L.plan.cap;
+      e = launch(DSA_STAGE_INDEXER, st, [&] { return launch_indexer_tc(qb, cm, sub, fo, err, st); });
+      if (e != cudaSuccess) return DSA_ERR_CUDA;
+    }
+    e = launch(DSA_STAGE_TOPK, st, [&] {
+      return launch_sel_select(qb, L.plan, samp, k, thr, cnt, cand, idx_s, ctr, fail_rows, err, st);
+    });
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    e = launch(DSA_STAGE_TOPK, st, [&] {
+      return launch_sel_fallback(qb, cm, sub, k, idx_s, slots, L.ld, L.fb_grid, ctr, fail_rows, err, st);
+    });
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  return cuda_status(
+      launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
+}
+
+// Recommended bytes of the fused forward: every row of the call in one
+// stage, up to kStageBytes.
+size_t fused_workspace_size(const dsa_query_desc* qd, int32_t k) {
+  const int fb = sel_fallback_grid(qd->num_q);
+  int64_t r = fused_rows_fitting(kStageBytes, fb, qd->max_kv, k, qd->num_q);
+  if (r == 0) r = 1;
+  return fused_layout(r, fb, qd->max_kv, k).total;
+}
+
 }  // namespace
 }  // namespace dsa
 
@@ -261,8 +385,20 @@ size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_indexer_in
   if (check_query(qd) != DSA_OK || check_indexer(ix) != DSA_OK || check_attn(at) != DSA_OK) return 0;
   if (k < 1 || k > kMaxTopk) return 0;
   if (qd->num_q == 0) return 256;
+  if (indexer_tc_supported(CacheMap{}, *ix)) return fused_workspace_size(qd, k);
   size_t bytes = (size_t)stage_rows(qd->num_q, qd->max_kv) * score_ld(qd->max_kv) * sizeof(float);
   return (bytes + 255) & ~size_t(255);
+}
+
+size_t dsa_forward_stage_workspace_size(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
+                                        const dsa_attn_inputs* at, int64_t stage_rows) {
+  if (check_query(qd) != DSA_OK || check_indexer(ix) != DSA_OK || check_attn(at) != DSA_OK) return 0;
+  if (k < 1 || k > kMaxTopk || stage_rows < 1) return 0;
+  if (qd->num_q == 0) return 256;
+  const int64_t r = std::min<int64_t>(stage_rows, qd->num_q);
+  if (indexer_tc_supported(CacheMap{}, *ix))   // one fallback score row per stage row, up to one per fallback CTA
+    return fused_layout(r, (int)std::min<int64_t>(sel_fallback_grid(qd->num_q), r), qd->max_kv, k).total;
+  return align256((size_t)r * score_ld(qd->max_kv) * sizeof(float));
 }
 
 dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix, int32_t k,
@@ -275,11 +411,15 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const
   DSA_TRY(check_indexer(ix));
   DSA_TRY(check_attn(at));
   if (!idx || !out || !lse || !aligned(idx, 4) || !aligned(out, 16) || !aligned(lse, 4)) return DSA_ERR_INVALID_ARG;
-  const size_t row_bytes = (size_t)score_ld(qd->max_kv) * sizeof(float);   // the least: one staged row
-  if (!workspace || !aligned(workspace, 256) || workspace_bytes < row_bytes) return DSA_ERR_WORKSPACE;
+  if (!workspace || !aligned(workspace, 256)) return DSA_ERR_WORKSPACE;
+  const bool fused = fused_supported(cd, ix);
+  // the least workspace: one stage of one row (and one fallback row)
+  const size_t least = fused ? fused_layout(1, 1, qd->max_kv, k).total : (size_t)score_ld(qd->max_kv) * sizeof(float);
+  if (workspace_bytes < least) return DSA_ERR_WORKSPACE;
   int* err = device_error_ptr();
   if (!err) return DSA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (fused) return run_fused(qd, cd, ix, k, at, idx, out, lse, workspace, workspace_bytes, err, st);
 
   const int64_t rows = (int64_t)(workspace_bytes / (score_ld(qd->max_kv) * sizeof(float)));
   return run_staged(qd, cd, ix, k, at, idx, out, lse, static_cast<float*>(workspace), rows, err, st);

@@ -261,7 +261,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
           s_e1 = e1 < k ? __ldg(irow + e1) : -1;
         }
         ATTN_TRACE(grp, gt, 0, lane == 0 && q4 == 0);
-        if (!(ok = mbar_wait(&B.s_full[grp], par, abort))) break;
+        if (!(ok = mbar_wait_warp(&B.s_full[grp], par, abort))) break;
         tc_fence_after();
         // own partial logits in base-2 units (fp32); the peer gets them rounded to fp16
         float x[64];
@@ -282,7 +282,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         mbar_arrive(&B.s_empty[grp]);   // S(gt+2) may be computed into this buffer
         ATTN_TRACE(grp, gt, 1, lane == 0 && q4 == 0);
         // own partial -> the peer's X[grp], once the peer has consumed what we wrote there two tiles ago
-        if (!(ok = mbar_wait<true>(&B.xe[grp], par ^ 1, abort))) break;
+        if (!(ok = mbar_wait_warp<true>(&B.xe[grp], par ^ 1, abort))) break;
 #pragma unroll
         for (int jq = 0; jq < 8; ++jq)
           st_async_v4_b32(x_peer + (uint32_t)(jq * 128 + h) * 16u,
@@ -290,7 +290,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
                                      f16x2_sat(x[8 * jq + 4], x[8 * jq + 5]), f16x2_sat(x[8 * jq + 6], x[8 * jq + 7])),
                           xf_peer);
         ATTN_TRACE(grp, gt, 2, lane == 0 && q4 == 0);
-        if (!(ok = mbar_wait<true>(&B.xf[grp], par, abort))) break;   // the peer's partial is in X[grp]
+        if (!(ok = mbar_wait_warp<true>(&B.xf[grp], par, abort))) break;   // the peer's partial is in X[grp]
         // arm the next phase: the peer writes X[grp] again only after all of
         // this group has read it and said so (below)
         if (gtid == 0) mbar_arrive_expect_tx(&B.xf[grp], kXBytes);
@@ -339,7 +339,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         // tile keeps the two groups within one tile of each other)
         float m_prev = -INFINITY;
         if (gt > 0) {
-          if (!(ok = mbar_wait(&B.mdone[grp ^ 1], ((gt - 1) >> 1) & 1, abort))) break;
+          if (!(ok = mbar_wait_warp(&B.mdone[grp ^ 1], ((gt - 1) >> 1) & 1, abort))) break;
           if (t > 0) m_prev = B.mpub[grp ^ 1][h];
         }
         // lazy rescaling: the maximum used only moves when exceeded by more than 8 (a factor 256)
@@ -368,11 +368,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
           l += (a.x + a.y) + (b2.x + b2.y);
         }
         ATTN_TRACE(grp, gt, 4, lane == 0 && q4 == 0);
-        if (t > 0 && m_use != m_prev) {
+        // The heads of a warp decide separately whether their maximum moved,
+        // but the TMEM loads and stores are warp-collective: the warp rescales
+        // when any of its heads needs it, the others by exactly 1.
+        const bool rescale = t > 0 && m_use != m_prev;
+        if (__any_sync(0xffffffffu, rescale)) {
           // O holds the P.V of tiles < gt relative to m_prev; that of tile gt-1 must be complete
-          if (!(ok = mbar_wait(&B.pv_done[grp ^ 1], ((gt - 1) >> 1) & 1, abort))) break;
+          if (!(ok = mbar_wait_warp(&B.pv_done[grp ^ 1], ((gt - 1) >> 1) & 1, abort))) break;
           tc_fence_after();
-          const float alpha = ex2_approx(m_prev - m_use);
+          const float alpha = rescale ? ex2_approx(m_prev - m_use) : 1.f;
 #pragma unroll 1
           for (int c = 0; c < 256; c += 16) {
             uint32_t r[16];
@@ -385,7 +389,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         }
         // P -> shared memory (SW128, row = head); P[grp] is free once the
         // P.V of tile gt-2 has completed
-        if (!(ok = mbar_wait(&B.pv_done[grp], par ^ 1, abort))) break;
+        if (!(ok = mbar_wait_warp(&B.pv_done[grp], par ^ 1, abort))) break;
         {
           uint8_t* prow = sm + kOffP + grp * kPBytes;
 #pragma unroll
@@ -406,12 +410,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       B.lsum[qb2][grp][h] = l;
       B.mseen[qb2][grp][h] = m_seen;
       mbar_arrive(&B.qend);
-      if (!mbar_wait(&B.qend, qb2, abort)) break;
+      if (!mbar_wait_warp(&B.qend, qb2, abort)) break;
       const float ma = B.mseen[qb2][0][h], mb = B.mseen[qb2][1][h];
       const float mf = fmaxf(ma, mb);
       const float lt = mf == -INFINITY ? 0.f
                                        : B.lsum[qb2][0][h] * ex2_approx(ma - mf) + B.lsum[qb2][1][h] * ex2_approx(mb - mf);
-      if (!mbar_wait(&B.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort)) break;
+      if (!mbar_wait_warp(&B.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort)) break;
       tc_fence_after();
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       uint4* o4 = reinterpret_cast<uint4*>(orow);
@@ -451,7 +455,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       const int seq = __ldg(qb.q_seq + i);
       const int32_t* irow = idx + (int64_t)i * k;
       // Q of this query: every S MMA of the previous query has completed
-      if (q_writer && !mbar_wait(&B.q_empty, (qv & 1) ^ 1, abort)) break;
+      if (q_writer && !mbar_wait_warp(&B.q_empty, (qv & 1) ^ 1, abort)) break;
       if (warp == 8 && lane == 0) {
         mbar_arrive_expect_tx(&B.q_rope, kQRopeBytes);
         tma_load_2d(sQr, &tm_q_rope, 512 + 32 * crank, i * kH, &B.q_rope);
@@ -529,7 +533,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
           uint2 ca[8], cb[8], cr[4];
           load8(0, ca);
           load8(8, cb);
-          if (!(ok = mbar_wait(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
+          if (!(ok = mbar_wait_warp(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
           ATTN_TRACE(2, g, 1 + 3 * wg, lane == 0);
           store8(0, ca);
           load8(16, ca);
@@ -553,7 +557,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
           ATTN_TRACE(2, g, 2 + 3 * wg, lane == 0);
           continue;
         }
-        if (!(ok = mbar_wait(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
+        if (!(ok = mbar_wait_warp(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
         ATTN_TRACE(2, g, 1 + 3 * wg, lane == 0);
         int row = -1;                                         // physical rows fit in 31 bits
         if (s_e >= 0 && s_e <= qi.pos) row = (int)cache_row(cm, seq, s_e, err);
@@ -605,14 +609,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       const QueryInfo qi = query_info(qb, idx, k, i, pv);
       const int nt = qi.nt;
       if (nt == 0) continue;
-      if (!mbar_wait(&B.q_full, qv & 1, abort) || !mbar_wait(&B.q_rope, qv & 1, abort)) break;
+      if (!mbar_wait_warp(&B.q_full, qv & 1, abort) || !mbar_wait_warp(&B.q_rope, qv & 1, abort)) break;
       bool ok = true;
       for (int t = 0; t < nt; ++t, ++g) {
         const uint32_t st = g % kStages, sb = g & 1;
         ATTN_TRACE(3, g, 0, lane == 0);
-        if (!(ok = mbar_wait(&B.kv_full[st], (g / kStages) & 1, abort))) break;
+        if (!(ok = mbar_wait_warp(&B.kv_full[st], (g / kStages) & 1, abort))) break;
         ATTN_TRACE(3, g, 1, lane == 0);
-        if (!(ok = mbar_wait(&B.s_empty[sb], ((g >> 1) & 1) ^ 1, abort))) break;
+        if (!(ok = mbar_wait_warp(&B.s_empty[sb], ((g >> 1) & 1) ^ 1, abort))) break;
         ATTN_TRACE(3, g, 2, lane == 0);
         tc_fence_after();
         if (lane == 0) {
@@ -652,10 +656,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       bool ok = true;
       for (int t = 0; t < nt; ++t, ++g) {
         ATTN_TRACE(3, g, 3, lane == 0);
-        if (!(ok = mbar_wait(&B.p_full[g & 1], (g >> 1) & 1, abort))) break;
+        if (!(ok = mbar_wait_warp(&B.p_full[g & 1], (g >> 1) & 1, abort))) break;
         ATTN_TRACE(3, g, 4, lane == 0);
         // the epilogue of the previous query has read O
-        if (t == 0 && !(ok = mbar_wait(&B.o_empty, (qv & 1) ^ 1, abort))) break;
+        if (t == 0 && !(ok = mbar_wait_warp(&B.o_empty, (qv & 1) ^ 1, abort))) break;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t skv = sKV + (g % kStages) * kKVStageBytes;

@@ -73,6 +73,15 @@ __device__ __forceinline__ uint32_t score_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// 64-bit selection key of a (score, position) pair: the score's key in the
+// high word, the complement of the position in the low word.  Larger means
+// selected first: higher score, then lower position; the keys of one row
+// are all distinct, so "the k largest keys" is a unique set.
+__device__ __forceinline__ uint64_t composite_key(float x, int pos) {
+  return ((uint64_t)score_key(x) << 32) | (uint64_t)(0xffffffffu - (uint32_t)pos);
+}
+__device__ __forceinline__ int composite_pos(uint64_t c) { return (int)(0xffffffffu - (uint32_t)c); }
+
 __device__ __forceinline__ float2 fp8x2_e4m3_to_float2(uint16_t v) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
   return __half22float2(*reinterpret_cast<__half2*>(&h));

@@ -1,0 +1,71 @@
+// The lightning indexer's epilogue arithmetic, shared by every kernel that
+// turns a tcgen05 accumulator row into a score: the tensor-core indexer and
+// the fused selection's fallback.  A (key, query) pair's 64 raw head dots sit
+// in one thread's TMEM row; the score is
+//   sum_j (w[t,j] sq[t,j]) * ReLU(<q8[t,j,:], k8[s,:]>)
+// added as four 16-head partials in the fixed order (P0 + P1) + (P2 + P3), so
+// every kernel that uses this function produces the same bits for a pair.
+#pragma once
+
+#include <stdint.h>
+
+#include "tc.cuh"
+
+namespace dsa {
+namespace idx_epi {
+
+// Two fp32 lanes in one 64-bit register pair, and d = a * b + c on both
+// lanes with one packed instruction (PTX fma.rn.f32x2).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// Weighted ReLU sum over 16 heads: r[i] is the raw dot of head h0 + i,
+// w4[0..3] the folded weights of those heads.  Two packed accumulators
+// (heads 4m, 4m+1 and 4m+2, 4m+3), added at the end.
+__device__ __forceinline__ float head_partial(const uint32_t (&r)[16], const float4* w4) {
+  uint64_t a = 0ull, b = 0ull;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const float4 wv = w4[m];
+    a = ffma2(pack2(wv.x, wv.y),
+              pack2(fmaxf(__uint_as_float(r[4 * m]), 0.f), fmaxf(__uint_as_float(r[4 * m + 1]), 0.f)), a);
+    b = ffma2(pack2(wv.z, wv.w),
+              pack2(fmaxf(__uint_as_float(r[4 * m + 2]), 0.f), fmaxf(__uint_as_float(r[4 * m + 3]), 0.f)), b);
+  }
+  float alo, ahi, blo, bhi;
+  unpack2(a, alo, ahi);
+  unpack2(b, blo, bhi);
+  return (alo + ahi) + (blo + bhi);
+}
+
+// Weighted head sum of the 64 TMEM columns starting at taddr (this thread's
+// lane), with the folded weights wq4[0..15] (heads 0..63): two pairs of
+// 16-column loads, four 16-head partials, (P0 + P1) + (P2 + P3).  Called by a
+// whole warp (tcgen05.ld is warp-collective).
+__device__ __forceinline__ float head_sum64(uint32_t taddr, const float4* wq4) {
+  float P[4];
+#pragma unroll
+  for (int uh = 0; uh < 2; ++uh) {
+    uint32_t r[2][16];
+    tc::tmem_ld16(taddr + 32 * uh, r[0]);
+    tc::tmem_ld16(taddr + 32 * uh + 16, r[1]);
+    tc::tmem_ld_wait();
+    P[2 * uh] = head_partial(r[0], wq4 + 8 * uh);
+    P[2 * uh + 1] = head_partial(r[1], wq4 + 8 * uh + 4);
+  }
+  return (P[0] + P[1]) + (P[2] + P[3]);
+}
+
+}  // namespace idx_epi
+}  // namespace dsa

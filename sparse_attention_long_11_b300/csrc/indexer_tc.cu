@@ -36,6 +36,7 @@
 #include <cstdint>
 #include <cstddef>
 
+#include "indexer_epi.cuh"
 #include "launch.h"
 #include "tc.cuh"
 #include "tmap.h"
@@ -80,6 +81,20 @@ __device__ long long g_idx_trace[3][1024][4];
   } while (0)
 #endif
 
+// Which key tiles a launch processes (IndexerOut::mode): every tile (kFull),
+// the sampled tiles 0, m, 2m, ... (kSample), or all the others (kFilter).
+// A pass's tiles are numbered by ordinal o = 0, 1, ...; tile(o) maps an
+// ordinal to its key tile.
+struct TileMap {
+  int mode, m;
+  __device__ __forceinline__ int count(int T) const {
+    return mode == IndexerOut::kFull ? T : mode == IndexerOut::kSample ? (T + m - 1) / m : T - (T + m - 1) / m;
+  }
+  __device__ __forceinline__ int tile(int o) const {
+    return mode == IndexerOut::kFull ? o : mode == IndexerOut::kSample ? o * m : (o / (m - 1)) * m + 1 + o % (m - 1);
+  }
+};
+
 // One group of 4 consecutive query rows: either one pass over a shared
 // sequence (uniform) or one pass per active query.
 struct Group {
@@ -87,10 +102,11 @@ struct Group {
   bool active[kQG];
   bool uniform;
   int npass;
-  int pass_q[kQG], pass_seq[kQG], pass_T[kQG], pass_maxpos[kQG];
+  int pass_q[kQG], pass_seq[kQG], pass_T[kQG], pass_N[kQG], pass_maxpos[kQG];   // T tiles, N ordinals
 };
 
-__device__ __forceinline__ void describe_group(const QueryBatch& qb, const CacheMap& cm, int gi, Group& G) {
+__device__ __forceinline__ void describe_group(const QueryBatch& qb, const CacheMap& cm, int gi, int min_pos,
+                                               const TileMap& tm, Group& G) {
   int first_seq = -1, nact = 0;
   bool same = true;
 #pragma unroll
@@ -101,7 +117,7 @@ __device__ __forceinline__ void describe_group(const QueryBatch& qb, const Cache
     if (r < qb.num_q) {
       sq = __ldg(qb.q_seq + r);
       ps = __ldg(qb.q_pos + r);
-      act = ps >= 0 && ps < qb.max_kv && sq >= 0 && sq < cm.num_seqs;
+      act = ps >= min_pos && ps < qb.max_kv && sq >= 0 && sq < cm.num_seqs;
     }
     G.seq[qq] = sq;
     G.pos[qq] = ps;
@@ -136,12 +152,14 @@ __device__ __forceinline__ void describe_group(const QueryBatch& qb, const Cache
     }
   }
   G.npass = np;
+#pragma unroll
+  for (int p = 0; p < kQG; ++p) G.pass_N[p] = p < np ? tm.count(G.pass_T[p]) : 0;
 }
 
-// Tiles of pass p in chunk c: [t0, t1).
+// Ordinals of pass p in chunk c: [t0, t1).
 __device__ __forceinline__ void pass_range(const Group& G, int p, int c, int ch, int& t0, int& t1) {
   t0 = c * ch;
-  t1 = min(t0 + ch, G.pass_T[p]);
+  t1 = min(t0 + ch, G.pass_N[p]);
 }
 
 // Entry e of an item (its tiles in pass order) -> pass and tile.
@@ -171,46 +189,34 @@ __device__ __forceinline__ int item_tiles(const Group& G, int c, int ch) {
   return n;
 }
 
-// Two fp32 lanes in one 64-bit register pair, and d = a * b + c on both
-// lanes with one packed instruction (PTX fma.rn.f32x2).
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-
-// Weighted ReLU sum over 16 heads: r[i] is the raw score of head h0 + i,
-// w4[0..3] the folded weights of those heads.  Two packed accumulators
-// (heads 4m, 4m+1 and 4m+2, 4m+3), added at the end.
-__device__ __forceinline__ float head_partial(const uint32_t (&r)[16], const float4* w4) {
-  uint64_t a = 0ull, b = 0ull;
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const float4 wv = w4[m];
-    a = ffma2(pack2(wv.x, wv.y),
-              pack2(fmaxf(__uint_as_float(r[4 * m]), 0.f), fmaxf(__uint_as_float(r[4 * m + 1]), 0.f)), a);
-    b = ffma2(pack2(wv.z, wv.w),
-              pack2(fmaxf(__uint_as_float(r[4 * m + 2]), 0.f), fmaxf(__uint_as_float(r[4 * m + 3]), 0.f)), b);
+// Output of one (key, query) score, by mode.  Called by a whole warp (the
+// filter appends with a warp ballot): row_q, t (the tile's ordinal) and thr
+// are warp-uniform, s is this lane's key, live whether it is a causal key of
+// a valid query with a readable cache row.
+__device__ __forceinline__ void emit(const IndexerOut& o, const QueryBatch& qb, int row_q, int t, int s, float sc,
+                                     bool live, uint64_t thr, int lane) {
+  if (o.mode == IndexerOut::kFull) {
+    if (s < qb.max_kv && row_q < qb.num_q) o.scores[(int64_t)row_q * o.ld + s] = live ? sc : -INFINITY;
+  } else if (o.mode == IndexerOut::kSample) {
+    if (row_q < qb.num_q) o.scores[(int64_t)row_q * o.ld + t * kKT + (s & (kKT - 1))] = live ? sc : -INFINITY;
+  } else {
+    const uint64_t ck = composite_key(sc, s);
+    const bool admit = live && row_q < qb.num_q && ck >= thr;
+    const uint32_t m = __ballot_sync(0xffffffffu, admit);
+    if (m) {
+      uint32_t base = 0;
+      if (lane == 0) base = atomicAdd(o.cnt + row_q, (uint32_t)__popc(m));
+      base = __shfl_sync(0xffffffffu, base, 0) + __popc(m & ((1u << lane) - 1u));
+      if (admit && base < (uint32_t)o.cap) o.cand[(int64_t)row_q * o.cap + base] = ck;
+    }
   }
-  float alo, ahi, blo, bhi;
-  unpack2(a, alo, ahi);
-  unpack2(b, blo, bhi);
-  return (alo + ahi) + (blo + bhi);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   QueryBatch qb, CacheMap cm, const float* __restrict__ q_scale, const float* __restrict__ w,
-                  const float* __restrict__ k_scale, float* __restrict__ scores, int64_t ld, int ngroups,
-                  int nchunk, int ch, long long wait_limit, int* err) {
+                  const float* __restrict__ k_scale, const IndexerOut out, int ngroups, int nchunk, int ch,
+                  long long wait_limit, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ Shared S;
@@ -218,6 +224,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   volatile int* abort = &S.abort;
   const uint32_t sB = smem_u32(sm), sA = smem_u32(sm + kOffA);
   const int n_items = ngroups * nchunk;
+  const TileMap tmap{out.mode, out.m};
+  float* __restrict__ scores = out.scores;
+  const int64_t ld = out.ld;
 
   if (tid == 0) {
     for (int s = 0; s < kStagesA; ++s) {
@@ -253,7 +262,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
         const int gi = item % ngroups, c = item / ngroups;
         Group G;
-        describe_group(qb, cm, gi, G);
+        describe_group(qb, cm, gi, out.min_pos, tmap, G);
         if (item_tiles(G, c, ch) == 0) continue;
         const int bb = j & 1;
         if (!mbar_wait(&S.b_empty[bb], ((j >> 1) & 1) ^ 1, abort, wait_limit)) break;
@@ -272,8 +281,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             IDX_TRACE(0, g, 1, true);
             int64_t rows[2];
             uint32_t bytes = 0;
+            const int tile = tmap.tile(t);
             for (int hh = 0; hh < 2; ++hh) {
-              const int sh = t * kKT + 64 * hh;
+              const int sh = tile * kKT + 64 * hh;
               rows[hh] = -1;
               if (sh > mp) continue;
               if (cm.block_size == 0) {
@@ -314,10 +324,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
       const int gi = item % ngroups, c = item / ngroups;
       Group G;
-      describe_group(qb, cm, gi, G);
+      describe_group(qb, cm, gi, out.min_pos, tmap, G);
       if (item_tiles(G, c, ch) == 0) continue;
       const int bb = j & 1;
-      if (!mbar_wait(&S.b_full[bb], (j >> 1) & 1, abort, wait_limit)) break;
+      if (!mbar_wait_warp(&S.b_full[bb], (j >> 1) & 1, abort, wait_limit)) break;
       bool ok = true;
       // One accumulator buffer holds one shared-pass tile (4 queries x 64
       // heads) or up to four consecutive per-query tiles (64 columns each),
@@ -332,9 +342,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int t = t0; t < t1; ++t, ++g, ++dq) {
           const int st = g % kStagesA, b = dq & 1;
           IDX_TRACE(1, g, 0, lane == 0);
-          if (!(ok = mbar_wait(&S.a_full[st], (g / kStagesA) & 1, abort, wait_limit))) break;
+          if (!(ok = mbar_wait_warp(&S.a_full[st], (g / kStagesA) & 1, abort, wait_limit))) break;
           IDX_TRACE(1, g, 1, lane == 0);
-          if (!(ok = mbar_wait(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort, wait_limit))) break;
+          if (!(ok = mbar_wait_warp(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort, wait_limit))) break;
           IDX_TRACE(1, g, 2, lane == 0);
           tc_fence_after();
           if (lane == 0) {
@@ -350,14 +360,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       for (int e0 = 0; e0 < ne && ok && !uni; e0 += per_d, ++dq) {
         const int b = dq & 1, nsub = min(per_d, ne - e0);
-        if (!(ok = mbar_wait(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort, wait_limit))) break;
+        if (!(ok = mbar_wait_warp(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort, wait_limit))) break;
         for (int u = 0; u < nsub; ++u, ++g) {
           int p, t;
           entry_at(G, c, ch, e0 + u, p, t);
           const uint32_t boff = bb * kBBytes + (uni ? 0u : (uint32_t)G.pass_q[p] * (kHI * 128));
           const int st = g % kStagesA;
           IDX_TRACE(1, g, 0, lane == 0);
-          if (!(ok = mbar_wait(&S.a_full[st], (g / kStagesA) & 1, abort, wait_limit))) break;
+          if (!(ok = mbar_wait_warp(&S.a_full[st], (g / kStagesA) & 1, abort, wait_limit))) break;
           IDX_TRACE(1, g, 1, lane == 0);
           tc_fence_after();
           if (lane == 0) {
@@ -389,7 +399,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
       const int gi = item % ngroups, c = item / ngroups;
       Group G;
-      describe_group(qb, cm, gi, G);
+      describe_group(qb, cm, gi, out.min_pos, tmap, G);
       if (item_tiles(G, c, ch) > 0) {
         const int bb = j & 1;
         {   // folded weights of this group (threads et < 256 fetch one each)
@@ -399,7 +409,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 r < qb.num_q ? __ldg(w + (int64_t)r * kHI + jj) * __ldg(q_scale + (int64_t)r * kHI + jj) : 0.f;
           }
           mbar_arrive(&S.epi_sync[bb]);
-          if (!mbar_wait(&S.epi_sync[bb], (j >> 1) & 1, abort, wait_limit)) break;
+          if (!mbar_wait_warp(&S.epi_sync[bb], (j >> 1) & 1, abort, wait_limit)) break;
         }
         bool ok = true;
         const bool uni = G.uniform;
@@ -411,10 +421,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const bool q_act = G.active[uq];
           const int q_pos = G.pos[uq], row_q = gi * kQG + uq;
           const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][uq]);
+          const uint64_t thr = out.mode == IndexerOut::kFilter && row_q < qb.num_q ? __ldg(out.thr + row_q) : 0ull;
           for (int t = t0; t < t1; ++t, ++dq) {
             const int b = dq & 1;
             // this lane's key and its scale, fetched before the wait
-            const int s = t * kKT + qd * 32 + lane;
+            const int s = tmap.tile(t) * kKT + qd * 32 + lane;
             float sk = 0.f;
             bool key_ok = s <= maxpos;
             if (key_ok) {
@@ -423,24 +434,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               if (key_ok) sk = __ldg(k_scale + row);
             }
             IDX_TRACE(2, dq, 0, et == 0);
-            if (!(ok = mbar_wait(&S.d_full[b], (dq >> 1) & 1, abort, wait_limit))) break;
+            if (!(ok = mbar_wait_warp(&S.d_full[b], (dq >> 1) & 1, abort, wait_limit))) break;
             IDX_TRACE(2, dq, 1, et == 0);
             tc_fence_after();
-            float P[4];
-#pragma unroll
-            for (int uh = 0; uh < 2; ++uh) {   // two 16-column loads at a time
-              uint32_t r[2][16];
-              tmem_ld16(tmem + lane_base + 256 * b + uq * 64 + 32 * uh, r[0]);
-              tmem_ld16(tmem + lane_base + 256 * b + uq * 64 + 32 * uh + 16, r[1]);
-              tmem_ld_wait();
-              P[2 * uh] = head_partial(r[0], wq4 + 8 * uh);
-              P[2 * uh + 1] = head_partial(r[1], wq4 + 8 * uh + 4);
-            }
-            const float acc = (P[0] + P[1]) + (P[2] + P[3]);
-            if (s < qb.max_kv && row_q < qb.num_q) {
-              const bool live = q_act && key_ok && s <= q_pos;
-              scores[(int64_t)row_q * ld + s] = live ? acc * sk : -INFINITY;
-            }
+            const float acc = idx_epi::head_sum64(tmem + lane_base + 256 * b + uq * 64, wq4);
+            emit(out, qb, row_q, t, s, acc * sk, q_act && key_ok && s <= q_pos, thr, lane);
             tc_fence_before();
             mbar_arrive(&S.d_empty[b]);
             IDX_TRACE(2, dq, 2, et == 0);
@@ -456,7 +454,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const int qq = uni ? uq : G.pass_q[p];
           // this lane's key and its scale, fetched before the wait so that
           // the load (from HBM when every key is read once) overlaps the MMA
-          const int s = t * kKT + qd * 32 + lane;
+          const int s = tmap.tile(t) * kKT + qd * 32 + lane;
+          const int row_q = gi * kQG + qq;
+          const uint64_t thr =
+              out.mode == IndexerOut::kFilter && mine && row_q < qb.num_q ? __ldg(out.thr + row_q) : 0ull;
           float sk = 0.f;
           bool key_ok = mine && s <= G.pass_maxpos[p];
           if (key_ok) {
@@ -465,29 +466,15 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             if (key_ok) sk = __ldg(k_scale + row);
           }
           IDX_TRACE(2, dq, 0, et == 0);
-          if (!(ok = mbar_wait(&S.d_full[b], (dq >> 1) & 1, abort, wait_limit))) break;
+          if (!(ok = mbar_wait_warp(&S.d_full[b], (dq >> 1) & 1, abort, wait_limit))) break;
           IDX_TRACE(2, dq, 1, et == 0);
           tc_fence_after();
           if (mine) {
-            // four 16-head partials added as (P0 + P1) + (P2 + P3): the same
-            // arithmetic in both modes, so a query's scores do not depend on its batch
+            // the same arithmetic as the shared pass, so a query's scores do
+            // not depend on its batch
             const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][qq]);
-            float P[4];
-#pragma unroll
-            for (int uh = 0; uh < 2; ++uh) {   // two 16-column loads at a time
-              uint32_t r[2][16];
-              tmem_ld16(tmem + lane_base + 256 * b + uq * 64 + 32 * uh, r[0]);
-              tmem_ld16(tmem + lane_base + 256 * b + uq * 64 + 32 * uh + 16, r[1]);
-              tmem_ld_wait();
-              P[2 * uh] = head_partial(r[0], wq4 + 8 * uh);
-              P[2 * uh + 1] = head_partial(r[1], wq4 + 8 * uh + 4);
-            }
-            const float acc = (P[0] + P[1]) + (P[2] + P[3]);
-            const int row_q = gi * kQG + qq;
-            if (s < qb.max_kv && row_q < qb.num_q) {
-              const bool live = G.active[qq] && key_ok && s <= G.pos[qq];
-              scores[(int64_t)row_q * ld + s] = live ? acc * sk : -INFINITY;
-            }
+            const float acc = idx_epi::head_sum64(tmem + lane_base + 256 * b + uq * 64, wq4);
+            emit(out, qb, row_q, t, s, acc * sk, G.active[qq] && key_ok && s <= G.pos[qq], thr, lane);
           }
           tc_fence_before();
           mbar_arrive(&S.d_empty[b]);
@@ -498,7 +485,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       // the item holding a group's last chunk also writes -inf from the end
       // of the group's scanned tiles to max_kv
-      if (c == nchunk - 1) {
+      if (out.mode == IndexerOut::kFull && c == nchunk - 1) {
         for (int qq = 0; qq < kQG; ++qq) {
           const int row_q = gi * kQG + qq;
           if (row_q >= qb.num_q) break;
@@ -551,14 +538,15 @@ bool indexer_tc_supported(const CacheMap& cm, const dsa_indexer_inputs& ix) {
   return true;
 }
 
-cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix, float* scores,
-                              int64_t ld, int* err, cudaStream_t stream, long long wait_limit) {
+cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
+                              const IndexerOut& out, int* err, cudaStream_t stream, long long wait_limit) {
+  const int tmax = indexer_tile_count(out, (qb.max_kv + kKT - 1) / kKT);   // most tiles (ordinals) of one pass
+  if (tmax == 0 || qb.num_q == 0) return cudaSuccess;
   CUtensorMap tm_q, tm_k;
   if (!make_tmap_rows128(&tm_q, ix.q, (uint64_t)qb.num_q * kHI, 128, kQG * kHI)) return cudaErrorInvalidValue;
   if (!make_tmap_rows128(&tm_k, ix.k, (uint64_t)cm.num_rows, 128, 64)) return cudaErrorInvalidValue;
   const int sms = sm_count_here();
   const int ngroups = (qb.num_q + kQG - 1) / kQG;
-  const int tmax = (qb.max_kv + kKT - 1) / kKT;
   // chunks of ch key tiles: the CTAs take items round-robin, so pick the ch
   // that minimises the busiest CTA's load (items x tiles, plus about one
   // tile's worth of fixed cost per item); ties go to the larger chunk
@@ -577,8 +565,8 @@ cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const ds
   const int grid = (int)std::min<int64_t>(sms, (int64_t)ngroups * nchunk);
   cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
-  indexer_tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tm_q, tm_k, qb, cm, ix.q_scale, ix.w, ix.k_scale, scores,
-                                                             ld, ngroups, nchunk, ch, wait_limit, err);
+  indexer_tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tm_q, tm_k, qb, cm, ix.q_scale, ix.w, ix.k_scale, out,
+                                                             ngroups, nchunk, ch, wait_limit, err);
   return cudaGetLastError();
 }
 

@@ -22,12 +22,52 @@ cudaError_t launch_attn_simt(const QueryBatch& qb, const CacheMap& cm, const dsa
 
 // Lightning indexer on tcgen05 tensor cores: FP8 e4m3, 64 heads x 128, contiguous
 // caches or paged caches whose block size is a multiple of 64.
+// Where the tensor-core indexer puts its scores.
+//   kFull:   score rows, scores[i * ld + s] (-inf beyond the query's position,
+//            up to max_kv), every key tile.
+//   kSample: only the key tiles 0, m, 2m, ...; the scores of the o-th of them
+//            go to scores[i * ld + o * 128 + (s - 128 o m)] (-inf beyond the
+//            query's position).
+//   kFilter: every other key tile; a key is appended to the query's candidate
+//            list (cand[i * cap + slot], its composite key) when its composite
+//            key is at least thr[i]; cnt[i] counts the appends (entries past
+//            cap are not stored).
+// In kSample and kFilter, queries at positions below min_pos are skipped.
+struct IndexerOut {
+  enum { kFull = 0, kSample = 1, kFilter = 2 };
+  int mode = kFull;
+  int m = 1;
+  int min_pos = 0;
+  int cap = 0;
+  float* scores = nullptr;
+  int64_t ld = 0;
+  const uint64_t* thr = nullptr;
+  uint32_t* cnt = nullptr;
+  uint64_t* cand = nullptr;
+};
+
+// Ordinal count of a mode's key tiles among T tiles (host side of the
+// kernel's tile map).
+inline int indexer_tile_count(const IndexerOut& o, int T) {
+  if (o.mode == IndexerOut::kFull) return T;
+  const int sampled = (T + o.m - 1) / o.m;
+  return o.mode == IndexerOut::kSample ? sampled : T - sampled;
+}
+
 // wait_limit: SM clocks after which any of the kernel's waits gives up
 // (DSA_ERR_TIMEOUT); the default is about one second.
 bool indexer_tc_supported(const CacheMap& cm, const dsa_indexer_inputs& ix);
 cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
-                              float* scores, int64_t ld, int* err, cudaStream_t stream,
+                              const IndexerOut& out, int* err, cudaStream_t stream,
                               long long wait_limit = 2000000000LL);
+inline cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
+                                     float* scores, int64_t ld, int* err, cudaStream_t stream,
+                                     long long wait_limit = 2000000000LL) {
+  IndexerOut o;
+  o.scores = scores;
+  o.ld = ld;
+  return launch_indexer_tc(qb, cm, ix, o, err, stream, wait_limit);
+}
 
 inline cudaError_t launch_indexer(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
                                   float* scores, int64_t ld, int* err, cudaStream_t stream,
@@ -35,6 +75,35 @@ inline cudaError_t launch_indexer(const QueryBatch& qb, const CacheMap& cm, cons
   if (indexer_tc_supported(cm, ix)) return launch_indexer_tc(qb, cm, ix, scores, ld, err, stream, wait_limit);
   return launch_indexer_simt(qb, cm, ix, scores, ld, err, stream);
 }
+
+// ---- The fused forward's selection (select.cu, select_fallback.cu)
+// Sampled key tiles per query row: the sample stride m is the smallest that
+// keeps a row's sampled tiles at or below this count.
+constexpr int kSelSampleTiles = 32;
+struct SelectPlan {
+  int m;             // sample stride in key tiles
+  int64_t lds;       // sample row length (floats): sampled tiles x 128
+  int cap;           // candidate list capacity per row (composite keys)
+  int list_cap;      // the select kernel's shared list: cap + lds
+};
+SelectPlan plan_select(int max_kv, int k);
+size_t select_shared_bytes(const SelectPlan& p);
+// Per row: the threshold (composite key) from the sampled scores; clears the
+// row's candidate count (and the fallback queue counters fail_ctr[0..1]).
+cudaError_t launch_sel_threshold(const QueryBatch& qb, const SelectPlan& p, const float* samp, int k, uint64_t* thr,
+                                 uint32_t* cnt, uint32_t* fail_ctr, cudaStream_t stream);
+// Per row: the exact top-k from the candidates and samples, written to idx in
+// ascending position; rows whose threshold missed go to the fallback queue.
+cudaError_t launch_sel_select(const QueryBatch& qb, const SelectPlan& p, const float* samp, int k, const uint64_t* thr,
+                              const uint32_t* cnt, const uint64_t* cand, int32_t* idx, uint32_t* fail_ctr,
+                              uint32_t* fail_rows, int* err, cudaStream_t stream);
+// The queued rows: scores recomputed (same arithmetic as the indexer) into
+// one row of `slots` (ld floats) per CTA, then the exact top-k.  FP8 indexer
+// operands only.
+int sel_fallback_grid(int num_q);
+cudaError_t launch_sel_fallback(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix, int k,
+                                int32_t* idx, float* slots, int64_t ld, int grid, uint32_t* fail_ctr,
+                                const uint32_t* fail_rows, int* err, cudaStream_t stream);
 
 // Sparse attention on tcgen05 tensor cores: 128 heads, d_qk 576, d_v 512, bf16
 // queries, a bf16 or FP8 (e4m3 + per-row scale) latent cache.

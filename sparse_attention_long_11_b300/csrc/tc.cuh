@@ -110,6 +110,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// mbar_wait for a whole warp whose lanes go on to warp-collective work
+// (tcgen05.ld/st are .sync.aligned): every lane waits and the result is
+// uniform across the warp, so an abort that reaches the lanes at different
+// moments never splits the warp.  All 32 lanes must call it.
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               long long limit = kWaitLimitCycles) {
+  const bool ok = mbar_wait<kCluster>(bar, parity, abort, limit);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Waits for a phase that completes by this thread's own asynchronous work
 // alone (its TMA loads, its MMAs): used before a CTA exits, so it ignores the
 // abort flag.  Bounded by kWaitLimitCycles; false if that expires.

@@ -60,8 +60,23 @@ def test_workspace_size_validation():
     big = api.QueryDesc(1 << 20, 0x10000, 0x10000, 131072)
     assert 131072 * 4 <= L.dsa_forward_workspace_size(ctypes.byref(big), ctypes.byref(_ix()), 2048,
                                                        ctypes.byref(_at())) <= 1 << 30
+    # 4 queries at a 2^22 context: one stage of all four rows, with a fallback score row for each
     huge = api.QueryDesc(4, 0x10000, 0x10000, 1 << 22)
-    assert L.dsa_forward_workspace_size(ctypes.byref(huge), ctypes.byref(_ix()), 2048, ctypes.byref(_at())) == 4 << 24
+    ws_huge = L.dsa_forward_workspace_size(ctypes.byref(huge), ctypes.byref(_ix()), 2048, ctypes.byref(_at()))
+    assert ws_huge == L.dsa_forward_stage_workspace_size(ctypes.byref(huge), ctypes.byref(_ix()), 2048,
+                                                         ctypes.byref(_at()), 4)
+    assert ws_huge >= 4 << 24
+    # per-stage sizes: more rows per stage need more bytes; below one row nothing
+    st = lambda q, r, ix=None: L.dsa_forward_stage_workspace_size(ctypes.byref(q), ctypes.byref(ix or _ix()), 2048,
+                                                                  ctypes.byref(_at()), r)
+    assert 0 < st(qd, 1) < st(qd, 8) < st(qd, 16) == st(qd, 100)           # capped at the batch
+    assert st(qd, 0) == 0 and st(qd, -3) == 0
+    # the FP8 path keeps a candidate list per row, far less than a score row at long contexts
+    long_q = api.QueryDesc(4096, 0x10000, 0x10000, 131072)
+    assert st(long_q, 4096) - st(long_q, 2048) < 2048 * 131072 * 4 // 4
+    # fp32 operands stage whole score rows
+    f32 = _ix(dtype=api.DSA_F32, heads=4, dim=64, scales=False)
+    assert st(qd, 3, f32) == 3 * 4096 * 4
 
 
 def test_host_validation_rejects_before_launch():
@@ -86,7 +101,10 @@ def test_host_validation_rejects_before_launch():
     assert f(*args(ws=None)) == api.DSA_ERR_WORKSPACE
     assert f(*args(ws=0x10010)) == api.DSA_ERR_WORKSPACE                      # not 256-byte aligned
     assert f(*args(wsb=1024)) == api.DSA_ERR_WORKSPACE
-    assert f(*args(wsb=4096 * 4 - 4)) == api.DSA_ERR_WORKSPACE                # less than one staged score row
+    least = L.dsa_forward_stage_workspace_size(ctypes.byref(qd), ctypes.byref(_ix()), 2048, ctypes.byref(_at()), 1)
+    assert f(*args(wsb=4096 * 4)) == api.DSA_ERR_WORKSPACE                    # one score row is not a stage
+    assert least > 4096 * 4
+    assert f(*args(wsb=least - 256)) == api.DSA_ERR_WORKSPACE                 # less than one stage of one row
     assert f(*args(q=api.QueryDesc(16, 0x10000, 0x10000, 0))) == api.DSA_ERR_INVALID_ARG
     assert f(*args(c=api.CacheDesc(2, 4096, 100, None, 0, 0))) == api.DSA_ERR_INVALID_ARG   # overlapping seqs
     assert f(*args(c=api.CacheDesc(1, 4096, 0, 0x10000, 64, 2))) == api.DSA_ERR_INVALID_ARG  # table too short

@@ -23,7 +23,8 @@ def _prefill(L=32768, k=2048):
 def test_pair_counts_of_the_long_prefill():
     n_idx, n_attn = bench._pairs(_prefill())
     L, k = 32768, 2048
-    assert n_idx == L * (L + 1) // 2 == 536_887_296                    # every causal pair
+    # every causal pair of the queries with more than k keys (t + 1 > k)
+    assert n_idx == L * (L + 1) // 2 - k * (k + 1) // 2 == 534_789_120
     assert n_attn == k * (k + 1) // 2 + (L - k) * k == 65_012_736      # min(t + 1, k) per query
 
 
@@ -49,7 +50,7 @@ def test_prefill_roofline_takes_the_dominant_kernel():
     # an indexer-dominated step reports against twice the bf16 peak (FP8)
     per_stage["indexer"][1] = 40 * 5.0
     r = bench._roofline_prefill(wl, per_stage, steps, PEAKS)
-    want = 536_887_296 / 8 * 16_384 / 5.0e-3 / 1e12
+    want = 534_789_120 / 8 * 16_384 / 5.0e-3 / 1e12
     assert r["kernel"] == "indexer" and math.isclose(r["achieved"], want, rel_tol=1e-12)
     assert math.isclose(r["peak"], 3600.0) and r["traffic"] is None
 
@@ -72,7 +73,7 @@ def test_decode_stage_fractions_count_each_stage_bytes():
     per_stage = {"indexer": [10, 10 * 0.146], "topk": [10, 10 * 0.034], "attention": [10, 10 * 0.061]}
     r = bench._decode_stage_roofline(wl, per_stage, 10, PEAKS)
     assert r["indexer"]["bytes"] == 64 * 65536 * 132
-    assert r["topk"]["bytes"] == 64 * 65536 * 4 + 64 * 2048 * 4          # staged rows read, index rows written
+    assert r["topk"]["bytes"] == 64 * 2048 * 8 + 64 * 2048 * 4           # k candidate keys read, index rows written
     assert r["attention"]["bytes"] == 64 * 2048 * 1152 + 64 * 128 * (576 + 512) * 2   # gather + q in + O out
     for name, ms in (("indexer", 0.146), ("topk", 0.034), ("attention", 0.061)):
         assert math.isclose(r[name]["ms"], ms)

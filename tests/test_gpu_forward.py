@@ -152,10 +152,10 @@ def test_workspace_size_does_not_change_results():
     wl = inputs.make_prefill(seed=8, device=DEV, L=2600)
     prob = api.Problem(wl)
     qd, ix, at = prob.rows(0, wl.num_q)
-    ld = (2600 + 3) // 4 * 4
     res = []
     for rows in (None, 100, 1):
-        nb = api.dsa_forward_workspace_size(qd, ix, wl.topk, at) if rows is None else rows * ld * 4
+        nb = (api.dsa_forward_workspace_size(qd, ix, wl.topk, at) if rows is None
+              else api.dsa_forward_stage_workspace_size(qd, ix, wl.topk, at, rows))
         ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
         idx = torch.empty((wl.num_q, wl.topk), dtype=torch.int32, device=DEV)
         out = torch.empty((wl.num_q, wl.H, wl.d_v), dtype=prob.out_dtype(), device=DEV)
