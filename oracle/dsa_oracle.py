@@ -231,6 +231,40 @@ def dense_causal_mqa(q, kv, q_pos, scale: float, d_v: int):
 
 
 # ---------------------------------------------------------------------------
+# Per-head attention over the selected entries (the prefill attention mode)
+# ---------------------------------------------------------------------------
+
+
+def sparse_attention_mha(q, k_nope, k_rope, v, scale: float):
+    """Softmax attention of H query heads over n selected keys, each head with
+    its own key and value rows: the per-head (non-absorbed) form of
+    multi-head latent attention.  Susan Zhang's thread on the DeepSeek-V3.2
+    write-up names separate attention modes for disaggregated prefill and
+    decode; this is the prefill one, the latent MQA of sparse_attention the
+    decode one.  A head's key is its own d_nope-wide part followed by the
+    d_rope-wide part that all heads share.
+
+    q [H, d_nope + d_rope], k_nope [n, H, d_nope], k_rope [n, d_rope],
+    v [n, H, d_v] float64.  Returns (O [H, d_v], LSE [H]); n = 0 gives
+    O = 0 and LSE = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    kn = np.asarray(k_nope, dtype=np.float64)
+    kr = np.asarray(k_rope, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    H = q.shape[0]
+    if kn.shape[0] == 0:
+        return np.zeros((H, v.shape[2])), np.full(H, -np.inf)
+    dn = kn.shape[2]
+    logits = scale * (np.einsum("hd,nhd->hn", q[:, :dn], kn) + q[:, dn:] @ kr.T)   # [H, n]
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    l = p.sum(axis=1, keepdims=True)
+    o = np.einsum("hn,nhd->hd", p, v) / l
+    return o, (m + np.log(l))[:, 0]
+
+
+# ---------------------------------------------------------------------------
 # The whole hot path for a set of queries
 # ---------------------------------------------------------------------------
 

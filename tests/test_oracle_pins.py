@@ -462,3 +462,62 @@ def test_indexer_kl_special_cases():
     for s in range(5):
         qq, _, ww, kk_, _, ss, pp = _kl_case(10 + s)
         assert O.indexer_kl_backward(qq, ww, kk_, ss, pp)["loss"] >= 0
+
+
+# --------------------------------------------------------------------------- per-head (prefill) attention mode
+
+def _latent_mha(seed, n, H=4, dl=24, dr=8, dn=6, dv=5):
+    """Latent rows c (dl latent + dr rope), per-head up-projections W_K, W_V,
+    the per-head keys and values they give, and a query."""
+    rng = np.random.default_rng(seed)
+    c = rng.standard_normal((n, dl + dr))
+    WK = rng.standard_normal((H, dn, dl))
+    WV = rng.standard_normal((H, dv, dl))
+    qn, qr = rng.standard_normal((H, dn)), rng.standard_normal((H, dr))
+    k_nope = np.einsum("hdl,nl->nhd", WK, c[:, :dl])
+    v = np.einsum("hdl,nl->nhd", WV, c[:, :dl])
+    return c, WK, WV, qn, qr, k_nope, c[:, dl:], v
+
+
+def test_mha_mode_equals_absorbed_latent_mqa():
+    """The two attention modes are one attention: with per-head keys and
+    values that are up-projections of latent rows (k_nope = W_K c,
+    v = W_V c, the rope part shared), per-head attention equals the latent MQA
+    of sparse_attention with the absorbed query (W_K^T q_nope, q_rope), its
+    output up-projected by W_V, and the two LSEs agree."""
+    dl = 24
+    c, WK, WV, qn, qr, k_nope, k_rope, v = _latent_mha(41, n=37, dl=dl)
+    o, lse = O.sparse_attention_mha(np.concatenate([qn, qr], 1), k_nope, k_rope, v, 0.3)
+    q_abs = np.concatenate([np.einsum("hdl,hd->hl", WK, qn), qr], 1)
+    o_lat, lse_lat = O.sparse_attention(q_abs, c, 0.3, dl)           # the value: the latent part
+    np.testing.assert_allclose(lse, lse_lat, rtol=0, atol=1e-11)
+    np.testing.assert_allclose(o, np.einsum("hdl,hl->hd", WV, o_lat), rtol=0, atol=1e-11)
+
+
+def test_mha_mode_dense_causal_matches_torch_sdpa():
+    rng = np.random.default_rng(42)
+    T, H, dn, dr, dv = 13, 3, 6, 4, 5
+    q = rng.standard_normal((T, H, dn + dr))
+    k_nope, k_rope, v = rng.standard_normal((T, H, dn)), rng.standard_normal((T, dr)), rng.standard_normal((T, H, dv))
+    kh = np.concatenate([k_nope, np.broadcast_to(k_rope[:, None, :], (T, H, dr))], 2)   # each head's full key
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q).permute(1, 0, 2), torch.tensor(kh).permute(1, 0, 2), torch.tensor(v).permute(1, 0, 2),
+        is_causal=True, scale=0.45).permute(1, 0, 2).numpy()
+    for t in range(T):
+        o, _ = O.sparse_attention_mha(q[t], k_nope[:t + 1], k_rope[:t + 1], v[:t + 1], 0.45)
+        np.testing.assert_allclose(o, ref[t], rtol=0, atol=1e-12)
+
+
+def test_mha_mode_special_cases():
+    _, _, _, qn, qr, k_nope, k_rope, v = _latent_mha(43, n=9)
+    q = np.concatenate([qn, qr], 1)
+    o, lse = O.sparse_attention_mha(q, k_nope[4:5], k_rope[4:5], v[4:5], 0.7)     # one key: its value row
+    np.testing.assert_allclose(o, v[4], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, 0.7 * (np.einsum("hd,hd->h", qn, k_nope[4]) + qr @ k_rope[4]), atol=1e-12)
+    o0, l0 = O.sparse_attention_mha(q, k_nope[:0], k_rope[:0], v[:0], 0.7)        # no key
+    assert np.all(o0 == 0) and np.all(np.isneginf(l0))
+    perm = np.random.default_rng(0).permutation(9)                                   # order of the keys is irrelevant
+    o1, l1 = O.sparse_attention_mha(q, k_nope, k_rope, v, 0.7)
+    o2, l2 = O.sparse_attention_mha(q, k_nope[perm], k_rope[perm], v[perm], 0.7)
+    np.testing.assert_allclose(o1, o2, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, atol=1e-13)
