@@ -348,10 +348,9 @@ def _time_append(wl, r: Runner, steps: int, warmup: int):
             "note": "latency-bound: one 128-thread block per 4 tokens; ms from the launch's own events"}
 
 
-FP32_FMA_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12   # CUDA-core fp32: SMs x FMA lanes x 2 x max SM clock
 
 
-def _time_kl_backward(r: Runner, steps: int, warmup: int):
+def _time_kl_backward(r: Runner, steps: int, warmup: int, peaks):
     """The indexer's training step (alignment loss + gradients) over the last
     4096-query call of the prefill, on the entries the forward selected and
     seeded synthetic targets.  One launch per step, timed with CUDA events."""
@@ -390,9 +389,60 @@ def _time_kl_backward(r: Runner, steps: int, warmup: int):
     tf = flop / (ms / 1e3) / 1e12
     return {"workload": f"queries {a}..{b - 1} of the L={wl.max_kv} prefill, k={k}, synthetic targets",
             "value": n / (ms / 1e3), "unit": "tokens/s", "ms": ms, "pairs": pairs,
-            "roofline": {"bound": "alu", "achieved": tf, "peak": FP32_FMA_PEAK_TFLOPS, "unit": "TFLOP/s",
-                         "frac": tf / FP32_FMA_PEAK_TFLOPS,
-                         "peak_src": "derived: 148 SMs x 128 fp32 FMA lanes x 2 FLOP x 2032 MHz"}}
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                         "frac": tf / peaks["bf16"],
+                         "peak_src": f"{peaks['src']} bf16 burst (the three contractions run as fp16 MMAs, "
+                                     f"the same rate)"}}
+
+
+def _time_mha_mode(r: Runner, peaks, nq: int = 512, steps: int = 5, warmup: int = 3):
+    """The per-head (non-absorbed) prefill attention mode against the latent
+    MQA mode on the same selections: the last nq queries of the prefill, the
+    entries the forward selected for them, per-head keys and values of 128
+    (rope part 64 shared) for 128 heads.  Each selected pair moves 65,664
+    bytes of rows in the per-head mode and 1,152 in the latent one."""
+    wl = r.wl
+    L = wl.max_kv
+    a, b = wl.num_q - nq, wl.num_q
+    mh = inputs.make_mha_prefill(seed=0, device=wl.q.device, L=L, heads=128, q_rows=(L - nq, L))
+    idx = r.idx[a:b].contiguous()
+    bdesc = api.Batch(mh.q_seq, mh.q_pos, L).desc()
+    cache = api.Cache(1, L, L).desc()
+    out = torch.empty((nq, 128, 128), dtype=torch.bfloat16, device=wl.q.device)
+    lse = torch.empty((nq, 128), dtype=torch.float32, device=wl.q.device)
+    at = api.mha_inputs(mh.q, mh.k_nope, mh.k_rope, mh.v, mh.softmax_scale)
+    qd, _, atl = r.prob.rows(a, b)
+    out_l = torch.empty((nq, 128, 512), dtype=torch.bfloat16, device=wl.q.device)
+    lse_l = torch.empty((nq, 128), dtype=torch.float32, device=wl.q.device)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    ms_mha = timed(lambda: api.dsa_sparse_attn_mha(bdesc, cache, at, idx, wl.topk, out, lse))
+    ms_lat = timed(lambda: api.dsa_sparse_attn(qd, r.cache, atl, idx, wl.topk, out_l, lse_l))
+    st = api.dsa_check_device_error()
+    if st != api.DSA_OK:
+        raise RuntimeError(f"device error in the per-head mode: {api.status_string(st)}")
+    pairs = int((idx >= 0).sum().item())
+    per_pair = 128 * (128 + 128) * 2 + 64 * 2
+    gbs = pairs * per_pair / (ms_mha / 1e3) / 1e9
+    del mh, out, lse, out_l, lse_l
+    torch.cuda.empty_cache()
+    return {"workload": f"queries {L - nq}..{L - 1} of the L={L} prefill on the forward's selections, 128 heads, "
+                        f"per-head keys/values 128 + shared rope 64 (bf16)",
+            "pairs": pairs, "bytes_per_pair": per_pair, "latent_bytes_per_pair": BYTES_PER_ATTN_KEY,
+            "ms": ms_mha, "latent_ms": ms_lat, "ratio": ms_mha / ms_lat,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "peak_src": f"{peaks['src']} hbm"}}
 
 
 def _e2e(wl, steps: int):
@@ -538,6 +588,7 @@ def main():
     ap.add_argument("--no-fp8-kv", action="store_true")
     ap.add_argument("--no-kl-backward", action="store_true")
     ap.add_argument("--no-mixed", action="store_true")
+    ap.add_argument("--no-mha", action="store_true")
     args = ap.parse_args()
     ws, rank, local = _dist()
     if args.impl == "reference":
@@ -556,7 +607,8 @@ def main():
     roof = _roofline_prefill(wl, per_stage, args.steps, peaks)
     stages = {k: {"launches": v[0], "ms_per_step": v[1] / args.steps} for k, v in per_stage.items()}
     # the indexer's training step on the selections of the last call (after the timed region)
-    kl_bwd = None if args.no_kl_backward else _time_kl_backward(r, 3, 2)
+    kl_bwd = None if args.no_kl_backward else _time_kl_backward(r, 3, 2, peaks)
+    mha_mode = None if args.no_mha else _time_mha_mode(r, peaks)
     del r
     torch.cuda.empty_cache()
     e2e_val, h2d, d2h, e2e_ms = _e2e(wl, args.e2e_steps)
@@ -685,7 +737,7 @@ def main():
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
                 "cpu_baseline": cpu, "decode": decode, "k_sweep": k_sweep,
                 "prefill_128k": long128k, "prefill_fp8_kv": prefill_fp8_kv, "indexer_kl_backward": kl_bwd,
-                "mixed": mixed}
+                "mixed": mixed, "prefill_mha_mode": mha_mode}
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist

@@ -137,7 +137,7 @@ typedef struct {
   int32_t d_v;
   const void* q;          /* [num_q, heads, d_qk] */
   const void* kv;         /* [num_rows, d_qk] latent KV cache */
-  float softmax_scale;    /* finite; logits are scale * <q, kv> */
+  float softmax_scale;    /* finite (positive for DSA_BF16 and DSA_FP8_E4M3); logits are scale * <q, kv> */
   const float* kv_scale;  /* DSA_FP8_E4M3: [num_rows] per-row scales; else NULL */
 } dsa_attn_inputs;
 
@@ -180,6 +180,44 @@ DSA_API dsa_status dsa_topk(const dsa_query_desc* qd, const float* scores, int64
 DSA_API dsa_status dsa_sparse_attn(const dsa_query_desc* qd, const dsa_cache_desc* cd,
                            const dsa_attn_inputs* at, const int32_t* idx, int32_t k,
                            void* out, float* lse, dsa_stream_t stream);
+
+/* Per-head attention operands: the prefill attention mode.
+ *
+ * Susan Zhang's thread on the DeepSeek-V3.2 write-up names separate attention
+ * modes for disaggregated prefill and decode.  dsa_sparse_attn is the latent
+ * (absorbed) form, one shared row per key; this is the per-head
+ * (non-absorbed) form of the same attention: every head has its own key and
+ * value rows, as up-projected from the latent rows, and the rope part of the
+ * key is shared by all heads.  With k_nope[s,h] = W_K[h] c[s], v[s,h] =
+ * W_V[h] c[s] and the absorbed query (W_K[h]^T q_nope[h], q_rope[h]), the two
+ * give the same attention (the output up-projected by W_V[h]).  The pages
+ * give no shapes; this library fixes d_nope = 128, d_rope = 64, d_v = 128,
+ * bf16, heads a multiple of 8 up to 128.  A selected pair then moves
+ * heads x 512 + 128 bytes of rows (65,664 at 128 heads) against 1,152 for the
+ * latent row: the mode is bound by the gathers.
+ * All pointers 16-byte aligned. */
+typedef struct {
+  dsa_dtype dtype;        /* DSA_BF16 */
+  int32_t heads;          /* H: 8 .. 128, a multiple of 8 */
+  int32_t d_nope;         /* 128 */
+  int32_t d_rope;         /* 64 */
+  int32_t d_v;            /* 128 */
+  const void* q;          /* [num_q, heads, d_nope + d_rope] */
+  const void* k_nope;     /* [num_rows, heads, d_nope] per-head key rows */
+  const void* k_rope;     /* [num_rows, d_rope] the rope part, shared by all heads */
+  const void* v;          /* [num_rows, heads, d_v] per-head value rows */
+  float softmax_scale;    /* finite */
+} dsa_mha_inputs;
+
+/* Per-head sparse attention of every query row over its selected positions
+ * idx[i * k .. i * k + k) (entries -1 are skipped; any order; a position must
+ * be <= q_pos[i]):
+ *   O[i,h,:] = sum_s softmax_s(scale * (<q_nope[i,h], k_nope[s,h]> + <q_rope[i,h], k_rope[s]>)) v[s,h,:]
+ * out [num_q, heads, d_v] bf16, lse [num_q, heads] fp32 (natural log; -inf
+ * and a zero row if nothing is selected).  1 <= k <= 8192.  Cache rows are
+ * mapped by the cache descriptor as for the other stages. */
+DSA_API dsa_status dsa_sparse_attn_mha(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_mha_inputs* at,
+                                       const int32_t* idx, int32_t k, void* out, float* lse, dsa_stream_t stream);
 
 /* Recommended bytes of workspace for dsa_forward on this batch (0 if the
  * arguments are invalid): every query row in one stage, capped at 1 GiB.

@@ -51,6 +51,13 @@ class AttnInputs(ctypes.Structure):
                 ("softmax_scale", ctypes.c_float), ("kv_scale", ctypes.c_void_p)]
 
 
+class MhaInputs(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("heads", ctypes.c_int32), ("d_nope", ctypes.c_int32),
+                ("d_rope", ctypes.c_int32), ("d_v", ctypes.c_int32), ("q", ctypes.c_void_p),
+                ("k_nope", ctypes.c_void_p), ("k_rope", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("softmax_scale", ctypes.c_float)]
+
+
 _P = ctypes.POINTER
 _SIGS = {
     "dsa_index_scores": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(IndexerInputs), ctypes.c_void_p,
@@ -61,6 +68,8 @@ _SIGS = {
                                 ctypes.c_void_p]),
     "dsa_sparse_attn": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(AttnInputs), ctypes.c_void_p,
                                        ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "dsa_sparse_attn_mha": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(MhaInputs), ctypes.c_void_p,
+                                           ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "dsa_forward_workspace_size": (ctypes.c_size_t, [_P(QueryDesc), _P(IndexerInputs), ctypes.c_int32,
                                                      _P(AttnInputs)]),
     "dsa_forward_stage_workspace_size": (ctypes.c_size_t, [_P(QueryDesc), _P(IndexerInputs), ctypes.c_int32,
@@ -195,6 +204,20 @@ def dsa_sparse_attn(batch: QueryDesc, cache: CacheDesc, at: AttnInputs, idx: tor
                     out: torch.Tensor, lse: torch.Tensor, stream=None) -> None:
     _check(lib().dsa_sparse_attn(ctypes.byref(batch), ctypes.byref(cache), ctypes.byref(at), _ptr(idx), k,
                                  _ptr(out), _ptr(lse), _stream(stream)), "dsa_sparse_attn")
+
+
+def mha_inputs(q, k_nope, k_rope, v, softmax_scale: float) -> MhaInputs:
+    """Per-head attention operands (bf16): q [num_q, H, 192], k_nope [rows, H, 128],
+    k_rope [rows, 64], v [rows, H, 128]."""
+    return MhaInputs(DSA_BF16, q.shape[1], k_nope.shape[-1], k_rope.shape[-1], v.shape[-1], _ptr(q), _ptr(k_nope),
+                     _ptr(k_rope), _ptr(v), softmax_scale)
+
+
+def dsa_sparse_attn_mha(batch: QueryDesc, cache: CacheDesc, at: MhaInputs, idx: torch.Tensor, k: int,
+                        out: torch.Tensor, lse: torch.Tensor, stream=None) -> None:
+    """Per-head (non-absorbed) sparse attention: the prefill attention mode."""
+    _check(lib().dsa_sparse_attn_mha(ctypes.byref(batch), ctypes.byref(cache), ctypes.byref(at), _ptr(idx), k,
+                                     _ptr(out), _ptr(lse), _stream(stream)), "dsa_sparse_attn_mha")
 
 
 def dsa_forward_workspace_size(batch: QueryDesc, ix: IndexerInputs, k: int, at: AttnInputs) -> int:

@@ -78,6 +78,7 @@ dsa_status check_attn(const dsa_attn_inputs* at) {
   if ((at->dtype == DSA_FP8_E4M3) != (at->kv_scale != nullptr)) return DSA_ERR_INVALID_ARG;
   if (at->kv_scale && !aligned(at->kv_scale, 4)) return DSA_ERR_INVALID_ARG;
   if (at->dtype == DSA_BF16 || at->dtype == DSA_FP8_E4M3) {
+    if (!(at->softmax_scale > 0.f)) return DSA_ERR_INVALID_ARG;   // the row maxima are taken on the raw dots
     if (at->heads != 128 || at->d_qk != 576 || at->d_v != 512) return DSA_ERR_UNSUPPORTED;
   } else if (at->dtype == DSA_F32) {
     if (at->heads < 8 || at->heads > 128 || at->heads % 8) return DSA_ERR_UNSUPPORTED;
@@ -377,6 +378,28 @@ dsa_status dsa_sparse_attn(const dsa_query_desc* qd, const dsa_cache_desc* cd, c
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return cuda_status(launch(DSA_STAGE_ATTN, st, [&] {
     return launch_attn(to_batch(qd), to_map(cd), *at, idx, k, out, lse, err, st);
+  }));
+}
+
+dsa_status dsa_sparse_attn_mha(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_mha_inputs* at,
+                               const int32_t* idx, int32_t k, void* out, float* lse, dsa_stream_t stream) {
+  DSA_TRY(check_query(qd));
+  if (k < 1 || k > kMaxTopk) return DSA_ERR_INVALID_ARG;
+  if (qd->num_q == 0) return DSA_OK;
+  DSA_TRY(check_cache(cd, qd->max_kv));
+  if (!at || !at->q || !at->k_nope || !at->k_rope || !at->v) return DSA_ERR_INVALID_ARG;
+  if (!aligned(at->q, 16) || !aligned(at->k_nope, 16) || !aligned(at->k_rope, 16) || !aligned(at->v, 16))
+    return DSA_ERR_INVALID_ARG;
+  if (!std::isfinite(at->softmax_scale)) return DSA_ERR_INVALID_ARG;
+  if (at->dtype != DSA_BF16 || at->d_nope != 128 || at->d_rope != 64 || at->d_v != 128) return DSA_ERR_UNSUPPORTED;
+  if (at->heads < 8 || at->heads > 128 || at->heads % 8) return DSA_ERR_UNSUPPORTED;
+  if (!idx || !out || !lse || !aligned(idx, 4) || !aligned(out, 16) || !aligned(lse, 4)) return DSA_ERR_INVALID_ARG;
+  int* err = device_error_ptr();
+  if (!err) return DSA_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] {
+    return launch_attn_mha(to_batch(qd), to_map(cd), at->heads, at->q, at->k_nope, at->k_rope, at->v,
+                           at->softmax_scale, idx, k, out, lse, err, st);
   }));
 }
 

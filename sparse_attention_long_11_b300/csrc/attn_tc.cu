@@ -60,14 +60,16 @@ constexpr uint32_t kQRopeBytes = 128 * 64;                 // rope half: 128 hea
 constexpr uint32_t kKVSlotBytes = kNK * 128;               // 64 keys x 128 B
 constexpr uint32_t kKVRopeBytes = kNK * 64;                // 64 keys x 64 B
 constexpr uint32_t kKVStageBytes = 4 * kKVSlotBytes + kKVRopeBytes;   // 36 KB
-constexpr uint32_t kXBytes = kH * kNK * 2;                 // one partial logit tile from the peer (fp16)
+constexpr uint32_t kXCodeBytes = kH * kNK * 2;             // one partial logit tile from the peer: 16-bit codes
+constexpr uint32_t kXBytes = kXCodeBytes + kH * 8;         // ... plus each head's (step, lo) pair
 constexpr int kStages = 4;
 constexpr uint32_t kOffQRope = 0;
 constexpr uint32_t kOffKV = kOffQRope + kQRopeBytes;       // 8 KB
 constexpr uint32_t kOffX = kOffKV + kStages * kKVStageBytes;   // 152 KB
 constexpr uint32_t kPBytes = kH * 128;                     // 128 x 64 bf16 probabilities (SW128)
-constexpr uint32_t kOffP = kOffX + 2 * kXBytes;            // 184 KB: P[0], P[1]
-constexpr uint32_t kSmemBytes = kOffP + 2 * kPBytes;       // 216 KB
+constexpr uint32_t kOffP = kOffX + 2 * kXBytes;            // 186 KB: P[0], P[1] (1024-aligned)
+constexpr uint32_t kSmemBytes = kOffP + 2 * kPBytes;       // 218 KB
+static_assert(kOffP % 1024 == 0, "P tiles are 128B-swizzled MMA operands");
 constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;         // + alignment slack
 constexpr int kGatherWarp0 = 8;
 constexpr int kGatherGroups = 3;                           // of two warps; group j gathers the tiles g = j mod 3
@@ -96,10 +98,11 @@ struct Bars {
   uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], xf[2], xe[2];
   uint64_t s_empty[2], p_full[2], pv_done[2], mdone[2];
   uint64_t q_full, q_rope, q_empty, o_empty, qend, fin[2];
-  float mtile[2][128];          // [group][head] scratch: the tile maximum
-  float mpub[2][128];           // [tile parity][head] running maximum after the group's latest tile
+  float mpub[2][128];           // [group][head] running maximum after the group's latest tile
   float lsum[2][2][128];        // [query parity][group][head] the groups' sums at the end of a query
+  float lrsum[2][2][128];       // ... the same sums of the bf16-rounded probabilities the MMA used
   float mseen[2][2][128];       // ... and the maxima they are relative to
+  float mdep;                   // write-only: orders the consumed-X arrive after the X loads (below)
   uint32_t tmem_base;
   int abort;
 };
@@ -233,6 +236,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     const uint32_t xf_peer = mapa(smem_u32(&B.xf[grp]), peer);
     const uint32_t xe_peer = mapa(smem_u32(&B.xe[grp]), peer);
     const uint4* X4 = reinterpret_cast<const uint4*>(sm + kOffX + grp * kXBytes);
+    const float2* XS = reinterpret_cast<const float2*>(sm + kOffX + grp * kXBytes + kXCodeBytes);
     uint32_t g = 0, qv = 0;   // tiles and queries (with tiles) so far, counted alike by both groups
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
       const QueryInfo qi = query_info(qb, idx, k, i, pv);
@@ -248,7 +252,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         continue;
       }
       const int n_valid = min(k, pos + 1);
-      float m_seen = -INFINITY, l = 0.f;   // the maximum this group last used, its sum relative to it
+      float m_seen = -INFINITY, l = 0.f, lr = 0.f;   // the maximum this group last used, its sums relative to it
       bool ok = true;
       const uint32_t g0 = g;
       for (int t = ((g0 & 1u) == (uint32_t)grp) ? 0 : 1; t < nt; t += 2) {
@@ -263,32 +267,64 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         ATTN_TRACE(grp, gt, 0, lane == 0 && q4 == 0);
         if (!(ok = mbar_wait_warp(&B.s_full[grp], par, abort))) break;
         tc_fence_after();
-        // own partial logits in base-2 units (fp32); the peer gets them rounded to fp16
+        // own partial logits, raw dots (the scale to base-2 units is applied
+        // in the exponent); the peer gets them as fp16 or, where they are
+        // large, as 16-bit fixed point (R20)
         float x[64];
         {
           uint32_t r[4][16];
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld16(tS + c * 16, r[c]);
           tmem_ld_wait();
-          const uint64_t sl2 = f2(scale_log2, scale_log2);
 #pragma unroll
-          for (int j = 0; j < 64; j += 2) {
-            const float2 v = f2_split(mul2(f2(__uint_as_float(r[j >> 4][j & 15]), __uint_as_float(r[j >> 4][(j & 15) + 1])), sl2));
-            x[j] = v.x;
-            x[j + 1] = v.y;
-          }
+          for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(r[j >> 4][j & 15]);
         }
         tc_fence_before();
         mbar_arrive(&B.s_empty[grp]);   // S(gt+2) may be computed into this buffer
         ATTN_TRACE(grp, gt, 1, lane == 0 && q4 == 0);
         // own partial -> the peer's X[grp], once the peer has consumed what we wrote there two tiles ago
         if (!(ok = mbar_wait_warp<true>(&B.xe[grp], par ^ 1, abort))) break;
+        bool precise;   // this warp sent fixed point (warp-uniform)
+        {
+          float mnA = x[0], mxA = x[0], mnB = x[32], mxB = x[32];
 #pragma unroll
-        for (int jq = 0; jq < 8; ++jq)
-          st_async_v4_b32(x_peer + (uint32_t)(jq * 128 + h) * 16u,
-                          make_uint4(f16x2_sat(x[8 * jq], x[8 * jq + 1]), f16x2_sat(x[8 * jq + 2], x[8 * jq + 3]),
-                                     f16x2_sat(x[8 * jq + 4], x[8 * jq + 5]), f16x2_sat(x[8 * jq + 6], x[8 * jq + 7])),
-                          xf_peer);
+          for (int j = 1; j < 31; j += 2) {
+            mnA = min3(mnA, x[j], x[j + 1]);
+            mxA = max3(mxA, x[j], x[j + 1]);
+            mnB = min3(mnB, x[32 + j], x[33 + j]);
+            mxB = max3(mxB, x[32 + j], x[33 + j]);
+          }
+          const float lo = fminf(fminf(mnA, x[31]), fminf(mnB, x[63]));
+          const float hi = fmaxf(fmaxf(mxA, x[31]), fmaxf(mxB, x[63]));
+          // fp16 carries a partial within 2^-11 of its size: a logit error
+          // under 0.004 base-2 units while |x| stays below 8 of them.  A warp
+          // with any larger partial sends 16-bit fixed point over each head's
+          // range instead: codes u = round((x - lo) / step), 0..65534, step =
+          // (hi - lo) / 65534, read back as lo + u step within about half a step.
+          precise = __any_sync(0xffffffffu, fmaxf(hi, -lo) * scale_log2 > 8.f);
+          uint32_t cw[32];
+          float step = -1.f;   // a negative step marks fp16 codes
+          if (precise) {
+            const float range = hi - lo;
+            const float inv = range > 0.f ? __fdividef(65534.f, range) : 0.f;
+            step = range * (1.f / 65534.f);
+            const uint64_t nlo2 = f2(-lo, -lo), inv2 = f2(inv, inv), mag2 = f2(12582912.f, 12582912.f);
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+              // (x - lo) * inv + 1.5 * 2^23: the low 16 bits of the float are the rounded code
+              const float2 y = f2_split(fma2(add2(f2(x[j], x[j + 1]), nlo2), inv2, mag2));
+              cw[j / 2] = prmt(__float_as_uint(y.x), __float_as_uint(y.y), 0x5410u);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) cw[j / 2] = f16x2_sat(x[j], x[j + 1]);
+          }
+#pragma unroll
+          for (int jq = 0; jq < 8; ++jq)
+            st_async_v4_b32(x_peer + (uint32_t)(jq * 128 + h) * 16u,
+                            make_uint4(cw[4 * jq], cw[4 * jq + 1], cw[4 * jq + 2], cw[4 * jq + 3]), xf_peer);
+          st_async_v2_f32(x_peer + kXCodeBytes + (uint32_t)h * 8u, step, lo, xf_peer);
+        }
         ATTN_TRACE(grp, gt, 2, lane == 0 && q4 == 0);
         if (!(ok = mbar_wait_warp<true>(&B.xf[grp], par, abort))) break;   // the peer's partial is in X[grp]
         // arm the next phase: the peer writes X[grp] again only after all of
@@ -304,20 +340,33 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
           vm_lo = __ballot_sync(0xffffffffu, s_e0 >= 0 && s_e0 <= pos);
           vm_hi = __ballot_sync(0xffffffffu, s_e1 >= 0 && s_e1 <= pos);
         }
-        // x = own (fp32) + peer (fp16).  The two CTAs' logits differ by the
-        // fp16 rounding of one partial; each CTA's half of O stays consistent
-        // with its own P and sum, which is all the normalisation needs.
+        // x = own (fp32) + peer (fp16 or fixed point), raw dots.  The two CTAs'
+        // logits differ by the rounding of one partial; each CTA's half of O
+        // stays consistent with its own P and sum, which is all the
+        // normalisation needs.
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         const bool full = (vm_lo & vm_hi) == 0xffffffffu;   // almost every tile: no masking
+        const float2 sc = XS[h];              // the peer's (step, lo) for this head
+        const bool peer_fixed = sc.x >= 0.f;  // warp-uniform: the peer's warp for these heads voted
+        const uint64_t st2 = f2(sc.x, sc.x), lo2 = f2(sc.y, sc.y), m23 = f2(-8388608.f, -8388608.f);
 #pragma unroll
         for (int jq = 0; jq < 8; ++jq) {
           const uint4 v = X4[jq * 128 + h];
           const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float2 p = f16x2_to_f32x2(pw[e]);
+            uint64_t pv2;
+            if (peer_fixed) {
+              // each 16-bit code u as the float 2^23 + u, less 2^23 (exact), then lo + u step
+              const uint64_t u2 = add2(f2(__uint_as_float(prmt(pw[e], 0x4B000000u, 0x7410u)),
+                                          __uint_as_float(prmt(pw[e], 0x4B000000u, 0x7432u))), m23);
+              pv2 = fma2(u2, st2, lo2);
+            } else {
+              const float2 pf = f16x2_to_f32x2(pw[e]);
+              pv2 = f2(pf.x, pf.y);
+            }
             const int j = 8 * jq + 2 * e;
-            const float2 sum = f2_split(add2(f2(x[j], x[j + 1]), f2(p.x, p.y)));
+            const float2 sum = f2_split(add2(f2(x[j], x[j + 1]), pv2));
             x[j] = sum.x;
             x[j + 1] = sum.y;
             if (!full) {
@@ -328,12 +377,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
             m4[e] = max3(m4[e], x[j], x[j + 1]);
           }
         }
-        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;   // base-2 units
         // X[grp] consumed: the store below needs mt, which depends on every
         // value loaded from X, and instructions issue in order, so the relaxed
         // arrive after it follows those loads (a release-ordered remote arrive
         // costs ~1.5k clk)
-        B.mtile[grp][h] = mt;
+        *reinterpret_cast<volatile float*>(&B.mdep) = mt;
         mbar_arrive_remote_relaxed(xe_peer);
         // the running maximum after tile gt-1 (waiting also at a query's first
         // tile keeps the two groups within one tile of each other)
@@ -346,26 +395,44 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         const float m_use = mt > m_prev + 8.f ? mt : m_prev;
         B.mpub[grp][h] = m_use;
         mbar_arrive(&B.mdone[grp]);
-        if (m_use != m_seen) {   // this group's sum follows the maximum
-          l *= ex2_approx(m_seen - m_use);
+        if (m_use != m_seen) {   // this group's sums follow the maximum
+          const float a = ex2_approx(m_seen - m_use);
+          l *= a;
+          lr *= a;
           m_seen = m_use;
         }
         const float msub = m_use == -INFINITY ? 0.f : m_use;   // all p are 0 while nothing is valid
         uint32_t pk[32];
-        uint64_t ps2[2] = {0ull, 0ull};   // the sum of the fp32 probabilities, two packed accumulators
-        const uint64_t nm2 = f2(-msub, -msub);
+        // the sum of the fp32 probabilities (for LSE), and the one that
+        // normalises O.  Where large partials travelled as fixed point (a
+        // peaked softmax) the latter sums the bf16-rounded probabilities the
+        // P.V MMA multiplies, so that O is an exact convex combination of the
+        // V rows with the rounded weights; elsewhere it is the fp32 sum.
+        const bool rounded_sum = __any_sync(0xffffffffu, precise || peer_fixed);
+        uint64_t ps2[2] = {0ull, 0ull}, pr2[2] = {0ull, 0ull};
+        const uint64_t sl2 = f2(scale_log2, scale_log2), nm2 = f2(-msub, -msub);
 #pragma unroll
         for (int j = 0; j < 64; j += 2) {
-          const float2 d = f2_split(add2(f2(x[j], x[j + 1]), nm2));
+          const float2 d = f2_split(fma2(f2(x[j], x[j + 1]), sl2, nm2));
           const float p0 = ex2_approx(d.x);
           const float p1 = ex2_approx(d.y);
           const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
           ps2[(j >> 1) & 1] = add2(ps2[(j >> 1) & 1], f2(p0, p1));
           pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+          if (rounded_sum)
+            pr2[(j >> 1) & 1] = add2(pr2[(j >> 1) & 1], f2(__uint_as_float(pk[j / 2] << 16),
+                                                            __uint_as_float(pk[j / 2] & 0xffff0000u)));
         }
         {
           const float2 a = f2_split(ps2[0]), b2 = f2_split(ps2[1]);
-          l += (a.x + a.y) + (b2.x + b2.y);
+          const float ls = (a.x + a.y) + (b2.x + b2.y);
+          l += ls;
+          if (rounded_sum) {
+            const float2 c = f2_split(pr2[0]), d2 = f2_split(pr2[1]);
+            lr += (c.x + c.y) + (d2.x + d2.y);
+          } else {
+            lr += ls;
+          }
         }
         ATTN_TRACE(grp, gt, 4, lane == 0 && q4 == 0);
         // The heads of a warp decide separately whether their maximum moved,
@@ -408,16 +475,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       // group normalises and stores half of this CTA's O columns
       const int qb2 = qv & 1;
       B.lsum[qb2][grp][h] = l;
+      B.lrsum[qb2][grp][h] = lr;
       B.mseen[qb2][grp][h] = m_seen;
       mbar_arrive(&B.qend);
       if (!mbar_wait_warp(&B.qend, qb2, abort)) break;
       const float ma = B.mseen[qb2][0][h], mb = B.mseen[qb2][1][h];
       const float mf = fmaxf(ma, mb);
-      const float lt = mf == -INFINITY ? 0.f
-                                       : B.lsum[qb2][0][h] * ex2_approx(ma - mf) + B.lsum[qb2][1][h] * ex2_approx(mb - mf);
+      const float fa = mf == -INFINITY ? 0.f : ex2_approx(ma - mf), fb = mf == -INFINITY ? 0.f : ex2_approx(mb - mf);
+      const float lt = B.lsum[qb2][0][h] * fa + B.lsum[qb2][1][h] * fb;      // for LSE
+      const float ltr = B.lrsum[qb2][0][h] * fa + B.lrsum[qb2][1][h] * fb;   // for O
       if (!mbar_wait_warp(&B.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort)) break;
       tc_fence_after();
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float inv = ltr > 0.f ? 1.f / ltr : 0.f;
       uint4* o4 = reinterpret_cast<uint4*>(orow);
 #pragma unroll 1
       for (int c = 0; c < 128; c += 16) {

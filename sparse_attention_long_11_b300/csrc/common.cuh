@@ -73,6 +73,11 @@ __device__ __forceinline__ uint32_t score_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The score a key stands for (the inverse of score_key; -0 comes back as +0).
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // 64-bit selection key of a (score, position) pair: the score's key in the
 // high word, the complement of the position in the low word.  Larger means
 // selected first: higher score, then lower position; the keys of one row

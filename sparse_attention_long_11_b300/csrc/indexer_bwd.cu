@@ -456,6 +456,8 @@ cudaError_t launch_t(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer
 cudaError_t launch_indexer_kl_bwd(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
                                   const int32_t* idx, int k, const float* p, float* loss, float* grad_scores,
                                   float* dw, float* dq, float* dk, int* err, cudaStream_t stream) {
+  if (indexer_kl_bwd_tc_supported(ix))
+    return launch_indexer_kl_bwd_tc(qb, cm, ix, idx, k, p, loss, grad_scores, dw, dq, dk, err, stream);
   const bool fp8 = ix.dtype == DSA_FP8_E4M3;
   switch (ix.dim) {
     case 32:

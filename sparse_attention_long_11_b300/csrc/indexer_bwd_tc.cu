@@ -1,0 +1,466 @@
+// Indexer training step on the 5th-generation tensor cores (FP8 indexer
+// operands, 64 heads x 128): the alignment loss KL(p || softmax(I)) over a
+// query's candidate entries and its gradients (news article on DeepSeek-V3.2,
+// continued-pre-training section: the indexer learns from a Kullback-Leibler
+// loss against the main attention's distribution, over all keys in the dense
+// warm-up and over the selected entries in the sparse phase).
+//
+// Same quantities as the CUDA-core kernel (indexer_bwd.cu); with the code
+// dots x_je = <q8_j, k8_e>, m_je = [x_je > 0] and the dequantising scales:
+//   I_e  = sum_j w_j sq_j sk_e ReLU(x_je),  pi = softmax(I),  g_e = pi_e - p_e
+//   dq_j = w_j sum_e g_e m_je sk_e k8_e                  = w_j D[:, j]
+//   dw_j = sum_e g_e m_je sq_j sk_e x_je = sq_j <q8_j, D[:, j]>
+//   dk_e = sum_j (g_e w_j m_je sq_j) q8_j
+// with D = K8^T G, G_ej = g_e m_je sk_e.  The identity for dw is exact: the
+// only rounding it adds is that of G, as in dq.
+//
+// One CTA (four warps, thread = entry of a 128-entry tile = TMEM lane) per
+// query, two passes over the query's entries:
+//   pass 1  gather the tile's key rows, decode them to fp16 (exact for e4m3),
+//           X = K Q^T on the tensor cores (kind::f16, M = 128 entries,
+//           N = 64 heads, K = 128 dims, fp32 accumulate: each product is
+//           exact, the sum is an fp32 sum); per entry its I and the 64-bit
+//           head mask, a dot within 1e-5 |q_j| |k_e| of zero re-decided in
+//           fp64 (exact for e4m3 products; the fp32 sum errs by less than
+//           127 2^-24 |q_j| |k_e|);
+//   then    pi, g, the loss; power-of-two scales that put G and B = g w m sq
+//           in fp16's normal range;
+//   pass 2  gather the tile again; write G and B (fp16, scaled) and run
+//           D += K^T G (M = 128 dims, N = 64 heads, K = 128 entries, both
+//           operands read MN-major from the rows just written) and
+//           dK = B Q8 (M = 128 entries, N = 128 dims, K = 64 heads); the dK
+//           rows are added to dk with vector atomics.
+//   end     dq and dw from D (TMEM lane = dim).
+// Operands of the gradient contractions are rounded once to fp16 (2^-11
+// relative), well inside the 1e-3 tolerance of each sum's magnitude.
+#include <algorithm>
+#include <cmath>
+
+#include "launch.h"
+#include "tc.cuh"
+
+namespace dsa {
+namespace {
+using namespace tc;
+
+constexpr int kThreads = 128;
+constexpr int kHI = 64, kDI = 128, kTile = 128;
+constexpr uint32_t kQHalf = kHI * 128;        // 64 heads x 64 dims (fp16), one 128B-swizzled half
+constexpr uint32_t kKHalf = kTile * 128;      // 128 entries x 64 dims (fp16)
+constexpr uint32_t kOffQ = 0;                 // Q: two halves (dims 0-63, 64-127)
+constexpr uint32_t kOffK = kOffQ + 2 * kQHalf;    // key tile: two halves
+constexpr uint32_t kOffG = kOffK + 2 * kKHalf;    // G: 128 entries x 64 heads (fp16)
+constexpr uint32_t kOffB = kOffG + kTile * 128;   // B: 128 entries x 64 heads (fp16)
+constexpr uint32_t kOffArr = kOffB + kTile * 128; // per entry: I then g (fp32), mask (u64)
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemX = 0, kTmemD = 64, kTmemK = 128;
+
+// fp16 instruction descriptor: D fp32, A and B fp16, M x N, majors as given.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+// Four e4m3 codes (one 32-bit word, memory order) -> two f16x2 words.
+__device__ __forceinline__ uint2 e4m3x4_to_f16(uint32_t c) {
+  uint2 r;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+      : "=r"(r.x), "=r"(r.y)
+      : "r"(c));
+  return r;
+}
+__device__ __forceinline__ float f16_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFF))); }
+__device__ __forceinline__ float f16_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+__device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+struct BwdShared {
+  uint64_t mma;
+  float qn[kHI], wv[kHI], sqv[kHI];
+  float red[kThreads / 32];
+  float dwp[kThreads / 32][kHI];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ float block_reduce(float v, float* red, bool is_max) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, u) : v + u;
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = red[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) t = is_max ? fmaxf(t, red[w]) : t + red[w];
+  return t;
+}
+
+// 2^e with e the exponent that puts v (> 0) just below 2^14.
+__device__ __forceinline__ float fp16_scale(float v) {
+  if (!(v > 0.f) || !isfinite(v)) return 1.f;
+  int e;
+  frexpf(v, &e);   // v < 2^e
+  return ldexpf(1.f, 14 - e);
+}
+
+// The exact dot of key row krow's 128 codes with head j of the query (fp16
+// rows in the 128B-swizzled halves at sq) in fp64: every product of two e4m3
+// values and every partial sum is exact in fp64.  The rare path of the sign
+// decision; kept out of line.
+__device__ __noinline__ double exact_code_dot(const uint8_t* krow, const uint8_t* sq, int j) {
+  double acc = 0.0;
+  const uint32_t* kw = reinterpret_cast<const uint32_t*>(krow);
+  for (int q = 0; q < kDI / 4; ++q) {   // dims 4q .. 4q + 3
+    const uint2 f = e4m3x4_to_f16(__ldg(kw + q));
+    const int d0 = 4 * q;
+    const uint8_t* chunk = sq + (d0 >> 6) * kQHalf + sw128_offset(j, (d0 & 63) >> 3) + 2 * (d0 & 7);
+    const uint32_t qw0 = *reinterpret_cast<const uint32_t*>(chunk);
+    const uint32_t qw1 = *reinterpret_cast<const uint32_t*>(chunk + 4);
+    acc = fma((double)f16_lo(f.x), (double)f16_lo(qw0), acc);
+    acc = fma((double)f16_hi(f.x), (double)f16_hi(qw0), acc);
+    acc = fma((double)f16_lo(f.y), (double)f16_lo(qw1), acc);
+    acc = fma((double)f16_hi(f.y), (double)f16_hi(qw1), acc);
+  }
+  return acc;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__ q8, const float* __restrict__ q_scale,
+                         const float* __restrict__ w, const uint8_t* __restrict__ k8, const float* __restrict__ k_scale,
+                         const int32_t* __restrict__ idx, int kk, const float* __restrict__ p,
+                         float* __restrict__ loss, float* __restrict__ grad_scores, float* __restrict__ dw,
+                         float* __restrict__ dq, float* __restrict__ dk, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ BwdShared S;
+  float* Ie = reinterpret_cast<float*>(sm + kOffArr);                        // [kk] I, then g
+  uint64_t* msk = reinterpret_cast<uint64_t*>(sm + kOffArr + ((4 * kk + 15) & ~15));   // [kk]
+  const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int* abort = &S.abort;
+  const uint32_t sQ = smem_u32(sm + kOffQ), sK = smem_u32(sm + kOffK), sG = smem_u32(sm + kOffG),
+                 sB = smem_u32(sm + kOffB);
+
+  const int pos = __ldg(qb.q_pos + t), seq = __ldg(qb.q_seq + t);
+  if (pos < 0 || pos >= qb.max_kv) {
+    if (tid == 0) {
+      flag_error(err, DSA_ERR_BOUNDS);
+      loss[t] = 0.f;
+    }
+    for (int j = tid; j < kHI; j += kThreads) dw[(int64_t)t * kHI + j] = 0.f;
+    for (int e = tid; e < kHI * kDI; e += kThreads) dq[(int64_t)t * kHI * kDI + e] = 0.f;
+    if (grad_scores)
+      for (int e = tid; e < kk; e += kThreads) grad_scores[(int64_t)t * kk + e] = 0.f;
+    return;
+  }
+  const int32_t* irow = idx + (int64_t)t * kk;
+  const float* prow = p + (int64_t)t * kk;
+
+  if (tid == 0) {
+    mbar_init(&S.mma, 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&S.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  // ---- the query: Q8 as fp16 (thread = head, half), code norms, weights, scales
+  {
+    const int j = tid >> 1, h = tid & 1;
+    const uint4* src = reinterpret_cast<const uint4*>(q8 + ((int64_t)t * kHI + j) * kDI + 64 * h);
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {   // 16 codes -> two 16-byte chunks of fp16
+      const uint4 v = __ldg(src + c);
+      const uint32_t cw[4] = {v.x, v.y, v.z, v.w};
+      uint32_t hw[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint2 f = e4m3x4_to_f16(cw[q]);
+        hw[2 * q] = f.x;
+        hw[2 * q + 1] = f.y;
+        const float a = f16_lo(f.x), b = f16_hi(f.x), c2 = f16_lo(f.y), d = f16_hi(f.y);
+        ss = fmaf(a, a, fmaf(b, b, fmaf(c2, c2, fmaf(d, d, ss))));
+      }
+      *reinterpret_cast<uint4*>(sm + kOffQ + h * kQHalf + sw128_offset(j, 2 * c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(sm + kOffQ + h * kQHalf + sw128_offset(j, 2 * c + 1)) =
+          make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    if (h == 0) {
+      S.qn[j] = sqrtf(ss);
+      S.wv[j] = __ldg(w + (int64_t)t * kHI + j);
+      S.sqv[j] = __ldg(q_scale + (int64_t)t * kHI + j);
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  uint32_t nmma = 0;   // MMA commits waited on (barrier phase)
+  bool ok = true;
+
+  // This thread's entry of tile e0: its key row decoded to fp16 into row tid
+  // of the key tile, its physical row, key scale and code norm.
+  auto gather = [&](int e0, int& row_out, float& sk_out, float& kn_out) {
+    const int e = e0 + tid;
+    int64_t row = -1;
+    if (e < kk) {
+      const int s = __ldg(irow + e);
+      if (s >= 0 && s <= pos) row = cache_row(cm, seq, s, err);
+      else if (s != -1) flag_error(err, DSA_ERR_BOUNDS);
+    }
+    row_out = (int)row;
+    sk_out = row >= 0 ? __ldg(k_scale + row) : 0.f;
+    const uint4* src = reinterpret_cast<const uint4*>(k8 + (row >= 0 ? row : 0) * kDI);
+    uint4 codes[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) codes[c] = row >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t cw[4] = {codes[c].x, codes[c].y, codes[c].z, codes[c].w};
+      uint32_t hw[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint2 f = e4m3x4_to_f16(cw[q]);
+        hw[2 * q] = f.x;
+        hw[2 * q + 1] = f.y;
+        const float a = f16_lo(f.x), b = f16_hi(f.x), c2 = f16_lo(f.y), d = f16_hi(f.y);
+        ss = fmaf(a, a, fmaf(b, b, fmaf(c2, c2, fmaf(d, d, ss))));
+      }
+      // 16 codes -> fp16 chunks 2(c%4), 2(c%4)+1 of half c/4
+      const uint32_t base = kOffK + (c >> 2) * kKHalf;
+      *reinterpret_cast<uint4*>(sm + base + sw128_offset(tid, 2 * (c & 3))) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(sm + base + sw128_offset(tid, 2 * (c & 3) + 1)) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    }
+    kn_out = sqrtf(ss);
+  };
+  // One thread issues `fn`'s MMAs and commits; every thread waits for them.
+  auto mma_round = [&](auto fn) -> bool {
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      fn();
+      mma_commit(&S.mma);
+    }
+    const bool r = mbar_wait_warp(&S.mma, nmma & 1, abort);
+    ++nmma;
+    tc_fence_after();
+    return r;
+  };
+
+  // ---------------------------------------------------------------- pass 1
+  float smax = 0.f;   // largest key scale among valid entries (this thread)
+  for (int e0 = 0; e0 < kk && ok; e0 += kTile) {
+    int row;
+    float sk, kn;
+    gather(e0, row, sk, kn);
+    if (row >= 0) smax = fmaxf(smax, sk);
+    ok = mma_round([&] {
+#pragma unroll
+      for (int s = 0; s < 8; ++s)   // K = 128 dims in steps of 16
+        mma_bf16(tmem + kTmemX, sdesc(sK + (s >> 2) * kKHalf + (s & 3) * 32, 16, 1024),
+                 sdesc(sQ + (s >> 2) * kQHalf + (s & 3) * 32, 16, 1024), idesc_f16(128, kHI, false, false),
+                 s > 0 ? 1u : 0u);
+    });
+    if (!ok) break;
+    const int e = e0 + tid;
+    uint64_t m = 0ull;
+    float iv = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {   // 16 heads at a time, straight from TMEM
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_base + kTmemX + 16 * c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int j = 16 * c + u;
+        float xv = __uint_as_float(r[u]);
+        const float bound = 1e-5f * S.qn[j] * kn;
+        bool posv = xv > 0.f;
+        if (row >= 0 && bound > 0.f && fabsf(xv) <= bound) {   // near zero: decide the sign exactly
+          const double exact = exact_code_dot(k8 + (int64_t)row * kDI, sm + kOffQ, j);
+          posv = exact > 0.0;
+          xv = (float)exact;
+        }
+        if (posv) {
+          m |= 1ull << j;
+          iv = fmaf(S.wv[j], xv * S.sqv[j] * sk, iv);
+        }
+      }
+    }
+    if (e < kk) {
+      Ie[e] = row >= 0 ? iv : -INFINITY;
+      msk[e] = row >= 0 ? m : 0ull;
+    }
+    tc_fence_before();
+    __syncthreads();   // the key tile and X are rewritten by the next tile
+  }
+
+  // ---------------------------------------------------------------- pi, g, loss, scales
+  float lmax = -INFINITY;
+  for (int e = tid; e < kk; e += kThreads) lmax = fmaxf(lmax, Ie[e]);
+  const float M = block_reduce(lmax, S.red, true);
+  float zp = 0.f;
+  if (M != -INFINITY)
+    for (int e = tid; e < kk; e += kThreads) zp += Ie[e] == -INFINITY ? 0.f : __expf(Ie[e] - M);
+  const float Z = block_reduce(zp, S.red, false);
+  const float logZ = logf(Z);
+  float lpart = 0.f, gmax = 0.f;
+  for (int e = tid; e < kk; e += kThreads) {
+    const float iv = Ie[e];
+    float g = 0.f;
+    if (iv != -INFINITY) {
+      const float lpi = iv - M - logZ;
+      const float pe = __ldg(prow + e);
+      g = __expf(lpi) - pe;
+      if (pe > 0.f) lpart += pe * (logf(pe) - lpi);
+    }
+    Ie[e] = g;
+    gmax = fmaxf(gmax, fabsf(g));
+    if (grad_scores) grad_scores[(int64_t)t * kk + e] = g;
+  }
+  const float lsum = block_reduce(lpart, S.red, false);
+  if (tid == 0) loss[t] = M == -INFINITY ? 0.f : lsum;
+  gmax = block_reduce(gmax, S.red, true);
+  smax = block_reduce(smax, S.red, true);
+  float wsmax = 0.f;
+  for (int j = tid; j < kHI; j += kThreads) wsmax = fmaxf(wsmax, fabsf(S.wv[j] * S.sqv[j]));
+  wsmax = block_reduce(wsmax, S.red, true);
+  const float scG = fp16_scale(gmax * smax), scB = fp16_scale(gmax * wsmax);   // G, B scaled below 2^14
+  __syncthreads();
+
+  // ---------------------------------------------------------------- pass 2
+  for (int e0 = 0; e0 < kk && ok; e0 += kTile) {
+    int row;
+    float sk, kn;
+    gather(e0, row, sk, kn);
+    const int e = e0 + tid;
+    const uint64_t m = e < kk ? msk[e] : 0ull;
+    const float ge = e < kk ? Ie[e] : 0.f;
+    {   // this entry's rows of G (g m sk) and B (g w m sq), scaled, as fp16
+      const float gs = ge * sk * scG;
+      const float gb = ge * scB;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t hg[4], hb[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = 8 * c + 2 * q;
+          const bool m0 = (m >> j) & 1ull, m1 = (m >> (j + 1)) & 1ull;
+          hg[q] = f16x2(m0 ? gs : 0.f, m1 ? gs : 0.f);
+          hb[q] = f16x2(m0 ? gb * S.wv[j] * S.sqv[j] : 0.f, m1 ? gb * S.wv[j + 1] * S.sqv[j + 1] : 0.f);
+        }
+        *reinterpret_cast<uint4*>(sm + kOffG + sw128_offset(tid, c)) = make_uint4(hg[0], hg[1], hg[2], hg[3]);
+        *reinterpret_cast<uint4*>(sm + kOffB + sw128_offset(tid, c)) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+      }
+    }
+    const bool first = e0 == 0;
+    ok = mma_round([&] {
+      // D[d][j] += sum_e K[e][d] G[e][j]: A = the key tile read MN-major (128 dims
+      // in two 64-dim blocks), B = G MN-major; 8 steps of 16 entries
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        mma_bf16(tmem + kTmemD, sdesc(sK + s * 2048, kKHalf, 1024), sdesc(sG + s * 2048, 8192, 1024),
+                 idesc_f16(128, kHI, true, true), (first && s == 0) ? 0u : 1u);
+      // dK[e][d] = sum_j B[e][j] Q[j][d]: A = B K-major, B = Q read MN-major
+      // (128 dims in two 64-dim blocks); 4 steps of 16 heads
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma_bf16(tmem + kTmemK, sdesc(sB + s * 32, 16, 1024), sdesc(sQ + s * 2048, kQHalf, 1024),
+                 idesc_f16(128, kDI, false, true), s > 0 ? 1u : 0u);
+    });
+    if (!ok) break;
+    {   // dk of this entry's key row (the TMEM loads are warp-collective: every lane loads)
+      const bool add = row >= 0 && m != 0ull && ge != 0.f;
+      const float inv = 1.f / scB;
+      float* dst = dk + (int64_t)(row >= 0 ? row : 0) * kDI;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_base + kTmemK + 16 * c, r);
+        tmem_ld_wait();
+        if (add) {
+#pragma unroll
+          for (int u = 0; u < 16; u += 4)
+            atomicAdd(reinterpret_cast<float4*>(dst + 16 * c + u),
+                      make_float4(__uint_as_float(r[u]) * inv, __uint_as_float(r[u + 1]) * inv,
+                                  __uint_as_float(r[u + 2]) * inv, __uint_as_float(r[u + 3]) * inv));
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+
+  // ---------------------------------------------------------------- dq, dw (thread = dim)
+  if (ok) {
+    const int d = tid;
+    const float inv = 1.f / scG;
+    const bool any = kk > 0 && M != -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t r[16];
+      tmem_ld16(tmem + lane_base + kTmemD + 16 * c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int j = 16 * c + u;
+        const float Dv = any ? __uint_as_float(r[u]) * inv : 0.f;
+        dq[((int64_t)t * kHI + j) * kDI + d] = S.wv[j] * Dv;
+        // q8[j][d] (fp16, exact) times D[d][j]: this thread's term of dw_j
+        const uint32_t qw = *reinterpret_cast<const uint32_t*>(
+            sm + kOffQ + (d >> 6) * kQHalf + sw128_offset(j, (d & 63) >> 3) + 2 * (d & 6));
+        const float qv = (d & 1) ? f16_hi(qw) : f16_lo(qw);
+        float v = qv * Dv;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) S.dwp[warp][j] = v;
+      }
+    }
+    __syncthreads();
+    if (tid < kHI) {
+      const float s = (S.dwp[0][tid] + S.dwp[1][tid]) + (S.dwp[2][tid] + S.dwp[3][tid]);
+      dw[(int64_t)t * kHI + tid] = S.sqv[tid] * s;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (tid == 0 && S.abort) flag_error(err, DSA_ERR_TIMEOUT);
+}
+
+}  // namespace
+
+bool indexer_kl_bwd_tc_supported(const dsa_indexer_inputs& ix) {
+  return ix.dtype == DSA_FP8_E4M3 && ix.heads == kHI && ix.dim == kDI;
+}
+
+cudaError_t launch_indexer_kl_bwd_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
+                                     const int32_t* idx, int k, const float* p, float* loss, float* grad_scores,
+                                     float* dw, float* dq, float* dk, int* err, cudaStream_t stream) {
+  const size_t smem = kOffArr + ((4 * (size_t)k + 15) & ~size_t(15)) + 8 * (size_t)k + 1024;
+  cudaError_t e = cudaFuncSetAttribute(indexer_kl_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  indexer_kl_bwd_tc_kernel<<<qb.num_q, kThreads, smem, stream>>>(
+      qb, cm, static_cast<const uint8_t*>(ix.q), ix.q_scale, ix.w, static_cast<const uint8_t*>(ix.k), ix.k_scale, idx,
+      k, p, loss, grad_scores, dw, dq, dk, err);
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -30,9 +30,27 @@ __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
   return d;
 }
 
+// Heads 4m + 2 and 4m + 3 take their ReLU on the FMA pipe, the others a max
+// on the ALU pipe, so the two pipes share the epilogue's per-element work.
+// On the FMA pipe: sat(2^-25 x) = 2^-25 ReLU(x) exactly for every code dot
+// (|x| <= 128 * 448^2 < 2^25 and the smallest nonzero |x| is 2^-18, so the
+// scaled value neither saturates high nor leaves the normal range); those
+// heads' folded weights carry the factor 2^25 (fold_weight), and the product
+// of the two scaled factors is exactly the unscaled product, so the scores
+// are bit for bit those of a max on every head.
+constexpr float kReluScale = 0x1p-25f;
+__host__ __device__ __forceinline__ float fold_weight(int head, float w) {
+  return (head & 2) ? w * 0x1p25f : w;
+}
+__device__ __forceinline__ float relu_scaled(float x) {
+  float y;
+  asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(y) : "f"(x), "f"(kReluScale));
+  return y;
+}
+
 // Weighted ReLU sum over 16 heads: r[i] is the raw dot of head h0 + i,
-// w4[0..3] the folded weights of those heads.  Two packed accumulators
-// (heads 4m, 4m+1 and 4m+2, 4m+3), added at the end.
+// w4[0..3] the folded weights of those heads (fold_weight applied).  Two
+// packed accumulators (heads 4m, 4m+1 and 4m+2, 4m+3), added at the end.
 __device__ __forceinline__ float head_partial(const uint32_t (&r)[16], const float4* w4) {
   uint64_t a = 0ull, b = 0ull;
 #pragma unroll
@@ -41,7 +59,7 @@ __device__ __forceinline__ float head_partial(const uint32_t (&r)[16], const flo
     a = ffma2(pack2(wv.x, wv.y),
               pack2(fmaxf(__uint_as_float(r[4 * m]), 0.f), fmaxf(__uint_as_float(r[4 * m + 1]), 0.f)), a);
     b = ffma2(pack2(wv.z, wv.w),
-              pack2(fmaxf(__uint_as_float(r[4 * m + 2]), 0.f), fmaxf(__uint_as_float(r[4 * m + 3]), 0.f)), b);
+              pack2(relu_scaled(__uint_as_float(r[4 * m + 2])), relu_scaled(__uint_as_float(r[4 * m + 3]))), b);
   }
   float alo, ahi, blo, bhi;
   unpack2(a, alo, ahi);

@@ -57,7 +57,10 @@ constexpr uint32_t kSmemAlloc = kSmemBytes + 1024;
 constexpr int kThreads = 576;
 constexpr int kEpiThreads = 512;
 
+constexpr int kStageCap = 128;                  // candidates an epilogue warp stages before a flush (kFilter)
+
 struct __align__(16) Shared {
+  uint64_t stage[kEpiThreads / 32][kStageCap];  // kFilter: each epilogue warp's admitted candidates
   uint64_t a_full[kStagesA], a_empty[kStagesA], d_full[2], d_empty[2];
   uint64_t b_full[2], b_empty[2], epi_sync[2], fin;
   alignas(16) float wq[2][kQG][kHI];   // w * q_scale of the item's group (double buffered; read as float4)
@@ -87,13 +90,23 @@ __device__ long long g_idx_trace[3][1024][4];
 // ordinal to its key tile.
 struct TileMap {
   int mode, m;
+  uint32_t inv;   // kFilter: division by m - 1 as a multiply-high (exact for ordinals and m below 2^16)
   __device__ __forceinline__ int count(int T) const {
     return mode == IndexerOut::kFull ? T : mode == IndexerOut::kSample ? (T + m - 1) / m : T - (T + m - 1) / m;
   }
   __device__ __forceinline__ int tile(int o) const {
-    return mode == IndexerOut::kFull ? o : mode == IndexerOut::kSample ? o * m : (o / (m - 1)) * m + 1 + o % (m - 1);
+    if (mode == IndexerOut::kFull) return o;
+    if (mode == IndexerOut::kSample) return o * m;
+    const int q = m == 2 ? o : (int)__umulhi((uint32_t)o, inv);   // o / (m - 1)
+    return q * m + 1 + (o - q * (m - 1));
   }
 };
+
+// The multiply-high reciprocal of d >= 2 (o / d == umulhi(o, r) for o, d < 2^16;
+// d = 1 needs 2^32 and is handled by the caller).
+__host__ __device__ __forceinline__ uint32_t recip32(uint32_t d) {
+  return d <= 1u ? 0u : (uint32_t)(0xffffffffull / d) + 1u;
+}
 
 // One group of 4 consecutive query rows: either one pass over a shared
 // sequence (uniform) or one pass per active query.
@@ -189,26 +202,57 @@ __device__ __forceinline__ int item_tiles(const Group& G, int c, int ch) {
   return n;
 }
 
+// kFilter: an epilogue warp's staged candidates (warp-uniform state): the
+// query row they belong to and how many are staged in its buffer.
+struct Stager {
+  int row = -1;
+  uint32_t n = 0;
+};
+
+// Appends the staged candidates to the query's list: one atomic reserves
+// their slots, then the warp copies them (entries past the list's capacity
+// are counted but not stored).  Called by a whole warp.
+__device__ __forceinline__ void stage_flush(const IndexerOut& o, Stager& st, const uint64_t* buf, int lane) {
+  if (st.n == 0) return;
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(o.cnt + st.row, st.n);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  __syncwarp();
+  uint64_t* dst = o.cand + (int64_t)st.row * o.cap;
+  for (uint32_t i = lane; i < st.n; i += 32)
+    if (base + i < (uint32_t)o.cap) dst[base + i] = buf[i];
+  __syncwarp();
+  st.n = 0;
+}
+
 // Output of one (key, query) score, by mode.  Called by a whole warp (the
-// filter appends with a warp ballot): row_q, t (the tile's ordinal) and thr
+// filter stages with a warp ballot): row_q, t (the tile's ordinal) and thr
 // are warp-uniform, s is this lane's key, live whether it is a causal key of
 // a valid query with a readable cache row.
 __device__ __forceinline__ void emit(const IndexerOut& o, const QueryBatch& qb, int row_q, int t, int s, float sc,
-                                     bool live, uint64_t thr, int lane) {
+                                     bool live, uint64_t thr, int lane, Stager& st, uint64_t* buf) {
   if (o.mode == IndexerOut::kFull) {
     if (s < qb.max_kv && row_q < qb.num_q) o.scores[(int64_t)row_q * o.ld + s] = live ? sc : -INFINITY;
   } else if (o.mode == IndexerOut::kSample) {
     if (row_q < qb.num_q) o.scores[(int64_t)row_q * o.ld + t * kKT + (s & (kKT - 1))] = live ? sc : -INFINITY;
   } else {
-    const uint64_t ck = composite_key(sc, s);
-    const bool admit = live && row_q < qb.num_q && ck >= thr;
+    // composite key >= thr, decided on the score (the high word orders like
+    // the score with -0 == +0) and the position (the low word)
+    // (a threshold of 0 admits every key: its high word stands for no score)
+    const float ts = key_score((uint32_t)(thr >> 32));
+    const int tp = composite_pos(thr);
+    const bool admit = live && row_q < qb.num_q && (thr == 0ull || sc > ts || (sc == ts && s <= tp));
     const uint32_t m = __ballot_sync(0xffffffffu, admit);
-    if (m) {
-      uint32_t base = 0;
-      if (lane == 0) base = atomicAdd(o.cnt + row_q, (uint32_t)__popc(m));
-      base = __shfl_sync(0xffffffffu, base, 0) + __popc(m & ((1u << lane) - 1u));
-      if (admit && base < (uint32_t)o.cap) o.cand[(int64_t)row_q * o.cap + base] = ck;
+    if (!m) return;
+    const uint64_t ck = composite_key(sc, s);
+    if (st.row != row_q) {   // the warp moves on to another query's candidates
+      stage_flush(o, st, buf, lane);
+      st.row = row_q;
     }
+    const uint32_t nn = __popc(m);
+    if (st.n + nn > (uint32_t)kStageCap) stage_flush(o, st, buf, lane);
+    if (admit) buf[st.n + __popc(m & ((1u << lane) - 1u))] = ck;
+    st.n += nn;
   }
 }
 
@@ -224,7 +268,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   volatile int* abort = &S.abort;
   const uint32_t sB = smem_u32(sm), sA = smem_u32(sm + kOffA);
   const int n_items = ngroups * nchunk;
-  const TileMap tmap{out.mode, out.m};
+  const TileMap tmap{out.mode, out.m, recip32((uint32_t)max(out.m - 1, 1))};
   float* __restrict__ scores = out.scores;
   const int64_t ld = out.ld;
 
@@ -395,6 +439,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // ------------------------------------------------------------ epilogue
     const int qd = warp & 3, uq = (warp - 2) >> 2, et = tid - 64;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    Stager stg;
+    uint64_t* sbuf = S.stage[warp - 2];
     uint32_t dq = 0, j = 0;   // accumulator-buffer uses, items with tiles
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
       const int gi = item % ngroups, c = item / ngroups;
@@ -405,8 +451,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         {   // folded weights of this group (threads et < 256 fetch one each)
           if (et < kQG * kHI) {
             const int qq = et / kHI, jj = et % kHI, r = gi * kQG + qq;
-            S.wq[bb][qq][jj] =
-                r < qb.num_q ? __ldg(w + (int64_t)r * kHI + jj) * __ldg(q_scale + (int64_t)r * kHI + jj) : 0.f;
+            S.wq[bb][qq][jj] = r < qb.num_q ? idx_epi::fold_weight(jj, __ldg(w + (int64_t)r * kHI + jj) *
+                                                                           __ldg(q_scale + (int64_t)r * kHI + jj))
+                                            : 0.f;
           }
           mbar_arrive(&S.epi_sync[bb]);
           if (!mbar_wait_warp(&S.epi_sync[bb], (j >> 1) & 1, abort, wait_limit)) break;
@@ -438,7 +485,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             IDX_TRACE(2, dq, 1, et == 0);
             tc_fence_after();
             const float acc = idx_epi::head_sum64(tmem + lane_base + 256 * b + uq * 64, wq4);
-            emit(out, qb, row_q, t, s, acc * sk, q_act && key_ok && s <= q_pos, thr, lane);
+            emit(out, qb, row_q, t, s, acc * sk, q_act && key_ok && s <= q_pos, thr, lane, stg, sbuf);
             tc_fence_before();
             mbar_arrive(&S.d_empty[b]);
             IDX_TRACE(2, dq, 2, et == 0);
@@ -474,13 +521,14 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // not depend on its batch
             const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][qq]);
             const float acc = idx_epi::head_sum64(tmem + lane_base + 256 * b + uq * 64, wq4);
-            emit(out, qb, row_q, t, s, acc * sk, G.active[qq] && key_ok && s <= G.pos[qq], thr, lane);
+            emit(out, qb, row_q, t, s, acc * sk, G.active[qq] && key_ok && s <= G.pos[qq], thr, lane, stg, sbuf);
           }
           tc_fence_before();
           mbar_arrive(&S.d_empty[b]);
           IDX_TRACE(2, dq, 2, et == 0);
         }
         if (!ok) break;
+        if (out.mode == IndexerOut::kFilter) stage_flush(out, stg, sbuf, lane);
         ++j;
       }
       // the item holding a group's last chunk also writes -inf from the end

@@ -122,11 +122,24 @@ inline cudaError_t launch_attn(const QueryBatch& qb, const CacheMap& cm, const d
   return launch_attn_simt(qb, cm, at, idx, k, out, lse, err, stream);
 }
 
+// Per-head (non-absorbed) sparse attention, the prefill attention mode:
+// bf16, heads a multiple of 8, per-head keys and values of 128 and a shared
+// rope part of 64 (attn_mha.cu).
+cudaError_t launch_attn_mha(const QueryBatch& qb, const CacheMap& cm, int heads, const void* q, const void* k_nope,
+                            const void* k_rope, const void* v, float softmax_scale, const int32_t* idx, int k,
+                            void* out, float* lse, int* err, cudaStream_t stream);
+
 // Indexer alignment loss KL(p || softmax(I)) over each query's candidate
-// entries and its gradients for w, q and k (dk accumulated).  CUDA cores.
+// entries and its gradients for w, q and k (dk accumulated): on the tensor
+// cores for FP8 operands with 64 heads x 128 (indexer_bwd_tc.cu), on CUDA
+// cores otherwise.
 cudaError_t launch_indexer_kl_bwd(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
                                   const int32_t* idx, int k, const float* p, float* loss, float* grad_scores,
                                   float* dw, float* dq, float* dk, int* err, cudaStream_t stream);
+bool indexer_kl_bwd_tc_supported(const dsa_indexer_inputs& ix);
+cudaError_t launch_indexer_kl_bwd_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,
+                                     const int32_t* idx, int k, const float* p, float* loss, float* grad_scores,
+                                     float* dw, float* dq, float* dk, int* err, cudaStream_t stream);
 
 // Appends new tokens to the caches: each key row (128 bf16 or fp32 values)
 // encoded as e4m3 codes with scale amax/448, and (when kv_new is non-null)

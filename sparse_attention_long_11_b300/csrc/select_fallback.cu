@@ -97,7 +97,8 @@ sel_fallback_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int i = S.row;
     const int seq = __ldg(qb.q_seq + i), pos = __ldg(qb.q_pos + i);
     const int n = pos + 1, T = (n + kKT - 1) / kKT;
-    if (tid < kHI) S.wq[tid] = __ldg(w + (int64_t)i * kHI + tid) * __ldg(q_scale + (int64_t)i * kHI + tid);
+    if (tid < kHI)
+      S.wq[tid] = idx_epi::fold_weight(tid, __ldg(w + (int64_t)i * kHI + tid) * __ldg(q_scale + (int64_t)i * kHI + tid));
     __syncthreads();
 
     if (warp == 4) {

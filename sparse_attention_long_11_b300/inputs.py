@@ -341,3 +341,39 @@ def random_index_sets(q_pos: torch.Tensor, k: int, seed: int) -> torch.Tensor:
             sel = torch.randperm(n, generator=g)[:k].sort().values
             out[i] = sel.to(torch.int32)
     return out
+
+
+@dataclasses.dataclass
+class MhaWorkload:
+    """Inputs of the per-head (non-absorbed) attention mode for one
+    single-sequence causal prefill: per-head key rows k_nope [L, H, 128], the
+    shared rope part k_rope [L, 64] and per-head values v [L, H, 128], bf16
+    ~ N(0,1); queries q [nq, H, 192] at positions q_pos; softmax scale
+    1/sqrt(192).  Cache rows are contiguous (row = position)."""
+    q: torch.Tensor
+    k_nope: torch.Tensor
+    k_rope: torch.Tensor
+    v: torch.Tensor
+    q_seq: torch.Tensor
+    q_pos: torch.Tensor
+    L: int
+    softmax_scale: float
+
+    @property
+    def num_q(self) -> int:
+        return int(self.q_pos.shape[0])
+
+    @property
+    def heads(self) -> int:
+        return int(self.q.shape[1])
+
+
+def make_mha_prefill(seed=0, device="cpu", L=4096, heads=128, q_rows: Optional[Tuple[int, int]] = None) -> MhaWorkload:
+    a, b = q_rows if q_rows is not None else (0, L)
+    q_seq, q_pos = _runs_layout([(0, a, b - a)], device)
+    return MhaWorkload(
+        q=_bf16_normal((b - a, heads, 192), seed, "mha_q", device),
+        k_nope=_bf16_normal((L, heads, 128), seed, "mha_k_nope", device),
+        k_rope=_bf16_normal((L, 64), seed, "mha_k_rope", device),
+        v=_bf16_normal((L, heads, 128), seed, "mha_v", device),
+        q_seq=q_seq, q_pos=q_pos, L=L, softmax_scale=1.0 / math.sqrt(192))

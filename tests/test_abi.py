@@ -93,6 +93,9 @@ def test_host_validation_rejects_before_launch():
     assert f(*args(ix=_ix(addr=0x10004))) == api.DSA_ERR_INVALID_ARG           # misaligned operand
     assert f(*args(ix=_ix(dtype=api.DSA_BF16))) == api.DSA_ERR_UNSUPPORTED
     assert f(*args(at=_at(heads=64))) == api.DSA_ERR_UNSUPPORTED
+    neg = _at()
+    neg.softmax_scale = -0.04
+    assert f(*args(at=neg)) == api.DSA_ERR_INVALID_ARG                        # tensor-core attention: scale > 0
     # FP8 latent cache: the per-row scales are required, 4-byte aligned, and only with that dtype
     assert f(*args(at=_at(dtype=api.DSA_FP8_E4M3))) == api.DSA_ERR_INVALID_ARG
     assert f(*args(at=_at(dtype=api.DSA_FP8_E4M3, kv_scale=0x10002))) == api.DSA_ERR_INVALID_ARG
