@@ -235,6 +235,16 @@ DSA_API size_t dsa_forward_workspace_size(const dsa_query_desc* qd, const dsa_in
 DSA_API size_t dsa_forward_stage_workspace_size(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
                                                 const dsa_attn_inputs* at, int64_t stage_rows);
 
+/* The number of query rows per stage that dsa_forward runs with a workspace
+ * of workspace_bytes (its stages are equal in size, so this is
+ * ceil(num_q / stages)); 0 if the workspace is below the least
+ * dsa_forward accepts or the arguments are invalid.  A workspace of
+ * dsa_forward_workspace_size() bytes runs the whole batch in one stage
+ * whenever that size is below the recommended cap.  Host-side only: no
+ * device work, no pointer is dereferenced. */
+DSA_API int64_t dsa_forward_stage_rows(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
+                                       const dsa_attn_inputs* at, size_t workspace_bytes);
+
 /* The whole hot path: indexer -> top-k -> sparse attention for a batch of
  * prefill chunks and/or decode tokens.  Writes idx [num_q, k] (the selected
  * positions, exactly as dsa_topk would write them for dsa_index_scores'

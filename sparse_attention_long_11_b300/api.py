@@ -74,6 +74,8 @@ _SIGS = {
                                                      _P(AttnInputs)]),
     "dsa_forward_stage_workspace_size": (ctypes.c_size_t, [_P(QueryDesc), _P(IndexerInputs), ctypes.c_int32,
                                                            _P(AttnInputs), ctypes.c_int64]),
+    "dsa_forward_stage_rows": (ctypes.c_int64, [_P(QueryDesc), _P(IndexerInputs), ctypes.c_int32,
+                                                _P(AttnInputs), ctypes.c_size_t]),
     "dsa_forward": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(IndexerInputs), ctypes.c_int32,
                                    _P(AttnInputs), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                    ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
@@ -228,6 +230,12 @@ def dsa_forward_stage_workspace_size(batch: QueryDesc, ix: IndexerInputs, k: int
                                      stage_rows: int) -> int:
     return int(lib().dsa_forward_stage_workspace_size(ctypes.byref(batch), ctypes.byref(ix), k, ctypes.byref(at),
                                                       int(stage_rows)))
+
+
+def dsa_forward_stage_rows(batch: QueryDesc, ix: IndexerInputs, k: int, at: AttnInputs, workspace_bytes: int) -> int:
+    """Query rows per stage that dsa_forward runs with this much workspace (0: too little)."""
+    return int(lib().dsa_forward_stage_rows(ctypes.byref(batch), ctypes.byref(ix), k, ctypes.byref(at),
+                                            int(workspace_bytes)))
 
 
 def dsa_forward(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, k: int, at: AttnInputs,

@@ -231,27 +231,49 @@ bool fused_supported(const dsa_cache_desc* cd, const dsa_indexer_inputs* ix) {
 int64_t fused_rows_fitting(size_t bytes, int fb_grid, int max_kv, int k, int64_t num_q) {
   const FusedLayout one = fused_layout(1, fb_grid, max_kv, k);
   if (one.total > bytes) return 0;
+  // the layout grows with the rows by at least `per` bytes a row: binary
+  // search the largest row count that fits below that bound
   const size_t per = (size_t)one.plan.lds * 4 + 8 + 4 + 4 + (size_t)one.plan.cap * 8;
-  const size_t fixed = align256((size_t)fb_grid * one.ld * 4) + 256 + 6 * 256;
-  int64_t r = bytes > fixed ? (int64_t)((bytes - fixed) / per) : 1;
-  r = std::max<int64_t>(1, std::min<int64_t>(r, num_q));
-  while (r > 1 && fused_layout(r, fb_grid, max_kv, k).total > bytes) --r;
-  return r;
+  int64_t lo = 1, hi = std::max<int64_t>(1, std::min<int64_t>(num_q, (int64_t)(bytes / per)));
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo + 1) / 2;
+    if (fused_layout(mid, fb_grid, max_kv, k).total <= bytes) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Rows per stage of the fused forward with ws_bytes of workspace and its
+// fallback grid (fb, in/out); 0 if not even one row fits.  The stages are
+// equal in size.
+int64_t fused_stage_rows(const dsa_query_desc* qd, int32_t k, size_t ws_bytes, int& fb) {
+  fb = sel_fallback_grid(qd->num_q);
+  int64_t max_rows = fused_rows_fitting(ws_bytes, fb, qd->max_kv, k, qd->num_q);
+  if (max_rows == 0) {   // a small workspace: one fallback row
+    fb = 1;
+    max_rows = fused_rows_fitting(ws_bytes, fb, qd->max_kv, k, qd->num_q);
+    if (max_rows == 0) return 0;
+  }
+  const int64_t stages = (qd->num_q + max_rows - 1) / max_rows;
+  return (qd->num_q + stages - 1) / stages;
+}
+
+// Rows per stage of the staged forward (score rows in the workspace).
+int64_t staged_stage_rows(const dsa_query_desc* qd, size_t ws_bytes) {
+  int64_t max_rows = (int64_t)(ws_bytes / (score_ld(qd->max_kv) * sizeof(float)));
+  if (max_rows < 1) return 0;
+  max_rows = std::min<int64_t>(max_rows, qd->num_q);
+  const int64_t stages = (qd->num_q + max_rows - 1) / max_rows;
+  return (qd->num_q + stages - 1) / stages;
 }
 
 dsa_status run_fused(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix, int32_t k,
                      const dsa_attn_inputs* at, int32_t* idx, void* out, float* lse, void* workspace, size_t ws_bytes,
                      int* err, cudaStream_t st) {
   const CacheMap cm = to_map(cd);
-  int fb = sel_fallback_grid(qd->num_q);
-  int64_t max_rows = fused_rows_fitting(ws_bytes, fb, qd->max_kv, k, qd->num_q);
-  if (max_rows == 0) {   // a small workspace: one fallback row
-    fb = 1;
-    max_rows = fused_rows_fitting(ws_bytes, fb, qd->max_kv, k, qd->num_q);
-    if (max_rows == 0) return DSA_ERR_WORKSPACE;
-  }
-  const int64_t stages = (qd->num_q + max_rows - 1) / max_rows;
-  const int64_t rows = (qd->num_q + stages - 1) / stages;   // equal stages
+  int fb = 0;
+  const int64_t rows = fused_stage_rows(qd, k, ws_bytes, fb);
+  if (rows == 0) return DSA_ERR_WORKSPACE;
   const FusedLayout L = fused_layout(rows, fb, qd->max_kv, k);
   uint8_t* base = static_cast<uint8_t*>(workspace);
   float* samp = reinterpret_cast<float*>(base + L.samp);
@@ -422,6 +444,15 @@ size_t dsa_forward_stage_workspace_size(const dsa_query_desc* qd, const dsa_inde
   if (indexer_tc_supported(CacheMap{}, *ix))   // one fallback score row per stage row, up to one per fallback CTA
     return fused_layout(r, (int)std::min<int64_t>(sel_fallback_grid(qd->num_q), r), qd->max_kv, k).total;
   return align256((size_t)r * score_ld(qd->max_kv) * sizeof(float));
+}
+
+int64_t dsa_forward_stage_rows(const dsa_query_desc* qd, const dsa_indexer_inputs* ix, int32_t k,
+                               const dsa_attn_inputs* at, size_t workspace_bytes) {
+  if (check_query(qd) != DSA_OK || check_indexer(ix) != DSA_OK || check_attn(at) != DSA_OK) return 0;
+  if (k < 1 || k > kMaxTopk || qd->num_q == 0) return 0;
+  int fb = 0;
+  if (indexer_tc_supported(CacheMap{}, *ix)) return fused_stage_rows(qd, k, workspace_bytes, fb);
+  return staged_stage_rows(qd, workspace_bytes);
 }
 
 dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix, int32_t k,

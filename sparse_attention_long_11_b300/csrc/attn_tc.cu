@@ -160,6 +160,100 @@ __device__ __forceinline__ uint4 e4m3x8_scaled_bf16(uint2 c, float s) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Reductions over one head's 64 logits of a tile (two independent chains of
+// three-input min / max).
+__device__ __forceinline__ float abs_max64(const float (&x)[64]) {
+  float a = fabsf(x[0]), b = fabsf(x[32]);
+#pragma unroll
+  for (int j = 1; j < 31; j += 2) {
+    a = max3(a, fabsf(x[j]), fabsf(x[j + 1]));
+    b = max3(b, fabsf(x[32 + j]), fabsf(x[33 + j]));
+  }
+  return max3(a, b, fmaxf(fabsf(x[31]), fabsf(x[63])));
+}
+__device__ __forceinline__ float max64(const float (&x)[64]) {
+  float a = x[0], b = x[32];
+#pragma unroll
+  for (int j = 1; j < 31; j += 2) {
+    a = max3(a, x[j], x[j + 1]);
+    b = max3(b, x[32 + j], x[33 + j]);
+  }
+  return max3(a, b, fmaxf(x[31], x[63]));
+}
+__device__ __forceinline__ void min_max64(const float (&x)[64], float& lo, float& hi) {
+  float mnA = x[0], mxA = x[0], mnB = x[32], mxB = x[32];
+#pragma unroll
+  for (int j = 1; j < 31; j += 2) {
+    mnA = min3(mnA, x[j], x[j + 1]);
+    mxA = max3(mxA, x[j], x[j + 1]);
+    mnB = min3(mnB, x[32 + j], x[33 + j]);
+    mxB = max3(mxB, x[32 + j], x[33 + j]);
+  }
+  lo = min3(mnA, mnB, fminf(x[31], x[63]));
+  hi = max3(mxA, mxB, fmaxf(x[31], x[63]));
+}
+
+// Adds the peer's partial logits of head h (row h of the received tile: 64
+// 16-bit codes, fp16 or fixed point with the head's (step, lo) in sc) to
+// this CTA's own x.
+template <bool kFixed>
+__device__ __forceinline__ void add_peer(float (&x)[64], const uint4* X4, int h, float2 sc) {
+  const uint64_t st2 = f2(sc.x, sc.x), lo2 = f2(sc.y, sc.y), m23 = f2(-8388608.f, -8388608.f);
+#pragma unroll
+  for (int jq = 0; jq < 8; ++jq) {
+    const uint4 v = X4[jq * 128 + h];
+    const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      uint64_t pv2;
+      if (kFixed) {
+        // each 16-bit code u as the float 2^23 + u, less 2^23 (exact), then lo + u step
+        const uint64_t u2 = add2(f2(__uint_as_float(prmt(pw[e], 0x4B000000u, 0x7410u)),
+                                    __uint_as_float(prmt(pw[e], 0x4B000000u, 0x7432u))),
+                                 m23);
+        pv2 = fma2(u2, st2, lo2);
+      } else {
+        const float2 pf = f16x2_to_f32x2(pw[e]);
+        pv2 = f2(pf.x, pf.y);
+      }
+      const int j = 8 * jq + 2 * e;
+      const float2 sum = f2_split(add2(f2(x[j], x[j + 1]), pv2));
+      x[j] = sum.x;
+      x[j + 1] = sum.y;
+    }
+  }
+}
+
+// P = 2^(x scale_log2 - msub) for one head's 64 logits, as bf16 pairs in pk;
+// ls = the sum of the fp32 probabilities and, with kRounded, lrs = the sum of
+// the bf16-rounded ones (else lrs = ls).
+template <bool kRounded>
+__device__ __forceinline__ void probabilities(const float (&x)[64], float scale_log2, float msub, uint32_t (&pk)[32],
+                                              float& ls, float& lrs) {
+  uint64_t ps2[2] = {0ull, 0ull}, pr2[2] = {0ull, 0ull};
+  const uint64_t sl2 = f2(scale_log2, scale_log2), nm2 = f2(-msub, -msub);
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) {
+    const float2 d = f2_split(fma2(f2(x[j], x[j + 1]), sl2, nm2));
+    const float p0 = ex2_approx(d.x);
+    const float p1 = ex2_approx(d.y);
+    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+    ps2[(j >> 1) & 1] = add2(ps2[(j >> 1) & 1], f2(p0, p1));
+    pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
+    if (kRounded)
+      pr2[(j >> 1) & 1] =
+          add2(pr2[(j >> 1) & 1], f2(__uint_as_float(pk[j / 2] << 16), __uint_as_float(pk[j / 2] & 0xffff0000u)));
+  }
+  const float2 a = f2_split(ps2[0]), b = f2_split(ps2[1]);
+  ls = (a.x + a.y) + (b.x + b.y);
+  if (kRounded) {
+    const float2 c = f2_split(pr2[0]), d = f2_split(pr2[1]);
+    lrs = (c.x + c.y) + (d.x + d.y);
+  } else {
+    lrs = ls;
+  }
+}
+
 // kFp8Kv: the latent cache holds e4m3 codes and per-row scales (kv_scale);
 // the gather dequantises each row into the same bf16 shared-memory tiles.
 template <bool kFp8Kv>
@@ -286,43 +380,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         if (!(ok = mbar_wait_warp<true>(&B.xe[grp], par ^ 1, abort))) break;
         bool precise;   // this warp sent fixed point (warp-uniform)
         {
-          float mnA = x[0], mxA = x[0], mnB = x[32], mxB = x[32];
-#pragma unroll
-          for (int j = 1; j < 31; j += 2) {
-            mnA = min3(mnA, x[j], x[j + 1]);
-            mxA = max3(mxA, x[j], x[j + 1]);
-            mnB = min3(mnB, x[32 + j], x[33 + j]);
-            mxB = max3(mxB, x[32 + j], x[33 + j]);
-          }
-          const float lo = fminf(fminf(mnA, x[31]), fminf(mnB, x[63]));
-          const float hi = fmaxf(fmaxf(mxA, x[31]), fmaxf(mxB, x[63]));
           // fp16 carries a partial within 2^-11 of its size: a logit error
           // under 0.004 base-2 units while |x| stays below 8 of them.  A warp
           // with any larger partial sends 16-bit fixed point over each head's
           // range instead: codes u = round((x - lo) / step), 0..65534, step =
           // (hi - lo) / 65534, read back as lo + u step within about half a step.
-          precise = __any_sync(0xffffffffu, fmaxf(hi, -lo) * scale_log2 > 8.f);
-          uint32_t cw[32];
-          float step = -1.f;   // a negative step marks fp16 codes
+          precise = __any_sync(0xffffffffu, abs_max64(x) * scale_log2 > 8.f);
+          float step = -1.f, lo = 0.f;   // a negative step marks fp16 codes
           if (precise) {
+            float hi;
+            min_max64(x, lo, hi);
             const float range = hi - lo;
             const float inv = range > 0.f ? __fdividef(65534.f, range) : 0.f;
             step = range * (1.f / 65534.f);
             const uint64_t nlo2 = f2(-lo, -lo), inv2 = f2(inv, inv), mag2 = f2(12582912.f, 12582912.f);
 #pragma unroll
-            for (int j = 0; j < 64; j += 2) {
-              // (x - lo) * inv + 1.5 * 2^23: the low 16 bits of the float are the rounded code
-              const float2 y = f2_split(fma2(add2(f2(x[j], x[j + 1]), nlo2), inv2, mag2));
-              cw[j / 2] = prmt(__float_as_uint(y.x), __float_as_uint(y.y), 0x5410u);
+            for (int jq = 0; jq < 8; ++jq) {
+              uint32_t cw[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                // (x - lo) * inv + 1.5 * 2^23: the low 16 bits of the float are the rounded code
+                const int j = 8 * jq + 2 * e;
+                const float2 y = f2_split(fma2(add2(f2(x[j], x[j + 1]), nlo2), inv2, mag2));
+                cw[e] = prmt(__float_as_uint(y.x), __float_as_uint(y.y), 0x5410u);
+              }
+              st_async_v4_b32(x_peer + (uint32_t)(jq * 128 + h) * 16u, make_uint4(cw[0], cw[1], cw[2], cw[3]),
+                              xf_peer);
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 64; j += 2) cw[j / 2] = f16x2_sat(x[j], x[j + 1]);
+            for (int jq = 0; jq < 8; ++jq) {
+              const int j = 8 * jq;
+              st_async_v4_b32(x_peer + (uint32_t)(jq * 128 + h) * 16u,
+                              make_uint4(f16x2_sat(x[j], x[j + 1]), f16x2_sat(x[j + 2], x[j + 3]),
+                                         f16x2_sat(x[j + 4], x[j + 5]), f16x2_sat(x[j + 6], x[j + 7])),
+                              xf_peer);
+            }
           }
-#pragma unroll
-          for (int jq = 0; jq < 8; ++jq)
-            st_async_v4_b32(x_peer + (uint32_t)(jq * 128 + h) * 16u,
-                            make_uint4(cw[4 * jq], cw[4 * jq + 1], cw[4 * jq + 2], cw[4 * jq + 3]), xf_peer);
           st_async_v2_f32(x_peer + kXCodeBytes + (uint32_t)h * 8u, step, lo, xf_peer);
         }
         ATTN_TRACE(grp, gt, 2, lane == 0 && q4 == 0);
@@ -344,40 +438,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         // logits differ by the rounding of one partial; each CTA's half of O
         // stays consistent with its own P and sum, which is all the
         // normalisation needs.
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        const bool full = (vm_lo & vm_hi) == 0xffffffffu;   // almost every tile: no masking
         const float2 sc = XS[h];              // the peer's (step, lo) for this head
         const bool peer_fixed = sc.x >= 0.f;  // warp-uniform: the peer's warp for these heads voted
-        const uint64_t st2 = f2(sc.x, sc.x), lo2 = f2(sc.y, sc.y), m23 = f2(-8388608.f, -8388608.f);
+        if (peer_fixed) add_peer<true>(x, X4, h, sc);
+        else add_peer<false>(x, X4, h, sc);
+        if ((vm_lo & vm_hi) != 0xffffffffu) {   // rare: a tile with invalid entries
 #pragma unroll
-        for (int jq = 0; jq < 8; ++jq) {
-          const uint4 v = X4[jq * 128 + h];
-          const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint64_t pv2;
-            if (peer_fixed) {
-              // each 16-bit code u as the float 2^23 + u, less 2^23 (exact), then lo + u step
-              const uint64_t u2 = add2(f2(__uint_as_float(prmt(pw[e], 0x4B000000u, 0x7410u)),
-                                          __uint_as_float(prmt(pw[e], 0x4B000000u, 0x7432u))), m23);
-              pv2 = fma2(u2, st2, lo2);
-            } else {
-              const float2 pf = f16x2_to_f32x2(pw[e]);
-              pv2 = f2(pf.x, pf.y);
-            }
-            const int j = 8 * jq + 2 * e;
-            const float2 sum = f2_split(add2(f2(x[j], x[j + 1]), pv2));
-            x[j] = sum.x;
-            x[j + 1] = sum.y;
-            if (!full) {
-              const uint32_t vm = j < 32 ? vm_lo : vm_hi;
-              if (!((vm >> (j & 31)) & 1u)) x[j] = -INFINITY;
-              if (!((vm >> ((j + 1) & 31)) & 1u)) x[j + 1] = -INFINITY;
-            }
-            m4[e] = max3(m4[e], x[j], x[j + 1]);
-          }
+          for (int j = 0; j < 64; ++j)
+            if (!(((j < 32 ? vm_lo : vm_hi) >> (j & 31)) & 1u)) x[j] = -INFINITY;
         }
-        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale_log2;   // base-2 units
+        const float mt = max64(x) * scale_log2;   // base-2 units
         // X[grp] consumed: the store below needs mt, which depends on every
         // value loaded from X, and instructions issue in order, so the relaxed
         // arrive after it follows those loads (a release-ordered remote arrive
@@ -408,32 +478,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         // peaked softmax) the latter sums the bf16-rounded probabilities the
         // P.V MMA multiplies, so that O is an exact convex combination of the
         // V rows with the rounded weights; elsewhere it is the fp32 sum.
-        const bool rounded_sum = __any_sync(0xffffffffu, precise || peer_fixed);
-        uint64_t ps2[2] = {0ull, 0ull}, pr2[2] = {0ull, 0ull};
-        const uint64_t sl2 = f2(scale_log2, scale_log2), nm2 = f2(-msub, -msub);
-#pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          const float2 d = f2_split(fma2(f2(x[j], x[j + 1]), sl2, nm2));
-          const float p0 = ex2_approx(d.x);
-          const float p1 = ex2_approx(d.y);
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-          ps2[(j >> 1) & 1] = add2(ps2[(j >> 1) & 1], f2(p0, p1));
-          pk[j / 2] = *reinterpret_cast<const uint32_t*>(&pb);
-          if (rounded_sum)
-            pr2[(j >> 1) & 1] = add2(pr2[(j >> 1) & 1], f2(__uint_as_float(pk[j / 2] << 16),
-                                                            __uint_as_float(pk[j / 2] & 0xffff0000u)));
-        }
-        {
-          const float2 a = f2_split(ps2[0]), b2 = f2_split(ps2[1]);
-          const float ls = (a.x + a.y) + (b2.x + b2.y);
-          l += ls;
-          if (rounded_sum) {
-            const float2 c = f2_split(pr2[0]), d2 = f2_split(pr2[1]);
-            lr += (c.x + c.y) + (d2.x + d2.y);
-          } else {
-            lr += ls;
-          }
-        }
+        float ls, lrs;
+        if (__any_sync(0xffffffffu, precise || peer_fixed)) probabilities<true>(x, scale_log2, msub, pk, ls, lrs);
+        else probabilities<false>(x, scale_log2, msub, pk, ls, lrs);
+        l += ls;
+        lr += lrs;
         ATTN_TRACE(grp, gt, 4, lane == 0 && q4 == 0);
         // The heads of a warp decide separately whether their maximum moved,
         // but the TMEM loads and stores are warp-collective: the warp rescales

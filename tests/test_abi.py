@@ -79,6 +79,28 @@ def test_workspace_size_validation():
     assert st(qd, 3, f32) == 3 * 4096 * 4
 
 
+@pytest.mark.parametrize("num_q,max_kv,k", [(4096, 32768, 2048), (4096, 131072, 2048), (4096, 4096, 2048),
+                                             (64, 65536, 2048), (1000, 20000, 8192), (7, 3000, 100)])
+def test_recommended_workspace_runs_one_stage(num_q, max_kv, k):
+    """dsa_forward_workspace_size() holds the whole batch in one stage (below the 1 GiB cap), and a
+    stage size's own workspace runs no more (equal) stages than stages of that many rows would."""
+    qd = api.QueryDesc(num_q, 0x10000, 0x10000, max_kv)
+    ix, at = _ix(), _at()
+    ws = api.dsa_forward_workspace_size(qd, ix, k, at)
+    assert ws > 0
+    assert api.dsa_forward_stage_rows(qd, ix, k, at, ws) == num_q
+    for r in sorted({1, 2, 3, num_q // 3 + 1, num_q - 1}):
+        if 1 <= r <= num_q:
+            rows = api.dsa_forward_stage_rows(qd, ix, k, at, api.dsa_forward_stage_workspace_size(qd, ix, k, at, r))
+            assert rows > 0 and -(-num_q // rows) <= -(-num_q // r), (r, rows)   # no more stages than r-row ones
+    least = api.dsa_forward_stage_workspace_size(qd, ix, k, at, 1)
+    assert api.dsa_forward_stage_rows(qd, ix, k, at, least - 256) == 0
+    # fp32 operands stage whole score rows: stages are equal and as large as the bytes allow
+    f32 = _ix(dtype=api.DSA_F32, heads=4, dim=64, scales=False)
+    row = ((max_kv + 3) // 4) * 16
+    assert api.dsa_forward_stage_rows(qd, f32, k, at, 3 * row) == -(-num_q // -(-num_q // min(3, num_q)))
+
+
 def test_host_validation_rejects_before_launch():
     L = api.lib()
     cd = api.CacheDesc(1, 4096, 4096, None, 0, 0)
