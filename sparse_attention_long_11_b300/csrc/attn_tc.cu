@@ -528,6 +528,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       B.mseen[qb2][grp][h] = m_seen;
       mbar_arrive(&B.qend);
       if (!mbar_wait_warp(&B.qend, qb2, abort)) break;
+      ATTN_TRACE(grp, g - 1, 6, lane == 0 && q4 == 0);
       const float ma = B.mseen[qb2][0][h], mb = B.mseen[qb2][1][h];
       const float mf = fmaxf(ma, mb);
       const float fa = mf == -INFINITY ? 0.f : ex2_approx(ma - mf), fb = mf == -INFINITY ? 0.f : ex2_approx(mb - mf);
@@ -552,6 +553,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         o4[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
         o4[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
+      ATTN_TRACE(grp, g - 1, 7, lane == 0 && q4 == 0);
       if (crank == 0 && grp == 0) lse[(int64_t)i * kH + h] = lt > 0.f ? (mf + log2f(lt)) * kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(&B.o_empty);
@@ -574,6 +576,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       const int32_t* irow = idx + (int64_t)i * k;
       // Q of this query: every S MMA of the previous query has completed
       if (q_writer && !mbar_wait_warp(&B.q_empty, (qv & 1) ^ 1, abort)) break;
+      ATTN_TRACE(2, g, 6, warp == 8 && lane == 0);
       if (warp == 8 && lane == 0) {
         mbar_arrive_expect_tx(&B.q_rope, kQRopeBytes);
         tma_load_2d(sQr, &tm_q_rope, 512 + 32 * crank, i * kH, &B.q_rope);
@@ -609,6 +612,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         }
         tc_fence_before();
         mbar_arrive(&B.q_full);
+        ATTN_TRACE(2, g, 7, warp == 8 && lane == 0);
       }
       bool ok = true;
       for (int t = 0; t < qi.nt; ++t, ++g) {
@@ -728,6 +732,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       const int nt = qi.nt;
       if (nt == 0) continue;
       if (!mbar_wait_warp(&B.q_full, qv & 1, abort) || !mbar_wait_warp(&B.q_rope, qv & 1, abort)) break;
+      ATTN_TRACE(3, g, 7, lane == 0);
       bool ok = true;
       for (int t = 0; t < nt; ++t, ++g) {
         const uint32_t st = g % kStages, sb = g & 1;
