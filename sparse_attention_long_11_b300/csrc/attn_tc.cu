@@ -98,6 +98,7 @@ struct Bars {
   uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], xf[2], xe[2];
   uint64_t s_empty[2], p_full[2], pv_done[2], mdone[2];
   uint64_t q_full, q_rope, q_empty, o_empty, qend, fin[2];
+  uint64_t ostg_full[2], ostg_free[2];   // [group] O staging (in the group's P buffer) written / read by the TMA
   float mpub[2][128];           // [group][head] running maximum after the group's latest tile
   float lsum[2][2][128];        // [query parity][group][head] the groups' sums at the end of a query
   float lrsum[2][2][128];       // ... the same sums of the bf16-rounded probabilities the MMA used
@@ -130,14 +131,19 @@ struct QueryInfo {
   bool ok;
 };
 
-__device__ __forceinline__ QueryInfo query_info(const QueryBatch& qb, const int32_t* idx, int k, int i,
+__device__ __forceinline__ QueryInfo query_info(const QueryBatch& qb, const int32_t* idx, int k, int i, int pos,
                                                 bool prefix_valid) {
   QueryInfo r;
-  r.pos = __ldg(qb.q_pos + i);
+  r.pos = pos;
   r.ok = r.pos >= 0 && r.pos < qb.max_kv;
   r.nt = r.ok ? count_tiles(idx + (int64_t)i * k, k, r.pos, prefix_valid) : 0;
   return r;
 }
+
+// The position (or sequence) of query n, or 0 past the batch: the loops
+// below load each value one query ahead, so the load's latency (under the
+// memory traffic of a query boundary) is off the boundary's path.
+__device__ __forceinline__ int ahead_ld(const int32_t* v, int n, int num_q) { return n < num_q ? __ldg(v + n) : 0; }
 
 // Eight e4m3 codes (memory order) -> the eight bf16 values
 // bf16(s * code): each code widened exactly (e4m3 -> f16 -> f32), the
@@ -258,7 +264,8 @@ __device__ __forceinline__ void probabilities(const float (&x)[64], float scale_
 // the gather dequantises each row into the same bf16 shared-memory tiles.
 template <bool kFp8Kv>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat16* __restrict__ q,
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_constant__ CUtensorMap tm_o,
+               const __nv_bfloat16* __restrict__ q,
                const void* __restrict__ kv_raw, const float* __restrict__ kv_scale, QueryBatch qb, CacheMap cm, const int32_t* __restrict__ idx, int k, int prefix_valid,
                float scale_log2, __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int* err) {
   extern __shared__ uint8_t smem_raw[];
@@ -290,6 +297,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       mbar_init(&B.s_empty[s], 128);   // the softmax group of this parity has loaded S
     }
     mbar_init(&B.o_empty, 256);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&B.ostg_full[s], 128);
+      mbar_init(&B.ostg_free[s], 1);
+    }
     mbar_init(&B.qend, 256);
     mbar_init(&B.fin[0], 1);
     mbar_init(&B.fin[1], 1);
@@ -332,8 +343,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     const uint4* X4 = reinterpret_cast<const uint4*>(sm + kOffX + grp * kXBytes);
     const float2* XS = reinterpret_cast<const float2*>(sm + kOffX + grp * kXBytes + kXCodeBytes);
     uint32_t g = 0, qv = 0;   // tiles and queries (with tiles) so far, counted alike by both groups
+    int pos_next = ahead_ld(qb.q_pos, cluster, qb.num_q);
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
-      const QueryInfo qi = query_info(qb, idx, k, i, pv);
+      const int pos_i = pos_next;
+      const QueryInfo qi = query_info(qb, idx, k, i, pos_i, pv);
       const int pos = qi.pos, nt = qi.nt;
       const int32_t* irow = idx + (int64_t)i * k;
       __nv_bfloat16* orow = out + ((int64_t)i * kH + h) * kDv + crank * 256 + grp * 128;
@@ -343,6 +356,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
         for (int c = 0; c < 16; ++c) o4[c] = make_uint4(0, 0, 0, 0);
         if (crank == 0 && grp == 0) lse[(int64_t)i * kH + h] = -INFINITY;
         if (!qi.ok && h == 0 && crank == 0 && grp == 0) flag_error(err, DSA_ERR_BOUNDS);
+        pos_next = ahead_ld(qb.q_pos, i + ncl, qb.num_q);
         continue;
       }
       const int n_valid = min(k, pos + 1);
@@ -520,6 +534,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       }
       g = g0 + nt;
       if (!ok) break;
+      pos_next = ahead_ld(qb.q_pos, i + ncl, qb.num_q);   // the next query's position, during this epilogue
       // epilogue: the two groups' sums relative to the final maximum; each
       // group normalises and stores half of this CTA's O columns
       const int qb2 = qv & 1;
@@ -537,28 +552,51 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
       if (!mbar_wait_warp(&B.pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort)) break;
       tc_fence_after();
       const float inv = ltr > 0.f ? 1.f / ltr : 0.f;
-      uint4* o4 = reinterpret_cast<uint4*>(orow);
+      // O leaves through the TMA: every P.V of the query has completed, so the
+      // group's P buffer is free and stages the group's 128 columns as two
+      // boxes of 64 (128 heads x 128 B, 128-byte swizzle); the rows of a
+      // box are stored as whole lines instead of one 16-byte piece per head.
+      uint8_t* stg = sm + kOffP + grp * kPBytes;
+      bool eok = true;
 #pragma unroll 1
-      for (int c = 0; c < 128; c += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_base + kTmemO + grp * 128 + c, r);
-        tmem_ld_wait();
-        uint32_t w[8];
+      for (int b = 0; b < 2 && eok; ++b) {
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem + lane_base + kTmemO + grp * 128 + 64 * b + c, r);
+          tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]) * inv,
-                                                         __uint_as_float(r[2 * j + 1]) * inv);
-          w[j] = *reinterpret_cast<const uint32_t*>(&v);
+          for (int q = 0; q < 2; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[8 * q + 2 * j]) * inv,
+                                                             __uint_as_float(r[8 * q + 2 * j + 1]) * inv);
+              w[j] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            *reinterpret_cast<uint4*>(stg + sw128_offset(h, c / 8 + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
-        o4[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-        o4[c / 8 + 1] = make_uint4(w[4], w[5], w[6], w[7]);
+        fence_proxy_async_smem();
+        mbar_arrive(&B.ostg_full[grp]);
+        if (gtid == 0) {
+          if ((eok = mbar_wait(&B.ostg_full[grp], b, abort))) {
+            tma_store_2d(&tm_o, smem_u32(stg), crank * 256 + grp * 128 + 64 * b, i * kH);
+            bulk_commit();
+            bulk_wait_read();   // the staging may be written again
+            mbar_arrive(&B.ostg_free[grp]);
+          }
+        }
+        eok = mbar_wait_warp(&B.ostg_free[grp], b, abort);
       }
+      if (!eok) break;
       ATTN_TRACE(grp, g - 1, 7, lane == 0 && q4 == 0);
       if (crank == 0 && grp == 0) lse[(int64_t)i * kH + h] = lt > 0.f ? (mf + log2f(lt)) * kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(&B.o_empty);
       ++qv;
     }
+    if (gtid == 0) bulk_wait_all();   // this group's O stores have completed before the CTA may exit
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ gather (cp.async) + Q (TMA)
     // Group grp (warps 8+2grp, 9+2grp) fills stage grp with the tiles g with
@@ -569,10 +607,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     const uint32_t q_lane = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t g = 0, qv = 0, n_rope = 0;   // n_rope: rope TMA loads issued (warp 8, lane 0)
     if (warp == 8 && lane == 0) tma_prefetch_desc(&tm_q_rope);
+    int pos_next = ahead_ld(qb.q_pos, cluster, qb.num_q), seq_next = ahead_ld(qb.q_seq, cluster, qb.num_q);
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
-      const QueryInfo qi = query_info(qb, idx, k, i, pv);
+      const int pos_i = pos_next, seq = seq_next;
+      pos_next = ahead_ld(qb.q_pos, i + ncl, qb.num_q);
+      seq_next = ahead_ld(qb.q_seq, i + ncl, qb.num_q);
+      const QueryInfo qi = query_info(qb, idx, k, i, pos_i, pv);
       if (qi.nt == 0) continue;
-      const int seq = __ldg(qb.q_seq + i);
       const int32_t* irow = idx + (int64_t)i * k;
       // Q of this query: every S MMA of the previous query has completed
       if (q_writer && !mbar_wait_warp(&B.q_empty, (qv & 1) ^ 1, abort)) break;
@@ -727,8 +768,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     // instead of waiting behind them.
     const uint32_t id_s = idesc_bf16(128, kNK, false);
     uint32_t g = 0, qv = 0;
+    int pos_next = ahead_ld(qb.q_pos, cluster, qb.num_q);
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
-      const QueryInfo qi = query_info(qb, idx, k, i, pv);
+      const int pos_i = pos_next;
+      pos_next = ahead_ld(qb.q_pos, i + ncl, qb.num_q);
+      const QueryInfo qi = query_info(qb, idx, k, i, pos_i, pv);
       const int nt = qi.nt;
       if (nt == 0) continue;
       if (!mbar_wait_warp(&B.q_full, qv & 1, abort) || !mbar_wait_warp(&B.q_rope, qv & 1, abort)) break;
@@ -772,8 +816,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __nv_bfloat1
     // ------------------------------------------------------------ P.V MMA issue (warp 15, lane 0)
     const uint32_t id_pv = idesc_bf16(128, 256, true);
     uint32_t g = 0, qv = 0;
+    int pos_next = ahead_ld(qb.q_pos, cluster, qb.num_q);
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
-      const QueryInfo qi = query_info(qb, idx, k, i, pv);
+      const int pos_i = pos_next;
+      pos_next = ahead_ld(qb.q_pos, i + ncl, qb.num_q);
+      const QueryInfo qi = query_info(qb, idx, k, i, pos_i, pv);
       const int nt = qi.nt;
       if (nt == 0) continue;
       bool ok = true;
@@ -838,17 +885,18 @@ extern "C" __attribute__((visibility("default"))) int dsa_attn_trace_read(long l
 
 cudaError_t launch_attn_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_attn_inputs& at, const int32_t* idx,
                            int k, bool prefix_valid, void* out, float* lse, int* err, cudaStream_t stream) {
-  CUtensorMap q_rope;
+  CUtensorMap q_rope, o_map;
   const uint64_t qrows = (uint64_t)qb.num_q * kH;
   if (!make_tmap_bf16(&q_rope, at.q, qrows, kDqk, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&o_map, out, qrows, kDv, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
   const int ncl = std::min(qb.num_q, sm_count() / 2);
   const bool fp8 = at.dtype == DSA_FP8_E4M3;
   auto kern = fp8 ? attn_tc_kernel<true> : attn_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
   const float scale_log2 = (float)((double)at.softmax_scale * 1.4426950408889634);
-  kern<<<2 * ncl, kThreads, kSmemAlloc, stream>>>(q_rope, static_cast<const __nv_bfloat16*>(at.q), at.kv,
+  kern<<<2 * ncl, kThreads, kSmemAlloc, stream>>>(q_rope, o_map, static_cast<const __nv_bfloat16*>(at.q), at.kv,
                                                   fp8 ? at.kv_scale : nullptr, qb, cm, idx, k,
                                                   prefix_valid ? 1 : 0, scale_log2,
                                                   static_cast<__nv_bfloat16*>(out), lse, err);

@@ -77,9 +77,17 @@ __device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
   return r;
 }
 
+constexpr int kPend = 4;   // near-zero dots an entry may defer per tile (more are decided inline)
+
 struct BwdShared {
   uint64_t mma;
+  uint8_t npend[kThreads];          // per entry of the tile: deferred exact decisions
+  uint8_t pend_j[kThreads][kPend];  // ... their heads, ascending
+  int prow[kThreads];               // ... and the entry's physical key row
+  float pend_x[kThreads][kPend];    // the exact dots (rounded to fp32)
   float qn[kHI], wv[kHI], sqv[kHI];
+  alignas(16) float wsq[kHI];   // w_j sq_j
+  float qn_max;                 // the largest code norm |q8_j|
   float red[kThreads / 32];
   float dwp[kThreads / 32][kHI];
   uint32_t tmem_base;
@@ -111,8 +119,27 @@ __device__ __forceinline__ float fp16_scale(float v) {
 
 // The exact dot of key row krow's 128 codes with head j of the query (fp16
 // rows in the 128B-swizzled halves at sq) in fp64: every product of two e4m3
-// values and every partial sum is exact in fp64.  The rare path of the sign
-// decision; kept out of line.
+// values and every partial sum is exact in fp64 (the sum of 128 products
+// between 2^-18 and 448^2 needs at most 43 bits), so any order gives the
+// same value.  Here one warp computes it: lane l takes dims 4l .. 4l+3 and a
+// butterfly adds the lanes' sums.  Called by a whole warp.
+__device__ __forceinline__ double exact_code_dot_warp(const uint8_t* krow, const uint8_t* sq, int j, int lane) {
+  const uint2 f = e4m3x4_to_f16(__ldg(reinterpret_cast<const uint32_t*>(krow) + lane));
+  const int d0 = 4 * lane;
+  const uint8_t* chunk = sq + (d0 >> 6) * kQHalf + sw128_offset(j, (d0 & 63) >> 3) + 2 * (d0 & 7);
+  const uint32_t qw0 = *reinterpret_cast<const uint32_t*>(chunk);
+  const uint32_t qw1 = *reinterpret_cast<const uint32_t*>(chunk + 4);
+  double acc = (double)f16_lo(f.x) * (double)f16_lo(qw0);
+  acc = fma((double)f16_hi(f.x), (double)f16_hi(qw0), acc);
+  acc = fma((double)f16_lo(f.y), (double)f16_lo(qw1), acc);
+  acc = fma((double)f16_hi(f.y), (double)f16_hi(qw1), acc);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  return acc;
+}
+
+// The same dot by one thread (an entry with more than kPend near-zero dots in
+// a tile: rare); kept out of line.
 __device__ __noinline__ double exact_code_dot(const uint8_t* krow, const uint8_t* sq, int j) {
   double acc = 0.0;
   const uint32_t* kw = reinterpret_cast<const uint32_t*>(krow);
@@ -193,17 +220,24 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
           make_uint4(hw[4], hw[5], hw[6], hw[7]);
     }
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    const float qnj = sqrtf(ss);
     if (h == 0) {
-      S.qn[j] = sqrtf(ss);
+      S.qn[j] = qnj;
       S.wv[j] = __ldg(w + (int64_t)t * kHI + j);
       S.sqv[j] = __ldg(q_scale + (int64_t)t * kHI + j);
+      S.wsq[j] = S.wv[j] * S.sqv[j];
     }
+    float qm = qnj;   // the largest head norm (all 128 threads hold one of the 64, twice)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) qm = fmaxf(qm, __shfl_xor_sync(0xffffffffu, qm, o));
+    if (lane == 0) S.red[warp] = qm;
   }
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  const float qn_max = fmaxf(fmaxf(S.red[0], S.red[1]), fmaxf(S.red[2], S.red[3]));
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   uint32_t nmma = 0;   // MMA commits waited on (barrier phase)
   bool ok = true;
@@ -277,31 +311,72 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
     if (!ok) break;
     const int e = e0 + tid;
     uint64_t m = 0ull;
-    float iv = 0.f;
+    float iv = 0.f;   // sum_j w_j sq_j ReLU(x_j); times sk at the end
+    int np = 0;       // near-zero dots deferred to the warps' exact pass below
+    const float kb = row >= 0 ? 1e-5f * kn : -1.f;   // |x_j| <= kb |q8_j| is near zero
+    const float4* wsq4 = reinterpret_cast<const float4*>(S.wsq);
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {   // 16 heads at a time, straight from TMEM
       uint32_t r[16];
       tmem_ld16(tmem + lane_base + kTmemX + 16 * c, r);
       tmem_ld_wait();
+      // screen: the smallest |x| of the 16 against the largest bound any of them has
+      float amin = fabsf(__uint_as_float(r[0]));
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int j = 16 * c + u;
-        float xv = __uint_as_float(r[u]);
-        const float bound = 1e-5f * S.qn[j] * kn;
-        bool posv = xv > 0.f;
-        if (row >= 0 && bound > 0.f && fabsf(xv) <= bound) {   // near zero: decide the sign exactly
-          const double exact = exact_code_dot(k8 + (int64_t)row * kDI, sm + kOffQ, j);
-          posv = exact > 0.0;
-          xv = (float)exact;
-        }
-        if (posv) {
-          m |= 1ull << j;
-          iv = fmaf(S.wv[j], xv * S.sqv[j] * sk, iv);
+      for (int u = 1; u < 15; u += 2)
+        amin = min3(amin, fabsf(__uint_as_float(r[u])), fabsf(__uint_as_float(r[u + 1])));
+      amin = fminf(amin, fabsf(__uint_as_float(r[15])));
+      const bool near = amin <= kb * qn_max;
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const float4 wq = wsq4[4 * c + u4];
+        const float wj[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int u = 4 * u4 + v, j = 16 * c + u;
+          float xv = __uint_as_float(r[u]);
+          bool posv = xv > 0.f;
+          if (near) {   // rare: the exact test of each head's bound
+            const float bound = kb * S.qn[j];
+            if (bound > 0.f && fabsf(xv) <= bound) {   // near zero: decide the sign exactly
+              if (np < kPend) {
+                S.pend_j[tid][np++] = (uint8_t)j;
+                continue;
+              }
+              const double exact = exact_code_dot(k8 + (int64_t)row * kDI, sm + kOffQ, j);
+              posv = exact > 0.0;
+              xv = (float)exact;
+            }
+          }
+          if (posv) {
+            m |= 1ull << j;
+            iv = fmaf(wj[v], xv, iv);
+          }
         }
       }
     }
+    // the deferred dots: each warp decides its own entries' (a warp per dot)
+    S.npend[tid] = (uint8_t)np;
+    S.prow[tid] = row;
+    __syncwarp();
+    for (uint32_t pm = __ballot_sync(0xffffffffu, np > 0); pm; pm &= pm - 1) {
+      const int et = warp * 32 + __ffs(pm) - 1, n = S.npend[et];
+      for (int q = 0; q < n; ++q) {
+        const double ex = exact_code_dot_warp(k8 + (int64_t)S.prow[et] * kDI, sm + kOffQ, S.pend_j[et][q], lane);
+        if (lane == 0) S.pend_x[et][q] = ex > 0.0 ? (float)ex : 0.f;
+      }
+    }
+    __syncwarp();
+    for (int q = 0; q < np; ++q) {   // heads ascending
+      const float xv = S.pend_x[tid][q];
+      if (xv > 0.f) {
+        const int j = S.pend_j[tid][q];
+        m |= 1ull << j;
+        iv = fmaf(S.wsq[j], xv, iv);
+      }
+    }
     if (e < kk) {
-      Ie[e] = row >= 0 ? iv : -INFINITY;
+      Ie[e] = row >= 0 ? iv * sk : -INFINITY;
       msk[e] = row >= 0 ? m : 0ull;
     }
     tc_fence_before();
@@ -360,7 +435,7 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
           const int j = 8 * c + 2 * q;
           const bool m0 = (m >> j) & 1ull, m1 = (m >> (j + 1)) & 1ull;
           hg[q] = f16x2(m0 ? gs : 0.f, m1 ? gs : 0.f);
-          hb[q] = f16x2(m0 ? gb * S.wv[j] * S.sqv[j] : 0.f, m1 ? gb * S.wv[j + 1] * S.sqv[j + 1] : 0.f);
+          hb[q] = f16x2(m0 ? gb * S.wsq[j] : 0.f, m1 ? gb * S.wsq[j + 1] : 0.f);
         }
         *reinterpret_cast<uint4*>(sm + kOffG + sw128_offset(tid, c)) = make_uint4(hg[0], hg[1], hg[2], hg[3]);
         *reinterpret_cast<uint4*>(sm + kOffB + sw128_offset(tid, c)) = make_uint4(hb[0], hb[1], hb[2], hb[3]);
