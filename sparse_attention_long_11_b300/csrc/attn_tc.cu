@@ -789,17 +789,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
         if (lane == 0) {
           const uint32_t dS = tmem + kTmemS + 64 * sb;
           const uint32_t skv = sKV + st * kKVStageBytes;
-          uint32_t n = 0;
+          // one descriptor per operand and tile; each MMA offsets its low word
+          const Desc2 kd = desc2(sdesc(skv, 16, 1024));
+          const Desc2 rq = desc2(sdesc_sw64(sQr, 512)), rk = desc2(sdesc_sw64(skv + 4 * kKVSlotBytes, 512));
 #pragma unroll
           for (int a = 0; a < 4; ++a)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk, ++n)
-              mma_bf16_ts(dS, tmem + kTmemQ + a * 32 + kk * 8, sdesc(skv + a * kKVSlotBytes + kk * 32, 16, 1024),
-                          id_s, n > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t aq = tmem + kTmemQ + a * 32 + kk * 8;
+              const Desc2 b = desc_at(kd, a * kKVSlotBytes + kk * 32);
+              if (a == 0 && kk == 0) mma_bf16_ts2<0>(dS, aq, b, id_s);
+              else mma_bf16_ts2<1>(dS, aq, b, id_s);
+            }
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-            mma_bf16(dS, sdesc_sw64(sQr + kk * 32, 512), sdesc_sw64(skv + 4 * kKVSlotBytes + kk * 32, 512), id_s,
-                     1u);
+          for (int kk = 0; kk < 2; ++kk) mma_bf16_2<1>(dS, desc_at(rq, kk * 32), desc_at(rk, kk * 32), id_s);
           mma_commit(&B.s_full[sb]);
           if (t == nt - 1) mma_commit(&B.q_empty);
         }
@@ -834,10 +837,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
         if (lane == 0) {
           const uint32_t skv = sKV + (g % kStages) * kKVStageBytes;
           const uint32_t sp = sP + (g & 1) * kPBytes;
+          const Desc2 pd = desc2(sdesc(sp, 16, 1024)), vd = desc2(sdesc(skv, kKVSlotBytes, 1024));
+          mma_bf16_2(tmem + kTmemO, pd, vd, id_pv, t > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16(tmem + kTmemO, sdesc(sp + kk * 32, 16, 1024), sdesc(skv + kk * 2048, kKVSlotBytes, 1024), id_pv,
-                     (t > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 1; kk < 4; ++kk) mma_bf16_2<1>(tmem + kTmemO, desc_at(pd, kk * 32), desc_at(vd, kk * 2048), id_pv);
           mma_commit(&B.pv_done[g & 1]);
           mma_commit(&B.kv_empty[g % kStages]);
         }

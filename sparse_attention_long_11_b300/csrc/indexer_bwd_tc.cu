@@ -302,11 +302,13 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
     gather(e0, row, sk, kn);
     if (row >= 0) smax = fmaxf(smax, sk);
     ok = mma_round([&] {
+      const Desc2 kd = desc2(sdesc(sK, 16, 1024)), qd = desc2(sdesc(sQ, 16, 1024));
+      constexpr uint32_t id = idesc_f16(128, kHI, false, false);
+      mma_bf16_2<0>(tmem + kTmemX, kd, qd, id);
 #pragma unroll
-      for (int s = 0; s < 8; ++s)   // K = 128 dims in steps of 16
-        mma_bf16(tmem + kTmemX, sdesc(sK + (s >> 2) * kKHalf + (s & 3) * 32, 16, 1024),
-                 sdesc(sQ + (s >> 2) * kQHalf + (s & 3) * 32, 16, 1024), idesc_f16(128, kHI, false, false),
-                 s > 0 ? 1u : 0u);
+      for (int s = 1; s < 8; ++s)   // K = 128 dims in steps of 16
+        mma_bf16_2<1>(tmem + kTmemX, desc_at(kd, (s >> 2) * kKHalf + (s & 3) * 32),
+                      desc_at(qd, (s >> 2) * kQHalf + (s & 3) * 32), id);
     });
     if (!ok) break;
     const int e = e0 + tid;
@@ -445,16 +447,17 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
     ok = mma_round([&] {
       // D[d][j] += sum_e K[e][d] G[e][j]: A = the key tile read MN-major (128 dims
       // in two 64-dim blocks), B = G MN-major; 8 steps of 16 entries
+      const Desc2 kd = desc2(sdesc(sK, kKHalf, 1024)), gd = desc2(sdesc(sG, 8192, 1024));
+      constexpr uint32_t idD = idesc_f16(128, kHI, true, true), idK = idesc_f16(128, kDI, false, true);
+      mma_bf16_2(tmem + kTmemD, kd, gd, idD, first ? 0u : 1u);
 #pragma unroll
-      for (int s = 0; s < 8; ++s)
-        mma_bf16(tmem + kTmemD, sdesc(sK + s * 2048, kKHalf, 1024), sdesc(sG + s * 2048, 8192, 1024),
-                 idesc_f16(128, kHI, true, true), (first && s == 0) ? 0u : 1u);
+      for (int s = 1; s < 8; ++s) mma_bf16_2<1>(tmem + kTmemD, desc_at(kd, s * 2048), desc_at(gd, s * 2048), idD);
       // dK[e][d] = sum_j B[e][j] Q[j][d]: A = B K-major, B = Q read MN-major
       // (128 dims in two 64-dim blocks); 4 steps of 16 heads
+      const Desc2 bd = desc2(sdesc(sB, 16, 1024)), qm = desc2(sdesc(sQ, kQHalf, 1024));
+      mma_bf16_2<0>(tmem + kTmemK, bd, qm, idK);
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_bf16(tmem + kTmemK, sdesc(sB + s * 32, 16, 1024), sdesc(sQ + s * 2048, kQHalf, 1024),
-                 idesc_f16(128, kDI, false, true), s > 0 ? 1u : 0u);
+      for (int s = 1; s < 4; ++s) mma_bf16_2<1>(tmem + kTmemK, desc_at(bd, s * 32), desc_at(qm, s * 2048), idK);
     });
     if (!ok) break;
     {   // dk of this entry's key row (the TMEM loads are warp-collective: every lane loads)

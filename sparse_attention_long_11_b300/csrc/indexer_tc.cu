@@ -392,10 +392,10 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           IDX_TRACE(1, g, 2, lane == 0);
           tc_fence_after();
           if (lane == 0) {
+            const Desc2 ad = desc2(sdesc(sA + st * kABytes, 16, 1024)), bd = desc2(sdesc(sB + boff, 16, 1024));
+            mma_e4m3_2<0>(tmem + 256 * b, ad, bd, idesc);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_e4m3(tmem + 256 * b, sdesc(sA + st * kABytes + kk * 32, 16, 1024),
-                       sdesc(sB + boff + kk * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+            for (int kk = 1; kk < 4; ++kk) mma_e4m3_2<1>(tmem + 256 * b, desc_at(ad, kk * 32), desc_at(bd, kk * 32), idesc);
             mma_commit(&S.a_empty[st]);
             mma_commit(&S.d_full[b]);
           }
@@ -415,10 +415,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           IDX_TRACE(1, g, 1, lane == 0);
           tc_fence_after();
           if (lane == 0) {
+            const Desc2 ad = desc2(sdesc(sA + st * kABytes, 16, 1024)), bd = desc2(sdesc(sB + boff, 16, 1024));
+            mma_e4m3_2<0>(tmem + 256 * b + 64 * u, ad, bd, idesc);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_e4m3(tmem + 256 * b + 64 * u, sdesc(sA + st * kABytes + kk * 32, 16, 1024),
-                       sdesc(sB + boff + kk * 32, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+            for (int kk = 1; kk < 4; ++kk)
+              mma_e4m3_2<1>(tmem + 256 * b + 64 * u, desc_at(ad, kk * 32), desc_at(bd, kk * 32), idesc);
             mma_commit(&S.a_empty[st]);
           }
           __syncwarp();

@@ -137,10 +137,10 @@ sel_fallback_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           if (!(ok = mbar_wait(&S.a_full[st], ph, abort))) break;
           if (!(ok = mbar_wait(&S.d_empty[st], ph ^ 1, abort))) break;
           tc_fence_after();
+          const Desc2 ad = desc2(sdesc(sA + st * kABytes, 16, 1024)), qd = desc2(sdesc(sQ, 16, 1024));
+          mma_e4m3_2<0>(tmem + 64 * st, ad, qd, idesc);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_e4m3(tmem + 64 * st, sdesc(sA + st * kABytes + kk * 32, 16, 1024), sdesc(sQ + kk * 32, 16, 1024),
-                     idesc, kk > 0 ? 1u : 0u);
+          for (int kk = 1; kk < 4; ++kk) mma_e4m3_2<1>(tmem + 64 * st, desc_at(ad, kk * 32), desc_at(qd, kk * 32), idesc);
           mma_commit(&S.d_full[st]);
           mma_commit(&S.a_free[st]);
           if (t + 2 < T) {   // reuse this stage for tile t + 2 once its MMAs have read it

@@ -393,6 +393,55 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// A shared-memory matrix descriptor as its two 32-bit words.  The start
+// address sits in the low word's bits 0-13 (address >> 4); moving the
+// operand by a byte offset (a multiple of 16, staying below 256 KB) adds
+// offset >> 4 to the low word alone.  An MMA issuer that builds one
+// descriptor per tile and offsets its low word per instruction spends one
+// integer add per MMA instead of rebuilding the 64-bit descriptor (the
+// rebuild, on the single issuing thread, measured about twice the tensor
+// core's time per 128x64x16 MMA).
+struct Desc2 {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ Desc2 desc2(uint64_t d) { return Desc2{(uint32_t)d, (uint32_t)(d >> 32)}; }
+__device__ __forceinline__ Desc2 desc_at(Desc2 d, uint32_t byte_off) { return Desc2{d.lo + (byte_off >> 4), d.hi}; }
+
+// D[tmem] (+)= A[tmem] x B[smem]^T and D (+)= A[smem] x B[smem]^T with
+// descriptors in halves; ACC is the accumulate flag (a constant).
+template <int ACC>
+__device__ __forceinline__ void mma_bf16_ts2(uint32_t d_tmem, uint32_t a_tmem, Desc2 b, uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 bd;\n setp.ne.b32 p, %5, 0;\n mov.b64 bd, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+template <int ACC>
+__device__ __forceinline__ void mma_bf16_2(uint32_t d_tmem, Desc2 a, Desc2 b, uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 ad, bd;\n setp.ne.b32 p, %6, 0;\n mov.b64 ad, {%1, %2};\n"
+      " mov.b64 bd, {%3, %4};\n tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+// Same with a runtime accumulate flag.
+__device__ __forceinline__ void mma_bf16_2(uint32_t d_tmem, Desc2 a, Desc2 b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 ad, bd;\n setp.ne.b32 p, %6, 0;\n mov.b64 ad, {%1, %2};\n"
+      " mov.b64 bd, {%3, %4};\n tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(acc)
+      : "memory");
+}
+template <int ACC>
+__device__ __forceinline__ void mma_e4m3_2(uint32_t d_tmem, Desc2 a, Desc2 b, uint32_t idesc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 ad, bd;\n setp.ne.b32 p, %6, 0;\n mov.b64 ad, {%1, %2};\n"
+      " mov.b64 bd, {%3, %4};\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %5, p;\n}\n" ::"r"(d_tmem),
+      "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every MMA this thread issued so far completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
