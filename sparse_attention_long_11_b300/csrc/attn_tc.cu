@@ -462,6 +462,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
             if (!(((j < 32 ? vm_lo : vm_hi) >> (j & 31)) & 1u)) x[j] = -INFINITY;
         }
         const float mt = max64(x) * scale_log2;   // base-2 units
+        ATTN_TRACE(grp, gt, 6, lane == 0 && q4 == 0 && t < nt - 1);
         // X[grp] consumed: the store below needs mt, which depends on every
         // value loaded from X, and instructions issue in order, so the relaxed
         // arrive after it follows those loads (a release-ordered remote arrive
@@ -475,6 +476,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           if (!(ok = mbar_wait_warp(&B.mdone[grp ^ 1], ((gt - 1) >> 1) & 1, abort))) break;
           if (t > 0) m_prev = B.mpub[grp ^ 1][h];
         }
+        ATTN_TRACE(grp, gt, 7, lane == 0 && q4 == 0 && t < nt - 1);
         // lazy rescaling: the maximum used only moves when exceeded by more than 8 (a factor 256)
         const float m_use = mt > m_prev + 8.f ? mt : m_prev;
         B.mpub[grp][h] = m_use;
