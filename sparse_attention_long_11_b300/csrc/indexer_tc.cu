@@ -88,8 +88,10 @@ __device__ long long g_idx_trace[3][1024][4];
 // the sampled tiles 0, m, 2m, ... (kSample), or all the others (kFilter).
 // A pass's tiles are numbered by ordinal o = 0, 1, ...; tile(o) maps an
 // ordinal to its key tile.
+template <int kMode>
 struct TileMap {
-  int mode, m;
+  static constexpr int mode = kMode;
+  int m;
   uint32_t inv;   // kFilter: division by m - 1 as a multiply-high (exact for ordinals and m below 2^16)
   __device__ __forceinline__ int count(int T) const {
     return mode == IndexerOut::kFull ? T : mode == IndexerOut::kSample ? (T + m - 1) / m : T - (T + m - 1) / m;
@@ -118,8 +120,9 @@ struct Group {
   int pass_q[kQG], pass_seq[kQG], pass_T[kQG], pass_N[kQG], pass_maxpos[kQG];   // T tiles, N ordinals
 };
 
+template <class TM>
 __device__ __forceinline__ void describe_group(const QueryBatch& qb, const CacheMap& cm, int gi, int min_pos,
-                                               const TileMap& tm, Group& G) {
+                                               const TM& tm, Group& G) {
   int first_seq = -1, nact = 0;
   bool same = true;
 #pragma unroll
@@ -229,11 +232,12 @@ __device__ __forceinline__ void stage_flush(const IndexerOut& o, Stager& st, con
 // filter stages with a warp ballot): row_q, t (the tile's ordinal) and thr
 // are warp-uniform, s is this lane's key, live whether it is a causal key of
 // a valid query with a readable cache row.
+template <int kMode>
 __device__ __forceinline__ void emit(const IndexerOut& o, const QueryBatch& qb, int row_q, int t, int s, float sc,
                                      bool live, uint64_t thr, int lane, Stager& st, uint64_t* buf) {
-  if (o.mode == IndexerOut::kFull) {
+  if (kMode == IndexerOut::kFull) {
     if (s < qb.max_kv && row_q < qb.num_q) o.scores[(int64_t)row_q * o.ld + s] = live ? sc : -INFINITY;
-  } else if (o.mode == IndexerOut::kSample) {
+  } else if (kMode == IndexerOut::kSample) {
     if (row_q < qb.num_q) o.scores[(int64_t)row_q * o.ld + t * kKT + (s & (kKT - 1))] = live ? sc : -INFINITY;
   } else {
     // composite key >= thr, decided on the score (the high word orders like
@@ -256,6 +260,9 @@ __device__ __forceinline__ void emit(const IndexerOut& o, const QueryBatch& qb, 
   }
 }
 
+// kMode: the pass (IndexerOut::kFull, kSample, kFilter) as a compile-time
+// constant, so the per-key epilogue carries no mode branches.
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   QueryBatch qb, CacheMap cm, const float* __restrict__ q_scale, const float* __restrict__ w,
@@ -268,7 +275,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   volatile int* abort = &S.abort;
   const uint32_t sB = smem_u32(sm), sA = smem_u32(sm + kOffA);
   const int n_items = ngroups * nchunk;
-  const TileMap tmap{out.mode, out.m, recip32((uint32_t)max(out.m - 1, 1))};
+  const TileMap<kMode> tmap{out.m, recip32((uint32_t)max(out.m - 1, 1))};
   float* __restrict__ scores = out.scores;
   const int64_t ld = out.ld;
 
@@ -469,7 +476,11 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const bool q_act = G.active[uq];
           const int q_pos = G.pos[uq], row_q = gi * kQG + uq;
           const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][uq]);
-          const uint64_t thr = out.mode == IndexerOut::kFilter && row_q < qb.num_q ? __ldg(out.thr + row_q) : 0ull;
+          const uint64_t thr = kMode == IndexerOut::kFilter && row_q < qb.num_q ? __ldg(out.thr + row_q) : 0ull;
+          // a contiguous cache holds this pass's keys at rows seq_base + s: one
+          // range check per item instead of one row lookup per key
+          const int64_t seq_base = (int64_t)seq * cm.seq_stride;
+          const bool contig = cm.block_size == 0 && seq_base + maxpos < cm.num_rows;
           for (int t = t0; t < t1; ++t, ++dq) {
             const int b = dq & 1;
             // this lane's key and its scale, fetched before the wait
@@ -477,7 +488,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             float sk = 0.f;
             bool key_ok = s <= maxpos;
             if (key_ok) {
-              const int64_t row = cache_row(cm, seq, s, err);
+              const int64_t row = contig ? seq_base + s : cache_row(cm, seq, s, err);
               key_ok = row >= 0;
               if (key_ok) sk = __ldg(k_scale + row);
             }
@@ -486,7 +497,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             IDX_TRACE(2, dq, 1, et == 0);
             tc_fence_after();
             const float acc = idx_epi::head_sum64(tmem + lane_base + 256 * b + uq * 64, wq4);
-            emit(out, qb, row_q, t, s, acc * sk, q_act && key_ok && s <= q_pos, thr, lane, stg, sbuf);
+            emit<kMode>(out, qb, row_q, t, s, acc * sk, q_act && key_ok && s <= q_pos, thr, lane, stg, sbuf);
             tc_fence_before();
             mbar_arrive(&S.d_empty[b]);
             IDX_TRACE(2, dq, 2, et == 0);
@@ -505,7 +516,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const int s = tmap.tile(t) * kKT + qd * 32 + lane;
           const int row_q = gi * kQG + qq;
           const uint64_t thr =
-              out.mode == IndexerOut::kFilter && mine && row_q < qb.num_q ? __ldg(out.thr + row_q) : 0ull;
+              kMode == IndexerOut::kFilter && mine && row_q < qb.num_q ? __ldg(out.thr + row_q) : 0ull;
           float sk = 0.f;
           bool key_ok = mine && s <= G.pass_maxpos[p];
           if (key_ok) {
@@ -522,19 +533,19 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             // not depend on its batch
             const float4* wq4 = reinterpret_cast<const float4*>(S.wq[bb][qq]);
             const float acc = idx_epi::head_sum64(tmem + lane_base + 256 * b + uq * 64, wq4);
-            emit(out, qb, row_q, t, s, acc * sk, G.active[qq] && key_ok && s <= G.pos[qq], thr, lane, stg, sbuf);
+            emit<kMode>(out, qb, row_q, t, s, acc * sk, G.active[qq] && key_ok && s <= G.pos[qq], thr, lane, stg, sbuf);
           }
           tc_fence_before();
           mbar_arrive(&S.d_empty[b]);
           IDX_TRACE(2, dq, 2, et == 0);
         }
         if (!ok) break;
-        if (out.mode == IndexerOut::kFilter) stage_flush(out, stg, sbuf, lane);
+        if (kMode == IndexerOut::kFilter) stage_flush(out, stg, sbuf, lane);
         ++j;
       }
       // the item holding a group's last chunk also writes -inf from the end
       // of the group's scanned tiles to max_kv
-      if (out.mode == IndexerOut::kFull && c == nchunk - 1) {
+      if (kMode == IndexerOut::kFull && c == nchunk - 1) {
         for (int qq = 0; qq < kQG; ++qq) {
           const int row_q = gi * kQG + qq;
           if (row_q >= qb.num_q) break;
@@ -612,10 +623,13 @@ cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const ds
   }
   const int nchunk = (tmax + ch - 1) / ch;
   const int grid = (int)std::min<int64_t>(sms, (int64_t)ngroups * nchunk);
-  cudaError_t e = cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+  auto kern = out.mode == IndexerOut::kSample   ? indexer_tc_kernel<IndexerOut::kSample>
+              : out.mode == IndexerOut::kFilter ? indexer_tc_kernel<IndexerOut::kFilter>
+                                                 : indexer_tc_kernel<IndexerOut::kFull>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
-  indexer_tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(tm_q, tm_k, qb, cm, ix.q_scale, ix.w, ix.k_scale, out,
-                                                             ngroups, nchunk, ch, wait_limit, err);
+  kern<<<grid, kThreads, kSmemAlloc, stream>>>(tm_q, tm_k, qb, cm, ix.q_scale, ix.w, ix.k_scale, out, ngroups, nchunk,
+                                               ch, wait_limit, err);
   return cudaGetLastError();
 }
 
