@@ -242,9 +242,18 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   uint32_t nmma = 0;   // MMA commits waited on (barrier phase)
   bool ok = true;
 
-  // This thread's entry of tile e0: its key row decoded to fp16 into row tid
-  // of the key tile, its physical row, key scale and code norm.
-  auto gather = [&](int e0, int& row_out, float& sk_out, float& kn_out) {
+  // The key rows of a tile reach shared memory in two steps, so that a
+  // tile's loads are in flight while the previous tile computes:
+  //   locate  this thread's entry e0 + tid: its physical row (-1: padding)
+  //           and key scale;
+  //   stage   cp.async of the warp's 32 rows of e4m3 codes into a staging
+  //           tile (128 B a row, 16-byte chunk c of row r at c ^ (r & 7);
+  //           lane l copies chunk l % 8 of row l / 8 + 4i, so each copy
+  //           instruction writes four whole rows);
+  //   decode  once the warp's copies have landed: this thread's row, decoded
+  //           to fp16 (exact for e4m3) into row tid of the key tile, and its
+  //           code norm.
+  auto locate = [&](int e0, int& row_out, float& sk_out) {
     const int e = e0 + tid;
     int64_t row = -1;
     if (e < kk) {
@@ -254,14 +263,23 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
     }
     row_out = (int)row;
     sk_out = row >= 0 ? __ldg(k_scale + row) : 0.f;
-    const uint4* src = reinterpret_cast<const uint4*>(k8 + (row >= 0 ? row : 0) * kDI);
-    uint4 codes[8];
+  };
+  auto stage = [&](uint32_t stg, int row) {
 #pragma unroll
-    for (int c = 0; c < 8; ++c) codes[c] = row >= 0 ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 8; ++i) {
+      const int rl = 4 * i + (lane >> 3), c = lane & 7, r = warp * 32 + rl;
+      const int src = __shfl_sync(0xffffffffu, row, rl);
+      cp_async16(stg + r * 128 + ((c ^ (r & 7)) << 4), k8 + (int64_t)(src >= 0 ? src : 0) * kDI + c * 16,
+                 src >= 0 ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  auto decode = [&](const uint8_t* stg, float& kn_out) {
     float ss = 0.f;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-      const uint32_t cw[4] = {codes[c].x, codes[c].y, codes[c].z, codes[c].w};
+      const uint4 v = *reinterpret_cast<const uint4*>(stg + tid * 128 + ((c ^ (tid & 7)) << 4));
+      const uint32_t cw[4] = {v.x, v.y, v.z, v.w};
       uint32_t hw[8];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -295,11 +313,27 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   };
 
   // ---------------------------------------------------------------- pass 1
+  // staging tiles: G's and B's space, free until pass 2, alternately
   float smax = 0.f;   // largest key scale among valid entries (this thread)
-  for (int e0 = 0; e0 < kk && ok; e0 += kTile) {
-    int row;
-    float sk, kn;
-    gather(e0, row, sk, kn);
+  int row_n = -1;
+  float sk_n = 0.f;
+  if (kk > 0) {
+    locate(0, row_n, sk_n);
+    stage(sG, row_n);
+  }
+  for (int e0 = 0, it = 0; e0 < kk && ok; e0 += kTile, ++it) {
+    const int row = row_n;
+    const float sk = sk_n;
+    if (e0 + kTile < kk) {   // the next tile's rows, in flight while this one computes
+      locate(e0 + kTile, row_n, sk_n);
+      stage((it & 1) ? sG : sB, row_n);
+      cp_async_wait_group1();
+    } else {
+      cp_async_wait_all();
+    }
+    __syncwarp();
+    float kn;
+    decode(sm + ((it & 1) ? kOffB : kOffG), kn);
     if (row >= 0) smax = fmaxf(smax, sk);
     ok = mma_round([&] {
       const Desc2 kd = desc2(sdesc(sK, 16, 1024)), qd = desc2(sdesc(sQ, 16, 1024));
@@ -417,12 +451,22 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   wsmax = block_reduce(wsmax, S.red, true);
   const float scG = fp16_scale(gmax * smax), scB = fp16_scale(gmax * wsmax);   // G, B scaled below 2^14
   __syncthreads();
+  if (ok && kk > 0) {   // pass 2's first tile
+    locate(0, row_n, sk_n);
+    stage(sG, row_n);
+  }
 
   // ---------------------------------------------------------------- pass 2
+  // one staging tile in G's space: each thread reads its staged row before
+  // it writes its G row over the same 128 bytes; the next tile is staged
+  // once this tile's MMAs have read G
   for (int e0 = 0; e0 < kk && ok; e0 += kTile) {
-    int row;
-    float sk, kn;
-    gather(e0, row, sk, kn);
+    const int row = row_n;
+    const float sk = sk_n;
+    cp_async_wait_all();
+    __syncwarp();
+    float kn;
+    decode(sm + kOffG, kn);
     const int e = e0 + tid;
     const uint64_t m = e < kk ? msk[e] : 0ull;
     const float ge = e < kk ? Ie[e] : 0.f;
@@ -460,6 +504,10 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
       for (int s = 1; s < 4; ++s) mma_bf16_2<1>(tmem + kTmemK, desc_at(bd, s * 32), desc_at(qm, s * 2048), idK);
     });
     if (!ok) break;
+    if (e0 + kTile < kk) {   // G has been read: stage the next tile there while dk is written
+      locate(e0 + kTile, row_n, sk_n);
+      stage(sG, row_n);
+    }
     {   // dk of this entry's key row (the TMEM loads are warp-collective: every lane loads)
       const bool add = row >= 0 && m != 0ull && ge != 0.f;
       const float inv = 1.f / scB;
@@ -514,6 +562,7 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
     }
   }
 
+  cp_async_wait_all();   // no copy into this CTA's shared memory is left in flight (an abort leaves early)
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

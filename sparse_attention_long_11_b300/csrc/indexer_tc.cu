@@ -520,7 +520,9 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           float sk = 0.f;
           bool key_ok = mine && s <= G.pass_maxpos[p];
           if (key_ok) {
-            const int64_t row = cache_row(cm, G.pass_seq[p], s, err);
+            const int64_t pbase = (int64_t)G.pass_seq[p] * cm.seq_stride;
+            const bool contig = cm.block_size == 0 && pbase + G.pass_maxpos[p] < cm.num_rows;
+            const int64_t row = contig ? pbase + s : cache_row(cm, G.pass_seq[p], s, err);
             key_ok = row >= 0;
             if (key_ok) sk = __ldg(k_scale + row);
           }
