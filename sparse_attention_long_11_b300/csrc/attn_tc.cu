@@ -317,6 +317,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
   __syncthreads();
   cluster_sync();   // the peer's barriers exist before anyone arrives on them remotely
   tc_fence_after();
+  pdl_wait();      // the set-up above ran while the stream's previous kernel finished
+  pdl_release();
   const uint32_t tmem = B.tmem_base;
   const uint32_t sQr = smem_u32(sm + kOffQRope), sKV = smem_u32(sm + kOffKV), sP = smem_u32(sm + kOffP);
 
@@ -901,11 +903,9 @@ cudaError_t launch_attn_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_a
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
   const float scale_log2 = (float)((double)at.softmax_scale * 1.4426950408889634);
-  kern<<<2 * ncl, kThreads, kSmemAlloc, stream>>>(q_rope, o_map, static_cast<const __nv_bfloat16*>(at.q), at.kv,
-                                                  fp8 ? at.kv_scale : nullptr, qb, cm, idx, k,
-                                                  prefix_valid ? 1 : 0, scale_log2,
-                                                  static_cast<__nv_bfloat16*>(out), lse, err);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(2 * ncl), dim3(kThreads), kSmemAlloc, stream, q_rope, o_map,
+                    static_cast<const __nv_bfloat16*>(at.q), at.kv, fp8 ? at.kv_scale : nullptr, qb, cm, idx, k,
+                    prefix_valid ? 1 : 0, scale_log2, static_cast<__nv_bfloat16*>(out), lse, err);
 }
 
 }  // namespace dsa

@@ -37,6 +37,16 @@ __device__ __forceinline__ void flag_error(int* err, int code) {
 
 // Physical row of (seq, pos), or -1 (and DSA_ERR_BOUNDS flagged) when any part
 // of the map is out of range.  Never dereferences an out-of-range pointer.
+// Programmatic dependent launch.  A kernel launched with programmatic
+// stream serialization may start while the previous kernel in the stream is
+// still running: pdl_wait() returns once that kernel has completed and its
+// memory operations are visible (immediately when there is no such
+// dependency), and pdl_release() lets the next kernel in the stream start
+// its own set-up early.  Work before pdl_wait() touches no memory another
+// kernel of the stream writes or reads.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ int64_t cache_row(const CacheMap& c, int seq, int pos, int* err) {
   if (seq < 0 || seq >= c.num_seqs || pos < 0) {
     flag_error(err, DSA_ERR_BOUNDS);

@@ -302,6 +302,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();      // the set-up above ran while the stream's previous kernel finished
+  pdl_release();
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
@@ -630,9 +632,8 @@ cudaError_t launch_indexer_tc(const QueryBatch& qb, const CacheMap& cm, const ds
                                                  : indexer_tc_kernel<IndexerOut::kFull>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, kSmemAlloc, stream>>>(tm_q, tm_k, qb, cm, ix.q_scale, ix.w, ix.k_scale, out, ngroups, nchunk,
-                                               ch, wait_limit, err);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), kSmemAlloc, stream, tm_q, tm_k, qb, cm, ix.q_scale, ix.w,
+                    ix.k_scale, out, ngroups, nchunk, ch, wait_limit, err);
 }
 
 }  // namespace dsa

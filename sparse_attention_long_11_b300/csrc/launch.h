@@ -3,9 +3,34 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <utility>
+
 #include "common.cuh"
 
 namespace dsa {
+
+// Launches `kern` with programmatic stream serialization: the kernel may
+// start (and run its set-up) while the previous kernel of the stream is
+// still running; it waits for that kernel's completion with pdl_wait()
+// before it touches memory the stream's other kernels use.  The fused
+// forward's kernels are launched this way, so a decode step's six short
+// launches do not each pay the launch latency and set-up on the critical path.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Lightning indexer, CUDA-core version: any supported dtype/shape.
 cudaError_t launch_indexer_simt(const QueryBatch& qb, const CacheMap& cm, const dsa_indexer_inputs& ix,

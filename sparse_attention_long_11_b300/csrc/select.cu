@@ -63,7 +63,10 @@ sel_threshold_kernel(QueryBatch qb, const float* __restrict__ samp, int64_t lds,
   __shared__ uint32_t warp_tot[32];
   __shared__ TopkShared<kThrThreads> S;
   __shared__ uint32_t lo_min;
+  __shared__ uint32_t hk[kSelSampleTiles * 128];   // the row's sample score keys
   const int i = blockIdx.x, tid = threadIdx.x;
+  pdl_wait();
+  pdl_release();
   if (tid == 0) {
     cnt[i] = 0;
     if (i == 0) {
@@ -81,13 +84,17 @@ sel_threshold_kernel(QueryBatch qb, const float* __restrict__ samp, int64_t lds,
     if (tid == 0) thr[i] = 0ull;
     return;
   }
+  // the samples' score keys, converted once into shared memory for the
+  // select's passes (each reads every sample)
   const float* row = samp + (int64_t)i * lds;
+  for (int x = tid; x < slots; x += kThrThreads) hk[x] = score_key(__ldg(row + x));
+  __syncthreads();
   const uint64_t G = select_kth_u64<kThrThreads>(
       slots,
       [&](int x, uint64_t& v) {
         const int s = sample_key(x, m);
         if (s > pos) return false;
-        v = composite_key(row[x], s);
+        v = ((uint64_t)hk[x] << 32) | (uint64_t)(0xffffffffu - (uint32_t)s);
         return true;
       },
       (uint32_t)r, hist, warp_tot, S, &lo_min);
@@ -111,6 +118,8 @@ sel_select_kernel(QueryBatch qb, const float* __restrict__ samp, int64_t lds, in
   uint64_t* list = reinterpret_cast<uint64_t*>(dsm + kWinBits / 8);      // [list_cap] candidate keys
   __shared__ SelShared Z;
   const int i = blockIdx.x, tid = threadIdx.x;
+  pdl_wait();
+  pdl_release();
   int32_t* out = idx + (int64_t)i * k;
   const int pos = __ldg(qb.q_pos + i);
   if (pos < 0 || pos >= qb.max_kv) {
@@ -228,8 +237,8 @@ size_t select_shared_bytes(const SelectPlan& p) { return (size_t)kWinBits / 8 + 
 
 cudaError_t launch_sel_threshold(const QueryBatch& qb, const SelectPlan& p, const float* samp, int k, uint64_t* thr,
                                  uint32_t* cnt, uint32_t* fail_ctr, cudaStream_t stream) {
-  sel_threshold_kernel<<<qb.num_q, kThrThreads, 0, stream>>>(qb, samp, p.lds, p.m, k, thr, cnt, fail_ctr);
-  return cudaGetLastError();
+  return launch_pdl(sel_threshold_kernel, dim3(qb.num_q), dim3(kThrThreads), 0, stream, qb, samp, p.lds, p.m, k, thr,
+                    cnt, fail_ctr);
 }
 
 cudaError_t launch_sel_select(const QueryBatch& qb, const SelectPlan& p, const float* samp, int k, const uint64_t* thr,
@@ -238,9 +247,8 @@ cudaError_t launch_sel_select(const QueryBatch& qb, const SelectPlan& p, const f
   const int smem = (int)select_shared_bytes(p);
   cudaError_t e = cudaFuncSetAttribute(sel_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  sel_select_kernel<<<qb.num_q, kSelThreads, smem, stream>>>(qb, samp, p.lds, p.m, k, thr, cnt, cand, p.cap,
-                                                             p.list_cap, idx, fail_ctr, fail_rows, err);
-  return cudaGetLastError();
+  return launch_pdl(sel_select_kernel, dim3(qb.num_q), dim3(kSelThreads), (size_t)smem, stream, qb, samp, p.lds, p.m,
+                    k, thr, cnt, cand, p.cap, p.list_cap, idx, fail_ctr, fail_rows, err);
 }
 
 }  // namespace dsa

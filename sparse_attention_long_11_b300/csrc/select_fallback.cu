@@ -62,6 +62,8 @@ sel_fallback_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ FbShared S;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  pdl_release();
   if (tid == 0) S.row = next_row(fail_ctr, fail_rows);
   __syncthreads();
   if (S.row < 0) return;   // nothing queued for this CTA
@@ -234,9 +236,8 @@ cudaError_t launch_sel_fallback(const QueryBatch& qb, const CacheMap& cm, const 
   cudaError_t e =
       cudaFuncSetAttribute(sel_fallback_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
   if (e != cudaSuccess) return e;
-  sel_fallback_kernel<<<grid, kFbThreads, kSmemAlloc, stream>>>(tm_q, tm_k, qb, cm, ix.q_scale, ix.w, ix.k_scale, k,
-                                                                 idx, slots, ld, fail_ctr, fail_rows, err);
-  return cudaGetLastError();
+  return launch_pdl(sel_fallback_kernel, dim3(grid), dim3(kFbThreads), kSmemAlloc, stream, tm_q, tm_k, qb, cm,
+                    ix.q_scale, ix.w, ix.k_scale, k, idx, slots, ld, fail_ctr, fail_rows, err);
 }
 
 }  // namespace dsa
