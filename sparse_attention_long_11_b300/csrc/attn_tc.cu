@@ -166,37 +166,29 @@ __device__ __forceinline__ uint4 e4m3x8_scaled_bf16(uint2 c, float s) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Reductions over one head's 64 logits of a tile (two independent chains of
-// three-input min / max).
-__device__ __forceinline__ float abs_max64(const float (&x)[64]) {
-  float a = fabsf(x[0]), b = fabsf(x[32]);
+// Reductions over one head's 64 logits of a tile: four independent chains of
+// three-input min / max (eight steps each) and a final combine, so the
+// result is ready soon after the last input without holding many temporaries.
+template <bool kAbs, bool kMin>
+__device__ __forceinline__ float tree64(const float (&x)[64]) {
+  auto in = [&](int j) { return kAbs ? fabsf(x[j]) : x[j]; };
+  auto op = [](float p, float q, float r) { return kMin ? min3(p, q, r) : max3(p, q, r); };
+  float c[4];
 #pragma unroll
-  for (int j = 1; j < 31; j += 2) {
-    a = max3(a, fabsf(x[j]), fabsf(x[j + 1]));
-    b = max3(b, fabsf(x[32 + j]), fabsf(x[33 + j]));
-  }
-  return max3(a, b, fmaxf(fabsf(x[31]), fabsf(x[63])));
-}
-__device__ __forceinline__ float max64(const float (&x)[64]) {
-  float a = x[0], b = x[32];
+  for (int q = 0; q < 4; ++q) c[q] = in(16 * q);
 #pragma unroll
-  for (int j = 1; j < 31; j += 2) {
-    a = max3(a, x[j], x[j + 1]);
-    b = max3(b, x[32 + j], x[33 + j]);
-  }
-  return max3(a, b, fmaxf(x[31], x[63]));
+  for (int j = 1; j < 15; j += 2)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) c[q] = op(c[q], in(16 * q + j), in(16 * q + j + 1));
+#pragma unroll
+  for (int q = 0; q < 4; ++q) c[q] = kMin ? fminf(c[q], in(16 * q + 15)) : fmaxf(c[q], in(16 * q + 15));
+  return op(op(c[0], c[1], c[2]), c[3], c[3]);
 }
+__device__ __forceinline__ float abs_max64(const float (&x)[64]) { return tree64<true, false>(x); }
+__device__ __forceinline__ float max64(const float (&x)[64]) { return tree64<false, false>(x); }
 __device__ __forceinline__ void min_max64(const float (&x)[64], float& lo, float& hi) {
-  float mnA = x[0], mxA = x[0], mnB = x[32], mxB = x[32];
-#pragma unroll
-  for (int j = 1; j < 31; j += 2) {
-    mnA = min3(mnA, x[j], x[j + 1]);
-    mxA = max3(mxA, x[j], x[j + 1]);
-    mnB = min3(mnB, x[32 + j], x[33 + j]);
-    mxB = max3(mxB, x[32 + j], x[33 + j]);
-  }
-  lo = min3(mnA, mnB, fminf(x[31], x[63]));
-  hi = max3(mxA, mxB, fmaxf(x[31], x[63]));
+  lo = tree64<false, true>(x);
+  hi = tree64<false, false>(x);
 }
 
 // Adds the peer's partial logits of head h (row h of the received tile: 64
