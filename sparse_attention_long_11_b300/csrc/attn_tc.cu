@@ -111,19 +111,30 @@ struct Bars {
 // Tiles to process for one query: up to the last tile holding a valid entry
 // (0 <= s <= pos).  With prefix_valid (rows written by the top-k stage:
 // ascending, valid entries first) that is ceil(min(k, pos+1) / 64) without
-// reading the row; otherwise a full warp scans it.  Every role computes it
-// the same way.
-__device__ __forceinline__ int count_tiles(const int32_t* row, int k, int pos, bool prefix_valid) {
-  if (prefix_valid) return (min(k, pos + 1) + kNK - 1) / kNK;
+// reading the row; otherwise a full warp searches the row from its end in
+// blocks of 256 entries, so a row whose last block holds a valid entry (any
+// full selection) costs one round of loads.  Every role computes it the
+// same way (the search out of line: inlined into every role it costs
+// registers there).
+__device__ __noinline__ int search_tiles(const int32_t* row, int k, int pos) {
+  const int lane = threadIdx.x & 31;
   int last = -1;
-#pragma unroll 8
-  for (int j = threadIdx.x & 31; j < k; j += 32) {
-    const int s = __ldg(row + j);
-    if (s >= 0 && s <= pos) last = j;
-  }
+  for (int b = (k - 1) / 256 * 256; b >= 0 && last < 0; b -= 256) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+    for (int u = 0; u < 8; ++u) {
+      const int j = b + 32 * u + lane;
+      if (j < k) {
+        const int s = __ldg(row + j);
+        if (s >= 0 && s <= pos) last = j;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  }
   return last < 0 ? 0 : last / kNK + 1;
+}
+__device__ __forceinline__ int count_tiles(const int32_t* row, int k, int pos, bool prefix_valid) {
+  return prefix_valid ? (min(k, pos + 1) + kNK - 1) / kNK : search_tiles(row, k, pos);
 }
 
 struct QueryInfo {
@@ -553,21 +564,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
       // boxes of 64 (128 heads x 128 B, 128-byte swizzle); the rows of a
       // box are stored as whole lines instead of one 16-byte piece per head.
       uint8_t* stg = sm + kOffP + grp * kPBytes;
+      constexpr int kEpiLoads = kFp8Kv ? 1 : 2;   // 16-column TMEM loads per wait (registers allowing)
       bool eok = true;
 #pragma unroll 1
       for (int b = 0; b < 2 && eok; ++b) {
 #pragma unroll 1
-        for (int c = 0; c < 64; c += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem + lane_base + kTmemO + grp * 128 + 64 * b + c, r);
-          tmem_ld_wait();
+        for (int c = 0; c < 64; c += 16 * kEpiLoads) {
+          uint32_t r2[kEpiLoads][16];
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
+          for (int u = 0; u < kEpiLoads; ++u) tmem_ld16(tmem + lane_base + kTmemO + grp * 128 + 64 * b + c + 16 * u, r2[u]);
+          tmem_ld_wait();
+          auto r = [&](int j) { return r2[j >> 4][j & 15]; };
+#pragma unroll
+          for (int q = 0; q < 2 * kEpiLoads; ++q) {
             uint32_t w[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[8 * q + 2 * j]) * inv,
-                                                             __uint_as_float(r[8 * q + 2 * j + 1]) * inv);
+              const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r(8 * q + 2 * j)) * inv,
+                                                             __uint_as_float(r(8 * q + 2 * j + 1)) * inv);
               w[j] = *reinterpret_cast<const uint32_t*>(&v);
             }
             *reinterpret_cast<uint4*>(stg + sw128_offset(h, c / 8 + q)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -603,6 +617,38 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
     const uint32_t q_lane = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t g = 0, qv = 0, n_rope = 0;   // n_rope: rope TMA loads issued (warp 8, lane 0)
     if (warp == 8 && lane == 0) tma_prefetch_desc(&tm_q_rope);
+    // bf16 rows: this lane's entry s_e of tile gt -> 16-byte cp.async pieces
+    // of the warp's 32 rows in stage st (latent half, then rope quarter)
+    auto issue_bf16 = [&](int s_e, int qpos, int seq, int st) {
+      int row = -1;                                         // physical rows fit in 31 bits
+      if (s_e >= 0 && s_e <= qpos) row = (int)cache_row(cm, seq, s_e, err);
+      else if (s_e != -1) flag_error(err, DSA_ERR_BOUNDS);
+      const uint32_t sb = sKV + st * kKVStageBytes;
+      const __nv_bfloat16* kv = static_cast<const __nv_bfloat16*>(kv_raw);
+      const __nv_bfloat16* lat = kv + crank * 256 + lane * 8;
+      // one 32-bit broadcast per row; batches of 16 rows let the shuffles pipeline
+#pragma unroll
+      for (int b0 = 0; b0 < 32; b0 += 16) {
+        int rr[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) rr[j] = __shfl_sync(0xffffffffu, row, b0 + j);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          cp_async16(sb + (lane >> 3) * kKVSlotBytes + sw128_offset(32 * wg + b0 + j, lane & 7),
+                     rr[j] >= 0 ? lat + (int64_t)rr[j] * kDqk : kv, rr[j] >= 0 ? 16u : 0u);
+      }
+      {
+        const __nv_bfloat16* rope = kv + 512 + 32 * crank + (lane & 3) * 8;
+        int rr[4];
+#pragma unroll
+        for (int it = 0; it < 4; ++it) rr[it] = __shfl_sync(0xffffffffu, row, it * 8 + (lane >> 2));
+#pragma unroll
+        for (int it = 0; it < 4; ++it)   // rope halves: 8 rows x 4 chunks per instruction
+          cp_async16(sb + 4 * kKVSlotBytes + sw64_offset(32 * wg + it * 8 + (lane >> 2), lane & 3),
+                     rr[it] >= 0 ? rope + (int64_t)rr[it] * kDqk : kv, rr[it] >= 0 ? 16u : 0u);
+      }
+      cp_async_commit();
+    };
     int pos_next = ahead_ld(qb.q_pos, cluster, qb.num_q), seq_next = ahead_ld(qb.q_seq, cluster, qb.num_q);
     for (int i = cluster; i < qb.num_q && !*abort; i += ncl) {
       const int pos_i = pos_next, seq = seq_next;
@@ -611,6 +657,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
       const QueryInfo qi = query_info(qb, idx, k, i, pos_i, pv);
       if (qi.nt == 0) continue;
       const int32_t* irow = idx + (int64_t)i * k;
+      // A Q writer's first tile of this query, when its stage is already
+      // free: its copies go out before Q is written, so they land meanwhile
+      // instead of after it (the query's first tiles wait on both).
+      int t_pre = -1;
+      if (!kFp8Kv && q_writer) {
+        const int t1 = (grp - (int)(g % kGatherGroups) + kGatherGroups) % kGatherGroups;
+        if (t1 < qi.nt) {
+          const uint32_t g1 = g + t1;
+          const int st1 = g1 % kStages;
+          const bool free1 = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_test(&B.kv_empty[st1], ((g1 / kStages) & 1) ^ 1) : 0, 0) != 0;
+          if (free1) {
+            const int e = t1 * kNK + 32 * wg + lane;
+            const int s_e = e < k ? __ldg(irow + e) : -1;
+            issue_bf16(s_e, qi.pos, seq, st1);
+            t_pre = t1;
+          }
+        }
+      }
       // Q of this query: every S MMA of the previous query has completed
       if (q_writer && !mbar_wait_warp(&B.q_empty, (qv & 1) ^ 1, abort)) break;
       ATTN_TRACE(2, g, 6, warp == 8 && lane == 0);
@@ -654,6 +718,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
       bool ok = true;
       for (int t = 0; t < qi.nt; ++t, ++g) {
         if ((int)(g % kGatherGroups) != grp) continue;
+        if (t == t_pre) {
+          cp_async_wait_all();
+          fence_proxy_async_smem();
+          mbar_arrive(&B.kv_full[g % kStages]);
+          ATTN_TRACE(2, g, 2 + 3 * wg, lane == 0);
+          continue;
+        }
         // row of this lane's entry (loaded before the wait so the latency overlaps it)
         const int e = t * kNK + 32 * wg + lane;
         int s_e = -1;
@@ -718,34 +789,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
         }
         if (!(ok = mbar_wait_warp(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
         ATTN_TRACE(2, g, 1 + 3 * wg, lane == 0);
-        int row = -1;                                         // physical rows fit in 31 bits
-        if (s_e >= 0 && s_e <= qi.pos) row = (int)cache_row(cm, seq, s_e, err);
-        else if (s_e != -1) flag_error(err, DSA_ERR_BOUNDS);
-        const uint32_t sb = sKV + st * kKVStageBytes;
-        const __nv_bfloat16* kv = static_cast<const __nv_bfloat16*>(kv_raw);
-        const __nv_bfloat16* lat = kv + crank * 256 + lane * 8;
-        // one 32-bit broadcast per row; batches of 16 rows let the shuffles pipeline
-#pragma unroll
-        for (int b0 = 0; b0 < 32; b0 += 16) {
-          int rr[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) rr[j] = __shfl_sync(0xffffffffu, row, b0 + j);
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            cp_async16(sb + (lane >> 3) * kKVSlotBytes + sw128_offset(32 * wg + b0 + j, lane & 7),
-                       rr[j] >= 0 ? lat + (int64_t)rr[j] * kDqk : kv, rr[j] >= 0 ? 16u : 0u);
-        }
-        {
-          const __nv_bfloat16* rope = kv + 512 + 32 * crank + (lane & 3) * 8;
-          int rr[4];
-#pragma unroll
-          for (int it = 0; it < 4; ++it) rr[it] = __shfl_sync(0xffffffffu, row, it * 8 + (lane >> 2));
-#pragma unroll
-          for (int it = 0; it < 4; ++it)   // rope halves: 8 rows x 4 chunks per instruction
-            cp_async16(sb + 4 * kKVSlotBytes + sw64_offset(32 * wg + it * 8 + (lane >> 2), lane & 3),
-                       rr[it] >= 0 ? rope + (int64_t)rr[it] * kDqk : kv, rr[it] >= 0 ? 16u : 0u);
-        }
-        cp_async_commit();
+        issue_bf16(s_e, qi.pos, seq, st);
         cp_async_wait_all();
         fence_proxy_async_smem();
         mbar_arrive(&B.kv_full[st]);
@@ -754,7 +798,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
       if (!ok) break;
       ++qv;
     }
-    // the last rope TMA issued here has landed before the CTA may exit
+    // copies issued before an abort, and the last rope TMA issued here, have
+    // landed before the CTA may exit
+    cp_async_wait_all();
     if (warp == 8 && lane == 0 && n_rope > 0) mbar_wait_own(&B.q_rope, (n_rope - 1) & 1);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ score MMA issue (lane 0)
