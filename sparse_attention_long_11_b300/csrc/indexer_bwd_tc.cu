@@ -253,14 +253,14 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   //   decode  once the warp's copies have landed: this thread's row, decoded
   //           to fp16 (exact for e4m3) into row tid of the key tile, and its
   //           code norm.
-  auto locate = [&](int e0, int& row_out, float& sk_out) {
-    const int e = e0 + tid;
+  // The entry indices are loaded one tile ahead of locate (ld_idx), so
+  // that locate, which the next tile's copies wait on, starts from a value
+  // already in a register.
+  auto ld_idx = [&](int e0) { return e0 + tid < kk ? __ldg(irow + e0 + tid) : -1; };
+  auto locate = [&](int s, int& row_out, float& sk_out) {
     int64_t row = -1;
-    if (e < kk) {
-      const int s = __ldg(irow + e);
-      if (s >= 0 && s <= pos) row = cache_row(cm, seq, s, err);
-      else if (s != -1) flag_error(err, DSA_ERR_BOUNDS);
-    }
+    if (s >= 0 && s <= pos) row = cache_row(cm, seq, s, err);
+    else if (s != -1) flag_error(err, DSA_ERR_BOUNDS);
     row_out = (int)row;
     sk_out = row >= 0 ? __ldg(k_scale + row) : 0.f;
   };
@@ -317,15 +317,19 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   float smax = 0.f;   // largest key scale among valid entries (this thread)
   int row_n = -1;
   float sk_n = 0.f;
+  int s_n = -1;   // the next tile's entry index (this thread's)
   if (kk > 0) {
-    locate(0, row_n, sk_n);
+    locate(ld_idx(0), row_n, sk_n);
     stage(sG, row_n);
+    s_n = ld_idx(kTile);
   }
   for (int e0 = 0, it = 0; e0 < kk && ok; e0 += kTile, ++it) {
     const int row = row_n;
     const float sk = sk_n;
     if (e0 + kTile < kk) {   // the next tile's rows, in flight while this one computes
-      locate(e0 + kTile, row_n, sk_n);
+      const int s1 = s_n;
+      s_n = ld_idx(e0 + 2 * kTile);
+      locate(s1, row_n, sk_n);
       stage((it & 1) ? sG : sB, row_n);
       cp_async_wait_group1();
     } else {
@@ -452,8 +456,9 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   const float scG = fp16_scale(gmax * smax), scB = fp16_scale(gmax * wsmax);   // G, B scaled below 2^14
   __syncthreads();
   if (ok && kk > 0) {   // pass 2's first tile
-    locate(0, row_n, sk_n);
+    locate(ld_idx(0), row_n, sk_n);
     stage(sG, row_n);
+    s_n = ld_idx(kTile);
   }
 
   // ---------------------------------------------------------------- pass 2
@@ -505,25 +510,42 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
     });
     if (!ok) break;
     if (e0 + kTile < kk) {   // G has been read: stage the next tile there while dk is written
-      locate(e0 + kTile, row_n, sk_n);
+      const int s1 = s_n;
+      s_n = ld_idx(e0 + 2 * kTile);
+      locate(s1, row_n, sk_n);
       stage(sG, row_n);
     }
-    {   // dk of this entry's key row (the TMEM loads are warp-collective: every lane loads)
+    {   // dk of the warp's 32 entries' key rows.  The TMEM loads give each
+        // lane its own entry's dims; the warp's rows of B (free: the MMAs
+        // that read them have completed) transpose 32 dims at a time, so that
+        // each vector atomic instruction covers four whole 128-byte row pieces
+        // instead of one 16-byte piece of 32 rows.
       const bool add = row >= 0 && m != 0ull && ge != 0.f;
       const float inv = 1.f / scB;
-      float* dst = dk + (int64_t)(row >= 0 ? row : 0) * kDI;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_base + kTmemK + 16 * c, r);
+      uint8_t* tw = sm + kOffB + warp * 32 * 128;   // this warp's 32 rows x 128 B
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r2[2][16];
+        tmem_ld16(tmem + lane_base + kTmemK + 32 * c, r2[0]);
+        tmem_ld16(tmem + lane_base + kTmemK + 32 * c + 16, r2[1]);
         tmem_ld_wait();
-        if (add) {
 #pragma unroll
-          for (int u = 0; u < 16; u += 4)
-            atomicAdd(reinterpret_cast<float4*>(dst + 16 * c + u),
-                      make_float4(__uint_as_float(r[u]) * inv, __uint_as_float(r[u + 1]) * inv,
-                                  __uint_as_float(r[u + 2]) * inv, __uint_as_float(r[u + 3]) * inv));
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t* v = &r2[q >> 2][4 * (q & 3)];
+          *reinterpret_cast<float4*>(tw + sw128_offset(lane, q)) =
+              make_float4(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv, __uint_as_float(v[2]) * inv,
+                          __uint_as_float(v[3]) * inv);
         }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {   // entries 4i .. 4i+3 of the warp, 8 lanes x 16 B each
+          const int er = 4 * i + (lane >> 3);
+          const int rr = __shfl_sync(0xffffffffu, row, er);
+          const bool ad = __shfl_sync(0xffffffffu, add, er);
+          const float4 v = *reinterpret_cast<const float4*>(tw + sw128_offset(er, lane & 7));
+          if (ad) atomicAdd(reinterpret_cast<float4*>(dk + (int64_t)rr * kDI + 32 * c + 4 * (lane & 7)), v);
+        }
+        __syncwarp();
       }
     }
     tc_fence_before();
