@@ -367,31 +367,47 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
         amin = min3(amin, fabsf(__uint_as_float(r[u])), fabsf(__uint_as_float(r[u + 1])));
       amin = fminf(amin, fabsf(__uint_as_float(r[15])));
       const bool near = amin <= kb * qn_max;
+      if (!near) {
+        // no dot of the 16 lies within its bound: every sign is the fp32
+        // dot's (straight-line code, the same sums as the loop below)
+        uint32_t mc = 0u;
 #pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4) {
-        const float4 wq = wsq4[4 * c + u4];
-        const float wj[4] = {wq.x, wq.y, wq.z, wq.w};
+        for (int u4 = 0; u4 < 4; ++u4) {
+          const float4 wq = wsq4[4 * c + u4];
+          const float wj[4] = {wq.x, wq.y, wq.z, wq.w};
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          const int u = 4 * u4 + v, j = 16 * c + u;
-          float xv = __uint_as_float(r[u]);
-          bool posv = xv > 0.f;
-          if (near) {   // rare: the exact test of each head's bound
-            const float bound = kb * S.qn[j];
-            if (bound > 0.f && fabsf(xv) <= bound) {   // near zero: decide the sign exactly
-              if (np < kPend) {
-                S.pend_j[tid][np++] = (uint8_t)j;
-                continue;
-              }
-              const double exact = exact_code_dot(k8 + (int64_t)row * kDI, sm + kOffQ, j);
-              posv = exact > 0.0;
-              xv = (float)exact;
+          for (int v = 0; v < 4; ++v) {
+            const float xv = __uint_as_float(r[4 * u4 + v]);
+            if (xv > 0.f) {
+              mc |= 1u << (4 * u4 + v);
+              iv = fmaf(wj[v], xv, iv);
             }
           }
-          if (posv) {
-            m |= 1ull << j;
-            iv = fmaf(wj[v], xv, iv);
+        }
+        m |= (uint64_t)mc << (16 * c);
+        continue;
+      }
+#pragma unroll 1
+      for (int u = 0; u < 16; ++u) {   // rare: the exact test of each head's bound
+        const int j = 16 * c + u;
+        float xv = __uint_as_float(r[0]);
+#pragma unroll
+        for (int q = 1; q < 16; ++q)
+          if (q == u) xv = __uint_as_float(r[q]);
+        bool posv = xv > 0.f;
+        const float bound = kb * S.qn[j];
+        if (bound > 0.f && fabsf(xv) <= bound) {   // near zero: decide the sign exactly
+          if (np < kPend) {
+            S.pend_j[tid][np++] = (uint8_t)j;
+            continue;
           }
+          const double exact = exact_code_dot(k8 + (int64_t)row * kDI, sm + kOffQ, j);
+          posv = exact > 0.0;
+          xv = (float)exact;
+        }
+        if (posv) {
+          m |= 1ull << j;
+          iv = fmaf(S.wsq[j], xv, iv);
         }
       }
     }
