@@ -90,6 +90,7 @@ struct BwdShared {
   float qn_max;                 // the largest code norm |q8_j|
   float red[kThreads / 32];
   float dwp[kThreads / 32][kHI];
+  float skst[2][kThreads];      // each entry's key scale, copied with its tile's rows
   uint32_t tmem_base;
   int abort;
 };
@@ -257,12 +258,14 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   // that locate, which the next tile's copies wait on, starts from a value
   // already in a register.
   auto ld_idx = [&](int e0) { return e0 + tid < kk ? __ldg(irow + e0 + tid) : -1; };
-  auto locate = [&](int s, int& row_out, float& sk_out) {
+  // locate also starts the copy of the entry's key scale into skst[buf][tid]
+  // (zero for padding); it joins the tile's copy group, which stage commits.
+  auto locate = [&](int s, int& row_out, int buf) {
     int64_t row = -1;
     if (s >= 0 && s <= pos) row = cache_row(cm, seq, s, err);
     else if (s != -1) flag_error(err, DSA_ERR_BOUNDS);
     row_out = (int)row;
-    sk_out = row >= 0 ? __ldg(k_scale + row) : 0.f;
+    cp_async4(smem_u32(&S.skst[buf][tid]), row >= 0 ? k_scale + row : k_scale, row >= 0 ? 4u : 0u);
   };
   auto stage = [&](uint32_t stg, int row) {
 #pragma unroll
@@ -316,26 +319,25 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   // staging tiles: G's and B's space, free until pass 2, alternately
   float smax = 0.f;   // largest key scale among valid entries (this thread)
   int row_n = -1;
-  float sk_n = 0.f;
   int s_n = -1;   // the next tile's entry index (this thread's)
   if (kk > 0) {
-    locate(ld_idx(0), row_n, sk_n);
+    locate(ld_idx(0), row_n, 0);
     stage(sG, row_n);
     s_n = ld_idx(kTile);
   }
   for (int e0 = 0, it = 0; e0 < kk && ok; e0 += kTile, ++it) {
     const int row = row_n;
-    const float sk = sk_n;
     if (e0 + kTile < kk) {   // the next tile's rows, in flight while this one computes
       const int s1 = s_n;
       s_n = ld_idx(e0 + 2 * kTile);
-      locate(s1, row_n, sk_n);
+      locate(s1, row_n, (it + 1) & 1);
       stage((it & 1) ? sG : sB, row_n);
       cp_async_wait_group1();
     } else {
       cp_async_wait_all();
     }
     __syncwarp();
+    const float sk = S.skst[it & 1][tid];
     float kn;
     decode(sm + ((it & 1) ? kOffB : kOffG), kn);
     if (row >= 0) smax = fmaxf(smax, sk);
@@ -449,18 +451,32 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   const float Z = block_reduce(zp, S.red, false);
   const float logZ = logf(Z);
   float lpart = 0.f, gmax = 0.f;
-  for (int e = tid; e < kk; e += kThreads) {
-    const float iv = Ie[e];
-    float g = 0.f;
-    if (iv != -INFINITY) {
-      const float lpi = iv - M - logZ;
-      const float pe = __ldg(prow + e);
-      g = __expf(lpi) - pe;
-      if (pe > 0.f) lpart += pe * (logf(pe) - lpi);
+  // the targets come from global memory: eight loads in flight per thread,
+  // then the eight entries in the same order as one at a time
+  constexpr int kPB = 8;
+  for (int e8 = tid; e8 < kk; e8 += kPB * kThreads) {
+    float pv[kPB];
+#pragma unroll
+    for (int u = 0; u < kPB; ++u) {
+      const int e = e8 + u * kThreads;
+      pv[u] = e < kk ? __ldg(prow + e) : 0.f;
     }
-    Ie[e] = g;
-    gmax = fmaxf(gmax, fabsf(g));
-    if (grad_scores) grad_scores[(int64_t)t * kk + e] = g;
+#pragma unroll
+    for (int u = 0; u < kPB; ++u) {
+      const int e = e8 + u * kThreads;
+      if (e >= kk) break;
+      const float iv = Ie[e];
+      float g = 0.f;
+      if (iv != -INFINITY) {
+        const float lpi = iv - M - logZ;
+        const float pe = pv[u];
+        g = __expf(lpi) - pe;
+        if (pe > 0.f) lpart += pe * (logf(pe) - lpi);
+      }
+      Ie[e] = g;
+      gmax = fmaxf(gmax, fabsf(g));
+      if (grad_scores) grad_scores[(int64_t)t * kk + e] = g;
+    }
   }
   const float lsum = block_reduce(lpart, S.red, false);
   if (tid == 0) loss[t] = M == -INFINITY ? 0.f : lsum;
@@ -472,7 +488,7 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   const float scG = fp16_scale(gmax * smax), scB = fp16_scale(gmax * wsmax);   // G, B scaled below 2^14
   __syncthreads();
   if (ok && kk > 0) {   // pass 2's first tile
-    locate(ld_idx(0), row_n, sk_n);
+    locate(ld_idx(0), row_n, 0);
     stage(sG, row_n);
     s_n = ld_idx(kTile);
   }
@@ -483,9 +499,9 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
   // once this tile's MMAs have read G
   for (int e0 = 0; e0 < kk && ok; e0 += kTile) {
     const int row = row_n;
-    const float sk = sk_n;
     cp_async_wait_all();
     __syncwarp();
+    const float sk = S.skst[0][tid];
     float kn;
     decode(sm + kOffG, kn);
     const int e = e0 + tid;
@@ -528,7 +544,7 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
     if (e0 + kTile < kk) {   // G has been read: stage the next tile there while dk is written
       const int s1 = s_n;
       s_n = ld_idx(e0 + 2 * kTile);
-      locate(s1, row_n, sk_n);
+      locate(s1, row_n, 0);
       stage(sG, row_n);
     }
     {   // dk of the warp's 32 entries' key rows.  The TMEM loads give each

@@ -137,6 +137,10 @@ __device__ __forceinline__ bool mbar_wait_own(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+// 4-byte global->shared copy (through L1); src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
 // Arrive on `bar` once all of this thread's earlier cp.async copies landed
 // (counts as one of the barrier's expected arrivals).
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
