@@ -657,9 +657,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
       const QueryInfo qi = query_info(qb, idx, k, i, pos_i, pv);
       if (qi.nt == 0) continue;
       const int32_t* irow = idx + (int64_t)i * k;
-      // A Q writer's first tile of this query, when its stage is already
-      // free: its copies go out before Q is written, so they land meanwhile
-      // instead of after it (the query's first tiles wait on both).
+      // Q of this query: every S MMA of the previous query has completed
+      if (q_writer && !mbar_wait_warp(&B.q_empty, (qv & 1) ^ 1, abort)) break;
+      // A Q writer's first tile of this query, when its stage is free by now
+      // (the previous query's last P.V MMAs have mostly completed): its
+      // copies go out before Q is written and land meanwhile, instead of
+      // after it (the query's first tiles wait on both).
       int t_pre = -1;
       if (!kFp8Kv && q_writer) {
         const int t1 = (grp - (int)(g % kGatherGroups) + kGatherGroups) % kGatherGroups;
@@ -675,8 +678,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           }
         }
       }
-      // Q of this query: every S MMA of the previous query has completed
-      if (q_writer && !mbar_wait_warp(&B.q_empty, (qv & 1) ^ 1, abort)) break;
       ATTN_TRACE(2, g, 6, warp == 8 && lane == 0);
       if (warp == 8 && lane == 0) {
         mbar_arrive_expect_tx(&B.q_rope, kQRopeBytes);
