@@ -228,8 +228,14 @@ SelectPlan plan_select(int max_kv, int k) {
     cap = std::max<int64_t>(cap, (int64_t)std::ceil(want));
   }
   p.cap = (int)((cap + 63) & ~int64_t(63));
-  // the shared list holds the candidates and the samples >= G (at most r <= S)
-  p.list_cap = p.cap + (int)p.lds;
+  // The shared list holds the candidates and the samples >= G: exactly r of
+  // them, r = threshold_rank(S, n, k).  A row's S is at most n/m + 128, so
+  // f = S k / n < k/m + 128 =: F, and r <= ceil(F + 6 sqrt(F) + 16) (r grows
+  // with f); r <= S <= lds as well.  Sized to that bound instead of to all
+  // the samples, the list leaves room for three or four blocks an SM.
+  const double F = (double)k / p.m + 128.0;
+  const int64_t r_bound = std::min<int64_t>(p.lds, (int64_t)std::ceil(F + 6.0 * std::sqrt(F) + 16.0));
+  p.list_cap = p.cap + (int)r_bound;
   return p;
 }
 
