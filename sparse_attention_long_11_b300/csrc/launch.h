@@ -109,7 +109,8 @@ struct SelectPlan {
   int m;             // sample stride in key tiles
   int64_t lds;       // sample row length (floats): sampled tiles x 128
   int cap;           // candidate list capacity per row (composite keys)
-  int list_cap;      // the select kernel's shared list: cap + lds
+  int list_cap;      // the select kernel's shared list: cap + a bound on the samples >= the threshold
+  int win;           // positions per bitmap window of the ordered output (a multiple of 64)
 };
 SelectPlan plan_select(int max_kv, int k);
 size_t select_shared_bytes(const SelectPlan& p);

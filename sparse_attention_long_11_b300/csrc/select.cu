@@ -39,7 +39,7 @@ using namespace topk_core;
 
 constexpr int kThrThreads = 256;
 constexpr int kSelThreads = 512;
-constexpr int kWinBits = 1 << 17;   // positions per bitmap window of the ordered output (16 KiB)
+constexpr int kWinBits = 1 << 17;   // most positions per bitmap window of the ordered output (16 KiB)
 
 // Sample layout of query row i: sampled tile o (key tile o*m) holds keys
 // o*m*128 + j, j < 128, at samp[i*lds + o*128 + j].
@@ -111,11 +111,11 @@ struct SelShared {
 __global__ void __launch_bounds__(kSelThreads)
 sel_select_kernel(QueryBatch qb, const float* __restrict__ samp, int64_t lds, int m, int k,
                   const uint64_t* __restrict__ thr, const uint32_t* __restrict__ cnt,
-                  const uint64_t* __restrict__ cand, int cap, int list_cap, int32_t* __restrict__ idx,
+                  const uint64_t* __restrict__ cand, int cap, int list_cap, int win, int32_t* __restrict__ idx,
                   uint32_t* __restrict__ fail_ctr, uint32_t* __restrict__ fail_rows, int* err) {
   extern __shared__ __align__(16) unsigned char dsm[];
-  uint32_t* bm = reinterpret_cast<uint32_t*>(dsm);                        // [kWinBits / 32] position bitmap
-  uint64_t* list = reinterpret_cast<uint64_t*>(dsm + kWinBits / 8);      // [list_cap] candidate keys
+  uint32_t* bm = reinterpret_cast<uint32_t*>(dsm);                        // [win / 32] position bitmap
+  uint64_t* list = reinterpret_cast<uint64_t*>(dsm + win / 8);           // [list_cap] candidate keys
   __shared__ SelShared Z;
   const int i = blockIdx.x, tid = threadIdx.x;
   pdl_wait();
@@ -173,14 +173,14 @@ sel_select_kernel(QueryBatch qb, const float* __restrict__ samp, int64_t lds, in
   // positions marked in a bitmap, then written in order (one contiguous run
   // of words per thread, offsets from a block scan)
   if (tid == 0) Z.out_base = 0;
-  for (int w0 = 0; w0 < n; w0 += kWinBits) {
-    const int words = (min(kWinBits, n - w0) + 31) / 32;
+  for (int w0 = 0; w0 < n; w0 += win) {
+    const int words = (min(win, n - w0) + 31) / 32;
     for (int j = tid; j < words; j += kSelThreads) bm[j] = 0u;
     __syncthreads();
     for (int j = tid; j < total; j += kSelThreads) {
       const uint64_t v = list[j];
       const int p = composite_pos(v) - w0;
-      if (v >= T && p >= 0 && p < kWinBits) atomicOr(bm + (p >> 5), 1u << (p & 31));
+      if (v >= T && p >= 0 && p < win) atomicOr(bm + (p >> 5), 1u << (p & 31));
     }
     __syncthreads();
     const int per = (words + kSelThreads - 1) / kSelThreads;
@@ -236,10 +236,12 @@ SelectPlan plan_select(int max_kv, int k) {
   const double F = (double)k / p.m + 128.0;
   const int64_t r_bound = std::min<int64_t>(p.lds, (int64_t)std::ceil(F + 6.0 * std::sqrt(F) + 16.0));
   p.list_cap = p.cap + (int)r_bound;
+  // the bitmap covers a whole row when the cache is shorter than a window
+  p.win = (int)std::min<int64_t>(kWinBits, ((int64_t)max_kv + 63) & ~int64_t(63));
   return p;
 }
 
-size_t select_shared_bytes(const SelectPlan& p) { return (size_t)kWinBits / 8 + (size_t)p.list_cap * 8; }
+size_t select_shared_bytes(const SelectPlan& p) { return (size_t)p.win / 8 + (size_t)p.list_cap * 8; }
 
 cudaError_t launch_sel_threshold(const QueryBatch& qb, const SelectPlan& p, const float* samp, int k, uint64_t* thr,
                                  uint32_t* cnt, uint32_t* fail_ctr, cudaStream_t stream) {
@@ -254,7 +256,7 @@ cudaError_t launch_sel_select(const QueryBatch& qb, const SelectPlan& p, const f
   cudaError_t e = cudaFuncSetAttribute(sel_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(sel_select_kernel, dim3(qb.num_q), dim3(kSelThreads), (size_t)smem, stream, qb, samp, p.lds, p.m,
-                    k, thr, cnt, cand, p.cap, p.list_cap, idx, fail_ctr, fail_rows, err);
+                    k, thr, cnt, cand, p.cap, p.list_cap, p.win, idx, fail_ctr, fail_rows, err);
 }
 
 }  // namespace dsa
