@@ -79,21 +79,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 384;  // S buffer b at kTmemS + 64 b
 constexpr float kLn2 = 0.69314718055994530942f;
 
-// Optional per-tile timeline of the first CTA (build with -DDSA_ATTN_TRACE):
-// SM clock stamps per role (0 softmax, 1 exchange, 2 producer, 3 MMA), tile
-// and event, read back with dsa_attn_trace_read().
-#ifdef DSA_ATTN_TRACE
-__device__ long long g_attn_trace[4][512][8];
-#define ATTN_TRACE(role, tile, ev, cond)                                                   \
-  do {                                                                                    \
-    if ((cond) && blockIdx.x == 0 && (tile) < 512) g_attn_trace[role][tile][ev] = clock64(); \
-  } while (0)
-#else
-#define ATTN_TRACE(role, tile, ev, cond) \
-  do {                                   \
-  } while (0)
-#endif
-
 struct Bars {
   uint64_t kv_full[kStages], kv_empty[kStages], s_full[2], xf[2], xe[2];
   uint64_t s_empty[2], p_full[2], pv_done[2], mdone[2];
@@ -377,7 +362,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           s_e0 = e0 < k ? __ldg(irow + e0) : -1;
           s_e1 = e1 < k ? __ldg(irow + e1) : -1;
         }
-        ATTN_TRACE(grp, gt, 0, lane == 0 && q4 == 0);
         if (!(ok = mbar_wait_warp(&B.s_full[grp], par, abort))) break;
         tc_fence_after();
         // own partial logits, raw dots (the scale to base-2 units is applied
@@ -394,7 +378,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
         }
         tc_fence_before();
         mbar_arrive(&B.s_empty[grp]);   // S(gt+2) may be computed into this buffer
-        ATTN_TRACE(grp, gt, 1, lane == 0 && q4 == 0);
         // own partial -> the peer's X[grp], once the peer has consumed what we wrote there two tiles ago
         if (!(ok = mbar_wait_warp<true>(&B.xe[grp], par ^ 1, abort))) break;
         bool precise;   // this warp sent fixed point (warp-uniform)
@@ -438,12 +421,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           }
           st_async_v2_f32(x_peer + kXCodeBytes + (uint32_t)h * 8u, step, lo, xf_peer);
         }
-        ATTN_TRACE(grp, gt, 2, lane == 0 && q4 == 0);
         if (!(ok = mbar_wait_warp<true>(&B.xf[grp], par, abort))) break;   // the peer's partial is in X[grp]
         // arm the next phase: the peer writes X[grp] again only after all of
         // this group has read it and said so (below)
         if (gtid == 0) mbar_arrive_expect_tx(&B.xf[grp], kXBytes);
-        ATTN_TRACE(grp, gt, 3, lane == 0 && q4 == 0);
         uint32_t vm_lo, vm_hi;
         if (pv) {
           const int rem = n_valid - t * kNK;   // the valid entries of this tile form a prefix
@@ -467,7 +448,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
             if (!(((j < 32 ? vm_lo : vm_hi) >> (j & 31)) & 1u)) x[j] = -INFINITY;
         }
         const float mt = max64(x) * scale_log2;   // base-2 units
-        ATTN_TRACE(grp, gt, 6, lane == 0 && q4 == 0 && t < nt - 1);
         // X[grp] consumed: the store below needs mt, which depends on every
         // value loaded from X, and instructions issue in order, so the relaxed
         // arrive after it follows those loads (a release-ordered remote arrive
@@ -481,7 +461,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           if (!(ok = mbar_wait_warp(&B.mdone[grp ^ 1], ((gt - 1) >> 1) & 1, abort))) break;
           if (t > 0) m_prev = B.mpub[grp ^ 1][h];
         }
-        ATTN_TRACE(grp, gt, 7, lane == 0 && q4 == 0 && t < nt - 1);
         // lazy rescaling: the maximum used only moves when exceeded by more than 8 (a factor 256)
         const float m_use = mt > m_prev + 8.f ? mt : m_prev;
         B.mpub[grp][h] = m_use;
@@ -504,7 +483,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
         else probabilities<false>(x, scale_log2, msub, pk, ls, lrs);
         l += ls;
         lr += lrs;
-        ATTN_TRACE(grp, gt, 4, lane == 0 && q4 == 0);
         // The heads of a warp decide separately whether their maximum moved,
         // but the TMEM loads and stores are warp-collective: the warp rescales
         // when any of its heads needs it, the others by exactly 1.
@@ -537,7 +515,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&B.p_full[grp]);
-        ATTN_TRACE(grp, gt, 5, lane == 0 && q4 == 0);
       }
       g = g0 + nt;
       if (!ok) break;
@@ -550,7 +527,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
       B.mseen[qb2][grp][h] = m_seen;
       mbar_arrive(&B.qend);
       if (!mbar_wait_warp(&B.qend, qb2, abort)) break;
-      ATTN_TRACE(grp, g - 1, 6, lane == 0 && q4 == 0);
       const float ma = B.mseen[qb2][0][h], mb = B.mseen[qb2][1][h];
       const float mf = fmaxf(ma, mb);
       const float fa = mf == -INFINITY ? 0.f : ex2_approx(ma - mf), fb = mf == -INFINITY ? 0.f : ex2_approx(mb - mf);
@@ -600,7 +576,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
         eok = mbar_wait_warp(&B.ostg_free[grp], b, abort);
       }
       if (!eok) break;
-      ATTN_TRACE(grp, g - 1, 7, lane == 0 && q4 == 0);
       if (crank == 0 && grp == 0) lse[(int64_t)i * kH + h] = lt > 0.f ? (mf + log2f(lt)) * kLn2 : -INFINITY;
       tc_fence_before();
       mbar_arrive(&B.o_empty);
@@ -678,7 +653,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           }
         }
       }
-      ATTN_TRACE(2, g, 6, warp == 8 && lane == 0);
       if (warp == 8 && lane == 0) {
         mbar_arrive_expect_tx(&B.q_rope, kQRopeBytes);
         tma_load_2d(sQr, &tm_q_rope, 512 + 32 * crank, i * kH, &B.q_rope);
@@ -714,7 +688,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
         }
         tc_fence_before();
         mbar_arrive(&B.q_full);
-        ATTN_TRACE(2, g, 7, warp == 8 && lane == 0);
       }
       bool ok = true;
       for (int t = 0; t < qi.nt; ++t, ++g) {
@@ -723,14 +696,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           cp_async_wait_all();
           fence_proxy_async_smem();
           mbar_arrive(&B.kv_full[g % kStages]);
-          ATTN_TRACE(2, g, 2 + 3 * wg, lane == 0);
           continue;
         }
         // row of this lane's entry (loaded before the wait so the latency overlaps it)
         const int e = t * kNK + 32 * wg + lane;
         int s_e = -1;
         if (e < k) s_e = __ldg(irow + e);
-        ATTN_TRACE(2, g, 0 + 3 * wg, lane == 0);
         const int st = g % kStages;
         if constexpr (kFp8Kv) {
           // FP8 rows go through registers (8 codes = 8 bytes per lane and row
@@ -765,7 +736,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           load8(0, ca);
           load8(8, cb);
           if (!(ok = mbar_wait_warp(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
-          ATTN_TRACE(2, g, 1 + 3 * wg, lane == 0);
           store8(0, ca);
           load8(16, ca);
           store8(8, cb);
@@ -785,16 +755,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           }
           fence_proxy_async_smem();
           mbar_arrive(&B.kv_full[st]);
-          ATTN_TRACE(2, g, 2 + 3 * wg, lane == 0);
           continue;
         }
         if (!(ok = mbar_wait_warp(&B.kv_empty[st], ((g / kStages) & 1) ^ 1, abort))) break;
-        ATTN_TRACE(2, g, 1 + 3 * wg, lane == 0);
         issue_bf16(s_e, qi.pos, seq, st);
         cp_async_wait_all();
         fence_proxy_async_smem();
         mbar_arrive(&B.kv_full[st]);
-        ATTN_TRACE(2, g, 2 + 3 * wg, lane == 0);
       }
       if (!ok) break;
       ++qv;
@@ -819,15 +786,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
       const int nt = qi.nt;
       if (nt == 0) continue;
       if (!mbar_wait_warp(&B.q_full, qv & 1, abort) || !mbar_wait_warp(&B.q_rope, qv & 1, abort)) break;
-      ATTN_TRACE(3, g, 7, lane == 0);
       bool ok = true;
       for (int t = 0; t < nt; ++t, ++g) {
         const uint32_t st = g % kStages, sb = g & 1;
-        ATTN_TRACE(3, g, 0, lane == 0);
         if (!(ok = mbar_wait_warp(&B.kv_full[st], (g / kStages) & 1, abort))) break;
-        ATTN_TRACE(3, g, 1, lane == 0);
         if (!(ok = mbar_wait_warp(&B.s_empty[sb], ((g >> 1) & 1) ^ 1, abort))) break;
-        ATTN_TRACE(3, g, 2, lane == 0);
         tc_fence_after();
         if (lane == 0) {
           const uint32_t dS = tmem + kTmemS + 64 * sb;
@@ -850,7 +813,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           if (t == nt - 1) mma_commit(&B.q_empty);
         }
         __syncwarp();
-        ATTN_TRACE(3, g, 5, lane == 0);
       }
       if (!ok) break;
       ++qv;
@@ -871,9 +833,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
       if (nt == 0) continue;
       bool ok = true;
       for (int t = 0; t < nt; ++t, ++g) {
-        ATTN_TRACE(3, g, 3, lane == 0);
         if (!(ok = mbar_wait_warp(&B.p_full[g & 1], (g >> 1) & 1, abort))) break;
-        ATTN_TRACE(3, g, 4, lane == 0);
         // the epilogue of the previous query has read O
         if (t == 0 && !(ok = mbar_wait_warp(&B.o_empty, (qv & 1) ^ 1, abort))) break;
         tc_fence_after();
@@ -888,7 +848,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q_rope, const __grid_const
           mma_commit(&B.kv_empty[g % kStages]);
         }
         __syncwarp();
-        ATTN_TRACE(3, g, 6, lane == 0);
       }
       if (!ok) break;
       ++qv;
@@ -922,12 +881,6 @@ int sm_count() {
 }
 
 }  // namespace
-
-#ifdef DSA_ATTN_TRACE
-extern "C" __attribute__((visibility("default"))) int dsa_attn_trace_read(long long* out) {
-  return (int)cudaMemcpyFromSymbol(out, g_attn_trace, sizeof(g_attn_trace));
-}
-#endif
 
 cudaError_t launch_attn_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_attn_inputs& at, const int32_t* idx,
                            int k, bool prefix_valid, void* out, float* lse, int* err, cudaStream_t stream) {

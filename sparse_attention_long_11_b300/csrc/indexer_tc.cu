@@ -70,20 +70,6 @@ struct __align__(16) Shared {
 
 static_assert(offsetof(Shared, wq) % 16 == 0, "wq is read with 16-byte vector loads");
 
-// Optional per-tile timeline of CTA 0 (build with -DDSA_INDEXER_TRACE): SM
-// clock stamps per role (0 producer, 1 MMA, 2 epilogue), tile and event.
-#ifdef DSA_INDEXER_TRACE
-__device__ long long g_idx_trace[3][1024][4];
-#define IDX_TRACE(role, tile, ev, cond)                                                    \
-  do {                                                                                    \
-    if ((cond) && blockIdx.x == 0 && (tile) < 1024) g_idx_trace[role][tile][ev] = clock64(); \
-  } while (0)
-#else
-#define IDX_TRACE(role, tile, ev, cond) \
-  do {                                  \
-  } while (0)
-#endif
-
 // Which key tiles a launch processes (IndexerOut::mode): every tile (kFull),
 // the sampled tiles 0, m, 2m, ... (kSample), or all the others (kFilter).
 // A pass's tiles are numbered by ordinal o = 0, 1, ...; tile(o) maps an
@@ -329,9 +315,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           pass_range(G, p, c, ch, t0, t1);
           for (int t = t0; t < t1; ++t, ++g) {
             const int st = g % kStagesA;
-            IDX_TRACE(0, g, 0, true);
             if (!(ok = mbar_wait(&S.a_empty[st], ((g / kStagesA) & 1) ^ 1, abort, wait_limit))) break;
-            IDX_TRACE(0, g, 1, true);
             int64_t rows[2];
             uint32_t bytes = 0;
             const int tile = tmap.tile(t);
@@ -394,11 +378,8 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const uint32_t boff = bb * kBBytes;
         for (int t = t0; t < t1; ++t, ++g, ++dq) {
           const int st = g % kStagesA, b = dq & 1;
-          IDX_TRACE(1, g, 0, lane == 0);
           if (!(ok = mbar_wait_warp(&S.a_full[st], (g / kStagesA) & 1, abort, wait_limit))) break;
-          IDX_TRACE(1, g, 1, lane == 0);
           if (!(ok = mbar_wait_warp(&S.d_empty[b], ((dq >> 1) & 1) ^ 1, abort, wait_limit))) break;
-          IDX_TRACE(1, g, 2, lane == 0);
           tc_fence_after();
           if (lane == 0) {
             const Desc2 ad = desc2(sdesc(sA + st * kABytes, 16, 1024)), bd = desc2(sdesc(sB + boff, 16, 1024));
@@ -419,9 +400,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           entry_at(G, c, ch, e0 + u, p, t);
           const uint32_t boff = bb * kBBytes + (uni ? 0u : (uint32_t)G.pass_q[p] * (kHI * 128));
           const int st = g % kStagesA;
-          IDX_TRACE(1, g, 0, lane == 0);
           if (!(ok = mbar_wait_warp(&S.a_full[st], (g / kStagesA) & 1, abort, wait_limit))) break;
-          IDX_TRACE(1, g, 1, lane == 0);
           tc_fence_after();
           if (lane == 0) {
             const Desc2 ad = desc2(sdesc(sA + st * kABytes, 16, 1024)), bd = desc2(sdesc(sB + boff, 16, 1024));
@@ -494,15 +473,12 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
               key_ok = row >= 0;
               if (key_ok) sk = __ldg(k_scale + row);
             }
-            IDX_TRACE(2, dq, 0, et == 0);
             if (!(ok = mbar_wait_warp(&S.d_full[b], (dq >> 1) & 1, abort, wait_limit))) break;
-            IDX_TRACE(2, dq, 1, et == 0);
             tc_fence_after();
             const float acc = idx_epi::head_sum64(tmem + lane_base + 256 * b + uq * 64, wq4);
             emit<kMode>(out, qb, row_q, t, s, acc * sk, q_act && key_ok && s <= q_pos, thr, lane, stg, sbuf);
             tc_fence_before();
             mbar_arrive(&S.d_empty[b]);
-            IDX_TRACE(2, dq, 2, et == 0);
           }
         }
         for (int e0 = 0; e0 < ne && ok && !uni; e0 += per_d, ++dq) {
@@ -528,9 +504,7 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             key_ok = row >= 0;
             if (key_ok) sk = __ldg(k_scale + row);
           }
-          IDX_TRACE(2, dq, 0, et == 0);
           if (!(ok = mbar_wait_warp(&S.d_full[b], (dq >> 1) & 1, abort, wait_limit))) break;
-          IDX_TRACE(2, dq, 1, et == 0);
           tc_fence_after();
           if (mine) {
             // the same arithmetic as the shared pass, so a query's scores do
@@ -541,7 +515,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           }
           tc_fence_before();
           mbar_arrive(&S.d_empty[b]);
-          IDX_TRACE(2, dq, 2, et == 0);
         }
         if (!ok) break;
         if (kMode == IndexerOut::kFilter) stage_flush(out, stg, sbuf, lane);
@@ -589,12 +562,6 @@ int sm_count_here() {
 }
 
 }  // namespace
-
-#ifdef DSA_INDEXER_TRACE
-extern "C" __attribute__((visibility("default"))) int dsa_indexer_trace_read(long long* out) {
-  return (int)cudaMemcpyFromSymbol(out, g_idx_trace, sizeof(g_idx_trace));
-}
-#endif
 
 bool indexer_tc_supported(const CacheMap& cm, const dsa_indexer_inputs& ix) {
   if (ix.dtype != DSA_FP8_E4M3 || ix.heads != kHI || ix.dim != kDI) return false;
