@@ -12,17 +12,18 @@
 //     [256c, 256c+256): its TMEM holds O_c (256 columns), two S buffers
 //     (2 x 64) and the query's 256 latent dims of this CTA (128 columns of
 //     packed bf16), the A operand of the latent score MMAs.  Keeping Q out
-//     of shared memory frees room for three KV stages and removes 64 KB of
+//     of shared memory frees room for four KV stages and removes 64 KB of
 //     operand reads per tile from the shared-memory bandwidth.
 //   * The score contraction is split by dims: CTA c contracts latent dims
 //     [256c, 256c+256) and rope dims [512+32c, 512+32c+32) (288 of 576), so
 //     every KV byte is gathered exactly once per query, by one CTA.  The two
-//     partial logit tiles (base-2 units, rounded to fp16 to halve the
-//     distributed-shared-memory traffic, which moves only ~15-19 B/clk per
-//     SM) are exchanged; each CTA adds the peer's fp16 partial to its own
-//     fp32 one and runs the online softmax for its half of O.  The receive
-//     tiles are double buffered, so the exchange of tile g overlaps the MMAs
-//     of tile g+1.
+//     partial logit tiles (raw dots, as fp16, or as 16-bit fixed point over
+//     each head's range where a warp's partials are large) are exchanged:
+//     16-bit codes halve the distributed-shared-memory traffic, which moves
+//     only ~15 B/clk per SM each way.  Each CTA adds the peer's partial to
+//     its own fp32 one and runs the online softmax for its half of O.  The
+//     receive tiles are double buffered, so the exchange of tile g overlaps
+//     the MMAs of tile g+1.
 //   * Tiles of 64 selected keys, gathered with coalesced 16-byte cp.async
 //     (a warp moves 512 contiguous bytes of one row per instruction) into
 //     128B-swizzled latent slots and a 64B-swizzled rope half.  (TMA
