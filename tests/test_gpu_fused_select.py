@@ -101,3 +101,15 @@ def test_fused_selection_paged_decode_batch():
     assert api.dsa_check_device_error() == api.DSA_OK
     _, want = _staged(prob)
     assert torch.equal(idx, want)
+
+
+def test_fused_selection_full_size_decode():
+    """The decode workload at full size (64 sequences x 65536 cached rows, one
+    query each, k = 2048, sample stride 16): the streamed selection equals the
+    stand-alone stages' selection on every row."""
+    wd = inputs.make_decode(seed=64, device=DEV)
+    prob = api.Problem(wd)
+    idx, _, _ = run_forward(prob)
+    assert api.dsa_check_device_error() == api.DSA_OK
+    _, want = _staged(prob)
+    assert torch.equal(idx, want)
