@@ -77,11 +77,14 @@ def test_fused_selection_equals_topk_of_the_score_rows(case):
     assert torch.equal(out, out2) and torch.equal(lse, lse2)
 
 
-@pytest.mark.parametrize("L,k", [(3000, 100), (5000, 8192), (40000, 2048), (20000, 1)])
+@pytest.mark.parametrize("L,k", [(3000, 100), (5000, 8192), (40000, 2048), (20000, 1), (131072, 2048),
+                                 (131072, 8192)])
 def test_fused_selection_other_shapes(L, k):
     """Small and large k, every tile sampled (m = 1, L <= 4096), rows shorter
-    than k, and a long row (m = 10), decode-style single rows included."""
-    q_rows = (L - 600, L) if L > 20000 else None
+    than k, long rows (m = 10; m = 32 at L = 131072, whose 2^17 positions fill
+    the select kernel's position window exactly), decode-style single rows
+    included."""
+    q_rows = (L - 600, L) if 20000 < L < 100000 else ((L - 256, L) if L >= 100000 else None)
     wl = inputs.make_prefill(seed=62 + k, device=DEV, L=L, topk=k, q_rows=q_rows)
     prob = api.Problem(wl)
     idx, _, _ = run_forward(prob)
