@@ -21,8 +21,8 @@
 //           N = 64 heads, K = 128 dims, fp32 accumulate: each product is
 //           exact, the sum is an fp32 sum); per entry its I and the 64-bit
 //           head mask, a dot within 1e-5 |q_j| |k_e| of zero re-decided in
-//           fp64 (exact for e4m3 products; the fp32 sum errs by less than
-//           127 2^-24 |q_j| |k_e|);
+//           fp64 from the fp16 rows already in shared memory (exact for e4m3
+//           products; the fp32 sum errs by less than 127 2^-24 |q_j| |k_e|);
 //   then    pi, g, the loss; power-of-two scales that put G and B = g w m sq
 //           in fp16's normal range;
 //   pass 2  gather the tile again; write G and B (fp16, scaled) and run
@@ -83,7 +83,6 @@ struct BwdShared {
   uint64_t mma;
   uint8_t npend[kThreads];          // per entry of the tile: deferred exact decisions
   uint8_t pend_j[kThreads][kPend];  // ... their heads, ascending
-  int prow[kThreads];               // ... and the entry's physical key row
   float pend_x[kThreads][kPend];    // the exact dots (rounded to fp32)
   float qn[kHI], wv[kHI], sqv[kHI];
   alignas(16) float wsq[kHI];   // w_j sq_j
@@ -118,22 +117,26 @@ __device__ __forceinline__ float fp16_scale(float v) {
   return ldexpf(1.f, 14 - e);
 }
 
-// The exact dot of key row krow's 128 codes with head j of the query (fp16
-// rows in the 128B-swizzled halves at sq) in fp64: every product of two e4m3
-// values and every partial sum is exact in fp64 (the sum of 128 products
-// between 2^-18 and 448^2 needs at most 43 bits), so any order gives the
-// same value.  Here one warp computes it: lane l takes dims 4l .. 4l+3 and a
-// butterfly adds the lanes' sums.  Called by a whole warp.
-__device__ __forceinline__ double exact_code_dot_warp(const uint8_t* krow, const uint8_t* sq, int j, int lane) {
-  const uint2 f = e4m3x4_to_f16(__ldg(reinterpret_cast<const uint32_t*>(krow) + lane));
+// Four consecutive fp16 values, dims d0 .. d0+3 (d0 a multiple of 4), of row
+// r of a tile held as two 128B-swizzled halves of 64 dims, `half` bytes apart.
+__device__ __forceinline__ uint2 f16x4_at(const uint8_t* tile, uint32_t half, int r, int d0) {
+  return *reinterpret_cast<const uint2*>(tile + (d0 >> 6) * half + sw128_offset(r, (d0 & 63) >> 3) + 2 * (d0 & 7));
+}
+
+// The exact dot of row kr of the decoded key tile at sk (fp16, decoded
+// exactly from the row's e4m3 codes) with head j of the query (fp16 rows in
+// the 128B-swizzled halves at sq) in fp64: every product of two e4m3 values
+// and every partial sum is exact in fp64 (the sum of 128 products between
+// 2^-18 and 448^2 needs at most 43 bits), so any order gives the same value.
+// Here one warp computes it: lane l takes dims 4l .. 4l+3 and a butterfly
+// adds the lanes' sums.  Called by a whole warp.
+__device__ __forceinline__ double exact_code_dot_warp(const uint8_t* sk, int kr, const uint8_t* sq, int j, int lane) {
   const int d0 = 4 * lane;
-  const uint8_t* chunk = sq + (d0 >> 6) * kQHalf + sw128_offset(j, (d0 & 63) >> 3) + 2 * (d0 & 7);
-  const uint32_t qw0 = *reinterpret_cast<const uint32_t*>(chunk);
-  const uint32_t qw1 = *reinterpret_cast<const uint32_t*>(chunk + 4);
-  double acc = (double)f16_lo(f.x) * (double)f16_lo(qw0);
-  acc = fma((double)f16_hi(f.x), (double)f16_hi(qw0), acc);
-  acc = fma((double)f16_lo(f.y), (double)f16_lo(qw1), acc);
-  acc = fma((double)f16_hi(f.y), (double)f16_hi(qw1), acc);
+  const uint2 f = f16x4_at(sk, kKHalf, kr, d0), g = f16x4_at(sq, kQHalf, j, d0);
+  double acc = (double)f16_lo(f.x) * (double)f16_lo(g.x);
+  acc = fma((double)f16_hi(f.x), (double)f16_hi(g.x), acc);
+  acc = fma((double)f16_lo(f.y), (double)f16_lo(g.y), acc);
+  acc = fma((double)f16_hi(f.y), (double)f16_hi(g.y), acc);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   return acc;
@@ -141,19 +144,14 @@ __device__ __forceinline__ double exact_code_dot_warp(const uint8_t* krow, const
 
 // The same dot by one thread (an entry with more than kPend near-zero dots in
 // a tile: rare); kept out of line.
-__device__ __noinline__ double exact_code_dot(const uint8_t* krow, const uint8_t* sq, int j) {
+__device__ __noinline__ double exact_code_dot(const uint8_t* sk, int kr, const uint8_t* sq, int j) {
   double acc = 0.0;
-  const uint32_t* kw = reinterpret_cast<const uint32_t*>(krow);
-  for (int q = 0; q < kDI / 4; ++q) {   // dims 4q .. 4q + 3
-    const uint2 f = e4m3x4_to_f16(__ldg(kw + q));
-    const int d0 = 4 * q;
-    const uint8_t* chunk = sq + (d0 >> 6) * kQHalf + sw128_offset(j, (d0 & 63) >> 3) + 2 * (d0 & 7);
-    const uint32_t qw0 = *reinterpret_cast<const uint32_t*>(chunk);
-    const uint32_t qw1 = *reinterpret_cast<const uint32_t*>(chunk + 4);
-    acc = fma((double)f16_lo(f.x), (double)f16_lo(qw0), acc);
-    acc = fma((double)f16_hi(f.x), (double)f16_hi(qw0), acc);
-    acc = fma((double)f16_lo(f.y), (double)f16_lo(qw1), acc);
-    acc = fma((double)f16_hi(f.y), (double)f16_hi(qw1), acc);
+  for (int d0 = 0; d0 < kDI; d0 += 4) {
+    const uint2 f = f16x4_at(sk, kKHalf, kr, d0), g = f16x4_at(sq, kQHalf, j, d0);
+    acc = fma((double)f16_lo(f.x), (double)f16_lo(g.x), acc);
+    acc = fma((double)f16_hi(f.x), (double)f16_hi(g.x), acc);
+    acc = fma((double)f16_lo(f.y), (double)f16_lo(g.y), acc);
+    acc = fma((double)f16_hi(f.y), (double)f16_hi(g.y), acc);
   }
   return acc;
 }
@@ -389,13 +387,10 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
         m |= (uint64_t)mc << (16 * c);
         continue;
       }
-#pragma unroll 1
+#pragma unroll
       for (int u = 0; u < 16; ++u) {   // rare: the exact test of each head's bound
         const int j = 16 * c + u;
-        float xv = __uint_as_float(r[0]);
-#pragma unroll
-        for (int q = 1; q < 16; ++q)
-          if (q == u) xv = __uint_as_float(r[q]);
+        float xv = __uint_as_float(r[u]);
         bool posv = xv > 0.f;
         const float bound = kb * S.qn[j];
         if (bound > 0.f && fabsf(xv) <= bound) {   // near zero: decide the sign exactly
@@ -403,7 +398,7 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
             S.pend_j[tid][np++] = (uint8_t)j;
             continue;
           }
-          const double exact = exact_code_dot(k8 + (int64_t)row * kDI, sm + kOffQ, j);
+          const double exact = exact_code_dot(sm + kOffK, tid, sm + kOffQ, j);
           posv = exact > 0.0;
           xv = (float)exact;
         }
@@ -415,12 +410,11 @@ indexer_kl_bwd_tc_kernel(QueryBatch qb, CacheMap cm, const uint8_t* __restrict__
     }
     // the deferred dots: each warp decides its own entries' (a warp per dot)
     S.npend[tid] = (uint8_t)np;
-    S.prow[tid] = row;
     __syncwarp();
     for (uint32_t pm = __ballot_sync(0xffffffffu, np > 0); pm; pm &= pm - 1) {
       const int et = warp * 32 + __ffs(pm) - 1, n = S.npend[et];
       for (int q = 0; q < n; ++q) {
-        const double ex = exact_code_dot_warp(k8 + (int64_t)S.prow[et] * kDI, sm + kOffQ, S.pend_j[et][q], lane);
+        const double ex = exact_code_dot_warp(sm + kOffK, et, sm + kOffQ, S.pend_j[et][q], lane);
         if (lane == 0) S.pend_x[et][q] = ex > 0.0 ? (float)ex : 0.f;
       }
     }
