@@ -353,6 +353,30 @@ DSA_API dsa_status dsa_cache_append(const dsa_cache_desc* cache, int32_t num_tok
                                     void* kv_cache, float* kv_scale, dsa_stream_t stream);
 
 /*
+ * dsa_kv_dequant -- the bf16 values an FP8 latent cache stands for.
+ * DeepSeek-V3.2 summary card, "How DSA Works": full attention runs on the
+ * selected tokens' latent rows; with the FP8 cache of dsa_attn_inputs'
+ * DSA_FP8_E4M3 those rows are read as
+ *     out[r][c] = bf16(kv_scale[r] * code[r][c])   (the product in fp32,
+ *                                                    rounded once to nearest even)
+ * which are exactly the values dsa_sparse_attn and dsa_forward read for row r.
+ *
+ *   num_rows  rows to convert (0 enqueues nothing; at most 2^31 - 1)
+ *   kv        [num_rows, 576] uint8 e4m3 codes, 16-byte aligned
+ *   kv_scale  [num_rows] fp32 per-row scales, 4-byte aligned
+ *   out       [num_rows, 576] bf16, 16-byte aligned; must not overlap kv
+ *
+ * dsa_forward does this itself, into its workspace, when a call reads each
+ * cache row many times over (prefill) and the workspace holds num_rows *
+ * 1152 bytes: its attention then gathers bf16 rows instead of converting
+ * every gathered element, with the same results bit for bit.  No device
+ * error is recorded (every code has a value).  Invalid arguments return
+ * DSA_ERR_INVALID_ARG before anything runs.
+ */
+DSA_API dsa_status dsa_kv_dequant(int64_t num_rows, const void* kv, const float* kv_scale, void* out,
+                                  dsa_stream_t stream);
+
+/*
  * dsa_indexer_kl_backward -- the indexer's training step: its alignment loss
  * and the gradients of that loss.  News article on DeepSeek-V3.2,
  * continued-pre-training section: the indexer is trained with a

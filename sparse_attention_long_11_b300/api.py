@@ -86,6 +86,8 @@ _SIGS = {
                                         ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_void_p]),
+    "dsa_kv_dequant": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p]),
     "dsa_indexer_kl_backward": (ctypes.c_int, [_P(QueryDesc), _P(CacheDesc), _P(IndexerInputs), ctypes.c_void_p,
                                                ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
@@ -270,6 +272,18 @@ def dsa_cache_append(cache: CacheDesc, tok_seq: torch.Tensor, tok_pos: torch.Ten
                                   None if kv_cache is None else _ptr(kv_cache),
                                   None if kv_scale is None else _ptr(kv_scale), _stream(stream)),
            "dsa_cache_append")
+
+
+def dsa_kv_dequant(kv: torch.Tensor, kv_scale: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """The bf16 rows an FP8 latent cache stands for: out = bf16(kv_scale * code)
+    per row (kv uint8 [num_rows, 576], kv_scale fp32 [num_rows], out bf16
+    [num_rows, 576])."""
+    n = int(kv.shape[0])
+    if kv.dtype != torch.uint8 or kv_scale.dtype != torch.float32 or out.dtype != torch.bfloat16:
+        raise TypeError("dsa_kv_dequant: kv uint8, kv_scale float32, out bfloat16")
+    if tuple(out.shape) != tuple(kv.shape) or kv_scale.numel() != n:
+        raise ValueError("dsa_kv_dequant: shapes")
+    _check(lib().dsa_kv_dequant(n, _ptr(kv), _ptr(kv_scale), _ptr(out), _stream(stream)), "dsa_kv_dequant")
 
 
 def dsa_indexer_kl_backward(batch: QueryDesc, cache: CacheDesc, ix: IndexerInputs, idx: torch.Tensor, k: int,

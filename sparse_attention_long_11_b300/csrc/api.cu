@@ -160,6 +160,35 @@ cudaError_t launch(int stage, cudaStream_t st, F&& f) {
   return e;
 }
 
+// The forward's attention launch.  With an FP8 latent cache whose rows the
+// call reads many times over (a prefill chunk reads each cache row about
+// num_q * k / num_rows times), the whole cache is converted to bf16 once,
+// into the workspace (the selection's scratch is dead by then), and the bf16
+// attention runs on that copy: its gathers then move bf16 rows instead of
+// converting every element of every gathered row again.  The copy holds
+// exactly the values the FP8 gather stages, so the results are the same
+// bits.  Without room for the copy, or with little reuse (decode), the FP8
+// gather runs as it is.
+constexpr int64_t kKvCopyReuse = 4;   // row reads per cache row above which the copy pays
+cudaError_t launch_forward_attn(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_attn_inputs* at,
+                                const int32_t* idx, int32_t k, void* out, float* lse, void* ws, size_t ws_bytes,
+                                int* err, cudaStream_t st) {
+  const CacheMap cm = to_map(cd);
+  const size_t copy_bytes = (size_t)cd->num_rows * (size_t)at->d_qk * 2;
+  const int64_t reads = (int64_t)qd->num_q * std::min<int64_t>(k, qd->max_kv);
+  if (at->dtype == DSA_FP8_E4M3 && ws && copy_bytes <= ws_bytes && reads >= kKvCopyReuse * cd->num_rows) {
+    cudaError_t e =
+        launch(DSA_STAGE_ATTN, st, [&] { return launch_kv_dequant(at->kv, at->kv_scale, cd->num_rows, ws, st); });
+    if (e != cudaSuccess) return e;
+    dsa_attn_inputs bf = *at;
+    bf.dtype = DSA_BF16;
+    bf.kv = ws;
+    bf.kv_scale = nullptr;
+    return launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, bf, idx, k, out, lse, err, st, true); });
+  }
+  return launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); });
+}
+
 // The fused forward over validated arguments: the queries in stages of at
 // most max_rows score rows (as many as the scratch holds), each stage's
 // indexer scores written to `scores` and reduced to its top-k rows, then one
@@ -167,7 +196,7 @@ cudaError_t launch(int stage, cudaStream_t st, F&& f) {
 // so the last one is not a sliver.
 dsa_status run_staged(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix, int32_t k,
                       const dsa_attn_inputs* at, int32_t* idx, void* out, float* lse, float* scores,
-                      int64_t max_rows, int* err, cudaStream_t st) {
+                      int64_t max_rows, int* err, cudaStream_t st, size_t copy_bytes = 0) {
   const CacheMap cm = to_map(cd);
   const int64_t ld = score_ld(qd->max_kv);
   max_rows = std::max<int64_t>(1, std::min<int64_t>(max_rows, qd->num_q));
@@ -186,8 +215,10 @@ dsa_status run_staged(const dsa_query_desc* qd, const dsa_cache_desc* cd, const 
     e = launch(DSA_STAGE_TOPK, st, [&] { return launch_topk(qb, scores, ld, k, idx + r0 * k, err, st); });
     if (e != cudaSuccess) return DSA_ERR_CUDA;
   }
-  return cuda_status(
-      launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
+  // (the score rows are dead now: with copy_bytes > 0 their space may hold
+  // the bf16 copy of an FP8 latent cache)
+  return cuda_status(launch_forward_attn(qd, cd, at, idx, k, out, lse, copy_bytes ? scores : nullptr, copy_bytes,
+                                         err, st));
 }
 
 // ---- The fused forward: the selection streams out of the indexer, so no
@@ -323,8 +354,7 @@ dsa_status run_fused(const dsa_query_desc* qd, const dsa_cache_desc* cd, const d
     });
     if (e != cudaSuccess) return DSA_ERR_CUDA;
   }
-  return cuda_status(
-      launch(DSA_STAGE_ATTN, st, [&] { return launch_attn(to_batch(qd), cm, *at, idx, k, out, lse, err, st, true); }));
+  return cuda_status(launch_forward_attn(qd, cd, at, idx, k, out, lse, workspace, ws_bytes, err, st));
 }
 
 // Recommended bytes of the fused forward: every row of the call in one
@@ -476,7 +506,17 @@ dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const
   if (fused) return run_fused(qd, cd, ix, k, at, idx, out, lse, workspace, workspace_bytes, err, st);
 
   const int64_t rows = (int64_t)(workspace_bytes / (score_ld(qd->max_kv) * sizeof(float)));
-  return run_staged(qd, cd, ix, k, at, idx, out, lse, static_cast<float*>(workspace), rows, err, st);
+  return run_staged(qd, cd, ix, k, at, idx, out, lse, static_cast<float*>(workspace), rows, err, st,
+                    workspace_bytes);
+}
+
+dsa_status dsa_kv_dequant(int64_t num_rows, const void* kv, const float* kv_scale, void* out, dsa_stream_t stream) {
+  if (num_rows < 0 || num_rows > INT32_MAX) return DSA_ERR_INVALID_ARG;
+  if (num_rows == 0) return DSA_OK;
+  if (!kv || !kv_scale || !out || !aligned(kv, 16) || !aligned(kv_scale, 4) || !aligned(out, 16))
+    return DSA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(launch(DSA_STAGE_ATTN, st, [&] { return launch_kv_dequant(kv, kv_scale, num_rows, out, st); }));
 }
 
 dsa_status dsa_indexer_kl_backward(const dsa_query_desc* qd, const dsa_cache_desc* cd, const dsa_indexer_inputs* ix,

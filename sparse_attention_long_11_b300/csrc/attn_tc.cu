@@ -881,7 +881,33 @@ int sm_count() {
   return cache[dev];
 }
 
+// A whole FP8 latent cache as bf16: each thread converts groups of eight
+// codes of one row with the gather's own conversion (e4m3x8_scaled_bf16),
+// so the copy holds exactly the values the FP8 gather stages.  Groups are
+// strided over the grid; loads and stores are contiguous across a warp.
+__global__ void __launch_bounds__(256) kv_dequant_kernel(const uint8_t* __restrict__ kv8,
+                                                         const float* __restrict__ kv_scale, int64_t num_rows,
+                                                         __nv_bfloat16* __restrict__ out) {
+  constexpr int kGroups = kDqk / 8;   // 72 groups of eight codes a row
+  const int64_t n = num_rows * kGroups;
+  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < n; g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = g / kGroups;
+    const uint2 c = __ldg(reinterpret_cast<const uint2*>(kv8) + g);
+    reinterpret_cast<uint4*>(out)[g] = e4m3x8_scaled_bf16(c, __ldg(kv_scale + r));
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_dequant(const void* kv, const float* kv_scale, int64_t num_rows, void* out,
+                              cudaStream_t stream) {
+  if (num_rows <= 0) return cudaSuccess;
+  const int64_t groups = num_rows * (kDqk / 8);
+  const int64_t blocks = std::min<int64_t>((groups + 255) / 256, (int64_t)sm_count() * 8);
+  kv_dequant_kernel<<<(unsigned)blocks, 256, 0, stream>>>(static_cast<const uint8_t*>(kv), kv_scale, num_rows,
+                                                          static_cast<__nv_bfloat16*>(out));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_attn_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_attn_inputs& at, const int32_t* idx,
                            int k, bool prefix_valid, void* out, float* lse, int* err, cudaStream_t stream) {

@@ -139,6 +139,13 @@ cudaError_t launch_attn_tc(const QueryBatch& qb, const CacheMap& cm, const dsa_a
                            const int32_t* idx, int k, bool prefix_valid, void* out, float* lse, int* err,
                            cudaStream_t stream);
 
+// An FP8 latent cache (e4m3 codes [num_rows, 576], one fp32 scale per row)
+// converted to bf16 [num_rows, 576]: out = bf16(scale * code), exactly the
+// values the FP8 attention's gather stages.  A plain (not programmatic)
+// launch: it starts after all earlier work in the stream has finished.
+cudaError_t launch_kv_dequant(const void* kv, const float* kv_scale, int64_t num_rows, void* out,
+                              cudaStream_t stream);
+
 // Stage dispatch: the tensor-core kernel for the latent shape (bf16 or FP8
 // cache), the CUDA-core kernel for fp32 operands.
 inline cudaError_t launch_attn(const QueryBatch& qb, const CacheMap& cm, const dsa_attn_inputs& at,

@@ -79,6 +79,45 @@ def test_forward_fp8_kv_cache(kind):
     torch.cuda.empty_cache()
 
 
+def test_forward_fp8_kv_copy_equals_gather():
+    """An FP8 latent cache in a prefill: with room in the workspace the
+    forward converts the cache to bf16 once and runs the bf16 attention on
+    the copy; with a workspace too small for the copy it gathers the FP8 rows
+    directly.  Both give the same indices, outputs and LSE, bit for bit."""
+    torch.cuda.empty_cache()
+    wl = inputs.with_fp8_kv(inputs.make_prefill(seed=3, device=DEV, L=3000))
+    prob = api.Problem(wl)
+    qd, ix, at = prob.rows(0, wl.num_q)
+    cache = prob.cache.desc()
+    copy_bytes = wl.kv.shape[0] * 576 * 2
+    assert wl.num_q * wl.topk >= 4 * wl.kv.shape[0]                   # enough reuse for the copy
+    big = api.dsa_forward_workspace_size(qd, ix, wl.topk, at)
+    assert big >= copy_bytes
+    # the largest stage whose workspace cannot hold the copy
+    lo, hi = 1, wl.num_q
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if api.dsa_forward_stage_workspace_size(qd, ix, wl.topk, at, mid) < copy_bytes:
+            lo = mid
+        else:
+            hi = mid - 1
+    small = api.dsa_forward_stage_workspace_size(qd, ix, wl.topk, at, lo)
+    assert 0 < small < copy_bytes
+    res = []
+    for wsb in (big, small):
+        idx = torch.empty((wl.num_q, wl.topk), dtype=torch.int32, device=DEV)
+        out = torch.empty((wl.num_q, wl.H, wl.d_v), dtype=torch.bfloat16, device=DEV)
+        lse = torch.empty((wl.num_q, wl.H), dtype=torch.float32, device=DEV)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+        api.dsa_forward(qd, cache, ix, wl.topk, at, idx, out, lse, ws)
+        assert api.dsa_check_device_error() == api.DSA_OK
+        res.append((idx, out, lse))
+    (i1, o1, l1), (i2, o2, l2) = res
+    assert torch.equal(i1, i2) and torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+    del wl, prob, res
+    torch.cuda.empty_cache()
+
+
 def test_forward_128k_context():
     """A 131072-token prefill context (the long-context end of the sweep):
     the last 4096 queries, one bench-sized call, sampled rows vs the oracle."""

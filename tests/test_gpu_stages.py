@@ -220,6 +220,26 @@ def test_fp8_kv_attention_equals_bf16_attention_on_the_dequantised_cache():
     assert np.array_equal(o8, ob) and np.array_equal(l8, lb)
 
 
+def test_kv_dequant_equals_the_oracle():
+    """dsa_kv_dequant writes bf16(scale * code) for every code (both zeros,
+    subnormals, the largest finite values; NaN codes excluded) and scales
+    from tiny to large, bit for bit as the oracle's dequantisation."""
+    from oracle import dsa_oracle as ref
+    g = torch.Generator().manual_seed(11)
+    finite = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=torch.uint8)
+    n = 1000
+    codes = finite[torch.randint(0, finite.numel(), (n, 576), generator=g)]
+    codes[0] = finite[torch.arange(576) % finite.numel()]            # every finite code in one row
+    scale = torch.exp(torch.empty(n).uniform_(-30.0, 30.0, generator=g)).float()
+    scale[1], scale[2], scale[3] = 1.0, 2.0 ** -20, 2.0 ** 20
+    out = torch.empty((n, 576), dtype=torch.bfloat16, device=DEV)
+    api.dsa_kv_dequant(codes.to(DEV), scale.to(DEV), out)
+    got = out.float().cpu().numpy().astype(np.float64)
+    want = ref.dequantize_kv_e4m3(codes.numpy(), scale.numpy())
+    assert np.array_equal(got, want)
+    api.dsa_kv_dequant(codes[:0].to(DEV), scale[:0].to(DEV), out[:0])   # no rows: nothing to do
+
+
 def test_sparse_attn_skips_padding_and_any_order():
     wl = inputs.make_tiny(seed=8, device=DEV, L=128, topk=48)
     prob = api.Problem(wl)
