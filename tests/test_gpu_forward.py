@@ -79,13 +79,20 @@ def test_forward_fp8_kv_cache(kind):
     torch.cuda.empty_cache()
 
 
-def test_forward_fp8_kv_copy_equals_gather():
+@pytest.mark.parametrize("kind", ["contiguous", "paged"])
+def test_forward_fp8_kv_copy_equals_gather(kind):
     """An FP8 latent cache in a prefill: with room in the workspace the
     forward converts the cache to bf16 once and runs the bf16 attention on
     the copy; with a workspace too small for the copy it gathers the FP8 rows
-    directly.  Both give the same indices, outputs and LSE, bit for bit."""
+    directly.  Both give the same indices, outputs and LSE, bit for bit, for
+    a contiguous cache and for a paged pool (the copy keeps the physical row
+    numbering, so the block table applies to it unchanged)."""
     torch.cuda.empty_cache()
-    wl = inputs.with_fp8_kv(inputs.make_prefill(seed=3, device=DEV, L=3000))
+    if kind == "contiguous":
+        base = inputs.make_prefill(seed=3, device=DEV, L=3000)
+    else:
+        base = inputs.make_mixed(seed=4, device=DEV, batch=2, lengths=[3000, 2500], prefill=1024, decode=4)
+    wl = inputs.with_fp8_kv(base)
     prob = api.Problem(wl)
     qd, ix, at = prob.rows(0, wl.num_q)
     cache = prob.cache.desc()
