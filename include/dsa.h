@@ -268,7 +268,14 @@ DSA_API int64_t dsa_forward_stage_rows(const dsa_query_desc* qd, const dsa_index
  * holds: dsa_forward_stage_workspace_size() gives the bytes for a stage size
  * (1 row is the least; DSA_ERR_WORKSPACE below it) and
  * dsa_forward_workspace_size() the recommended size.  Any size gives the same
- * results; fewer, fuller stages run faster. */
+ * results; fewer, fuller stages run faster.
+ *
+ * With an FP8 latent cache (at->dtype DSA_FP8_E4M3), when the call reads each
+ * cache row at least 4 times on average (num_q * min(k, max_kv) >= 4 *
+ * num_rows: prefill chunks) and the workspace holds num_rows * 1152 bytes,
+ * the workspace is then reused for a bf16 copy of the whole cache
+ * (dsa_kv_dequant) and the attention runs on that copy instead of converting
+ * the rows in its gather; the results are the same bits either way. */
 DSA_API dsa_status dsa_forward(const dsa_query_desc* qd, const dsa_cache_desc* cd,
                        const dsa_indexer_inputs* ix, int32_t k, const dsa_attn_inputs* at,
                        int32_t* idx, void* out, float* lse,
