@@ -59,11 +59,22 @@ constexpr int kEpiThreads = 512;
 
 constexpr int kStageCap = 128;                  // candidates an epilogue warp stages before a flush (kFilter)
 
+// One group of 4 consecutive query rows: either one pass over a shared
+// sequence (uniform) or one pass per active query.
+struct Group {
+  int seq[kQG], pos[kQG];
+  bool active[kQG];
+  bool uniform;
+  int npass;
+  int pass_q[kQG], pass_seq[kQG], pass_T[kQG], pass_N[kQG], pass_maxpos[kQG];   // T tiles, N ordinals
+};
+
 struct __align__(16) Shared {
   uint64_t stage[kEpiThreads / 32][kStageCap];  // kFilter: each epilogue warp's admitted candidates
   uint64_t a_full[kStagesA], a_empty[kStagesA], d_full[2], d_empty[2];
   uint64_t b_full[2], b_empty[2], epi_sync[2], fin;
   alignas(16) float wq[2][kQG][kHI];   // w * q_scale of the item's group (double buffered; read as float4)
+  Group grp[2];                        // the epilogue's description of its current item (double buffered)
   uint32_t tmem_base;
   int abort;
 };
@@ -96,15 +107,6 @@ __host__ __device__ __forceinline__ uint32_t recip32(uint32_t d) {
   return d <= 1u ? 0u : (uint32_t)(0xffffffffull / d) + 1u;
 }
 
-// One group of 4 consecutive query rows: either one pass over a shared
-// sequence (uniform) or one pass per active query.
-struct Group {
-  int seq[kQG], pos[kQG];
-  bool active[kQG];
-  bool uniform;
-  int npass;
-  int pass_q[kQG], pass_seq[kQG], pass_T[kQG], pass_N[kQG], pass_maxpos[kQG];   // T tiles, N ordinals
-};
 
 template <class TM>
 __device__ __forceinline__ void describe_group(const QueryBatch& qb, const CacheMap& cm, int gi, int min_pos,
@@ -430,23 +432,28 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     Stager stg;
     uint64_t* sbuf = S.stage[warp - 2];
-    uint32_t dq = 0, j = 0;   // accumulator-buffer uses, items with tiles
+    uint32_t dq = 0, ep = 0;   // accumulator-buffer uses, items
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
       const int gi = item % ngroups, c = item / ngroups;
-      Group G;
-      describe_group(qb, cm, gi, out.min_pos, tmap, G);
-      if (item_tiles(G, c, ch) > 0) {
-        const int bb = j & 1;
-        {   // folded weights of this group (threads et < 256 fetch one each)
-          if (et < kQG * kHI) {
-            const int qq = et / kHI, jj = et % kHI, r = gi * kQG + qq;
-            S.wq[bb][qq][jj] = r < qb.num_q ? idx_epi::fold_weight(jj, __ldg(w + (int64_t)r * kHI + jj) *
-                                                                           __ldg(q_scale + (int64_t)r * kHI + jj))
-                                            : 0.f;
-          }
-          mbar_arrive(&S.epi_sync[bb]);
-          if (!mbar_wait_warp(&S.epi_sync[bb], (j >> 1) & 1, abort, wait_limit)) break;
+      const int bb = ep & 1;
+      {   // the item's description (one copy in shared memory for all epilogue
+          // threads, instead of one per thread in local memory) and the folded
+          // weights of its group (threads et < 256 fetch one each).  Slot bb
+          // is rewritten two items later, once every epilogue thread has
+          // passed the next item's barrier, i.e. finished with this item.
+        if (et == 0) describe_group(qb, cm, gi, out.min_pos, tmap, S.grp[bb]);
+        if (et < kQG * kHI) {
+          const int qq = et / kHI, jj = et % kHI, r = gi * kQG + qq;
+          S.wq[bb][qq][jj] = r < qb.num_q ? idx_epi::fold_weight(jj, __ldg(w + (int64_t)r * kHI + jj) *
+                                                                         __ldg(q_scale + (int64_t)r * kHI + jj))
+                                          : 0.f;
         }
+        mbar_arrive(&S.epi_sync[bb]);
+        if (!mbar_wait_warp(&S.epi_sync[bb], (ep >> 1) & 1, abort, wait_limit)) break;
+        ++ep;
+      }
+      const Group& G = S.grp[bb];
+      if (item_tiles(G, c, ch) > 0) {
         bool ok = true;
         const bool uni = G.uniform;
         const int ne = item_tiles(G, c, ch), per_d = uni ? 1 : 4;
@@ -518,7 +525,6 @@ indexer_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         if (!ok) break;
         if (kMode == IndexerOut::kFilter) stage_flush(out, stg, sbuf, lane);
-        ++j;
       }
       // the item holding a group's last chunk also writes -inf from the end
       // of the group's scanned tiles to max_kv
