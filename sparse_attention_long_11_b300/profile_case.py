@@ -3,7 +3,8 @@
     python -m sparse_attention_long_11_b300.profile_case --workload prefill --reps 2
 
 Workloads: tiny, prefill (L=4096), long (L=32768, 8 chunks), decode
-(64 x 65536), mixed (8 paged sequences).  With --kl-backward it runs, after
+(64 x 65536), mixed (8 paged sequences).  --fp8-kv stores the latent cache
+as FP8 (e4m3 codes and a scale per row).  With --kl-backward it runs, after
 the forward repetitions, the indexer's training step (dsa_indexer_kl_backward)
 on the selected entries with seeded synthetic targets, --reps times.
 Exits non-zero on a device error.
@@ -27,6 +28,7 @@ def main() -> int:
                     help="then run the indexer backward on the forward's selections, --reps times")
     ap.add_argument("--decode-batch", type=int, default=64,
                     help="sequences of the decode workload (65536 cached rows each)")
+    ap.add_argument("--fp8-kv", action="store_true", help="the latent cache stored as FP8")
     a = ap.parse_args()
     if a.q_rows and a.workload in ("prefill", "long"):
         r0, r1 = (int(x) for x in a.q_rows.split(":"))
@@ -36,6 +38,8 @@ def main() -> int:
         wl = inputs.make_decode(seed=a.seed, device="cuda", batch=a.decode_batch)
     else:
         wl = inputs.make_config(inputs.CONFIG_NAMES.index(a.workload), seed=a.seed, device="cuda")
+    if a.fp8_kv:
+        wl = inputs.with_fp8_kv(wl)
     prob = api.Problem(wl)
     idx = torch.empty((wl.num_q, wl.topk), dtype=torch.int32, device="cuda")
     out = torch.empty((wl.num_q, wl.H, wl.d_v), dtype=prob.out_dtype(), device="cuda")
